@@ -1,0 +1,250 @@
+/*
+ * mla_cache.h -- C ABI of libmla_cache, the GB300 (sm_103a) library for the
+ * MLA latent-KV data-movement path:
+ *
+ *   1. the grouped multi-layer cache insert ("PR #55356 [Kimi Perf] Group fp8
+ *      mla cache insertion", Implementation items 2-3 and Source snippets:
+ *      concat_and_cache_mla_grouped), optionally preceded by the per-layer
+ *      RMSNorm of kv_c and the RoPE rotation of k_pe that the DSpark drafter
+ *      applies before it ("PR #50585 [K3 Perf] Optimize k3 dspark fused kv",
+ *      Source snippets: _precompute_fused_context_kv);
+ *   2. the chunked-context K/V pack: gather of latent rows from the paged cache
+ *      with the conditional dtype cast, then the fused [k_nope | k_pe] key and V
+ *      pack ("PR #51772 [Attention][MLA] Fuse Kimi-K3 chunked-context K/V
+ *      packing", Implementation items 1-2 and Source snippets:
+ *      fused_mla_kv_concat / fused_mla_kv_concat_quant_fp8).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Ownership: the caller owns every buffer.  The library allocates no memory,
+ *   never synchronises the host with the device, and launches its kernels on
+ *   the stream it is given (NULL = the legacy default stream).  Every call
+ *   returns as soon as its launch is queued.
+ * - Pointers: every data pointer is a DEVICE pointer on the current CUDA
+ *   device unless the comment says otherwise.  The small metadata arrays
+ *   (per-layer cache pointers, slot mapping, scales, positions, tables) are
+ *   checked with cudaPointerGetAttributes; a host pointer there is rejected
+ *   with MLA_ERR_INVALID_ARG before any launch.
+ * - Strides and sizes are in ELEMENTS of the named tensor's element type.
+ * - Alignment: every row that is read or written must start on a 16-byte
+ *   boundary (base pointer and strides), else MLA_ERR_MISALIGNED.  There is no
+ *   unaligned fallback.
+ * - Outputs never alias inputs.
+ * - Errors: arguments are validated synchronously, before any launch, and the
+ *   call returns a status; the message of the last failure on the calling
+ *   thread is returned by mla_last_error().  A failed launch returns
+ *   MLA_ERR_CUDA.  Bad DATA found by a kernel (a slot or block id out of
+ *   range, a position outside the rotary table, a misaligned per-layer cache
+ *   pointer) never traps: the affected row is skipped (left untouched) and the
+ *   matching MLA_ERRBIT_* is OR-ed into *err_word when err_word is not NULL.
+ * - num_tokens == 0 returns MLA_OK and launches nothing.
+ * - Kernels are launched with programmatic dependent launch enabled (each
+ *   kernel waits for the previous grid on the stream before touching memory),
+ *   so back-to-back calls overlap launch latency; see mla_set_pdl().
+ */
+#ifndef MLA_CACHE_H
+#define MLA_CACHE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* mla_stream_t;
+
+/* Element formats of caches and outputs.  The vLLM cache-dtype strings map as
+ * "auto"/"bfloat16" -> MLA_BF16, "fp8"/"fp8_e4m3" -> MLA_FP8_E4M3,
+ * "fp8_e5m2" -> MLA_FP8_E5M2 ("PR #55356", Source snippets: the host dtype
+ * whitelist and the three template instances). */
+typedef enum { MLA_BF16 = 0, MLA_FP8_E4M3 = 1, MLA_FP8_E5M2 = 2 } mla_dtype_t;
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1, /* a null / inconsistent / host-side argument */
+  MLA_ERR_UNSUPPORTED = 2, /* a valid request this build does not implement */
+  MLA_ERR_MISALIGNED = 3,  /* a row would not start on a 16-byte boundary */
+  MLA_ERR_CUDA = 4         /* the CUDA runtime reported an error */
+} mla_status_t;
+
+/* Bits a kernel ORs into *err_word for data it skipped. */
+enum {
+  MLA_ERRBIT_SLOT_OOB = 1u,   /* slot >= num_blocks * block_size */
+  MLA_ERRBIT_BLOCK_OOB = 2u,  /* block table index or block id out of range */
+  MLA_ERRBIT_POS_OOB = 4u,    /* position outside [0, max_position) */
+  MLA_ERRBIT_MISALIGNED = 8u  /* a per-layer cache base not 16-byte aligned */
+};
+
+/* Map a vLLM kv-cache-dtype string to mla_dtype_t; -1 if it is not one of
+ * the five accepted strings.  Host only. */
+int mla_dtype_from_string(const char* kv_cache_dtype);
+
+/* Message of the last failed call on this thread ("" if none).  The pointer
+ * stays valid until the next call on the same thread. */
+const char* mla_last_error(void);
+
+/* Library version string, e.g. "mla_cache 1.0 sm_103a". */
+const char* mla_version(void);
+
+/* Enable (1, the default) or disable (0) programmatic dependent launch for
+ * every later launch from this process.  Returns the previous setting. */
+int mla_set_pdl(int enable);
+
+/*
+ * Optional pre-processing of the grouped insert ("PR #50585", Source snippets:
+ * ops.rms_norm with a [L, kv_lora_rank] weight, then the rotary embedding with
+ * the token positions repeated for every layer).  Pass NULL for a raw insert.
+ *
+ *   gamma               bf16 [L, kv_lora_rank], layer l's row at
+ *                       l * gamma_layer_stride; NULL = no RMSNorm.
+ *                       y = x / sqrt(mean(x^2) + eps) * gamma[l], in fp32,
+ *                       rounded to bf16 (round to nearest even).
+ *   eps                 RMSNorm epsilon (>= 0).
+ *   positions           int64 [num_tokens], the same for every layer;
+ *                       NULL = no RoPE.
+ *   cos_sin_cache       fp32 [max_position, pe_dim]; row p = cos(p f_i) for
+ *                       i < pe_dim/2 then sin(p f_i) (see
+ *                       mla_rope_cos_sin_cache).  Neox pairing: element i
+ *                       rotates with element i + pe_dim/2; the result is
+ *                       rounded to bf16.
+ *   max_position        rows of cos_sin_cache; a position outside
+ *                       [0, max_position) skips the row (MLA_ERRBIT_POS_OOB).
+ * The rounded bf16 values are what the fp8 conversion then divides by k_scale.
+ */
+typedef struct {
+  const void* gamma;
+  int64_t gamma_layer_stride;
+  float eps;
+  const int64_t* positions;
+  const float* cos_sin_cache;
+  int64_t max_position;
+} mla_norm_rope_t;
+
+/*
+ * Grouped multi-layer MLA cache insert, all layers in ONE launch
+ * ("PR #55356 [Kimi Perf] Group fp8 mla cache insertion", Source snippets:
+ * concat_and_cache_mla_grouped_kernel and its host function; the result must
+ * equal one single-layer insert per layer, test_concat_and_cache_mla_grouped).
+ *
+ * For every layer l < num_layers and token t < num_tokens:
+ *   s = slot_mapping[l * slot_layer_stride + t]      (slot_layer_stride 0 =
+ *       one mapping shared by all layers); s < 0 is padding and is skipped;
+ *   row = [kv_c[l, t, 0:kv_lora_rank] | k_pe[l, t, 0:pe_dim]]   (bf16),
+ *       after the optional RMSNorm / RoPE of norm_rope;
+ *   cache_l = (element type*) kv_cache_ptrs[l];
+ *   cache_l[(s / block_size) * block_stride + (s % block_size) * entry_stride
+ *           + i] = row[i]                 for a bf16 cache (the bf16 bits), or
+ *           = fp8(float(row[i]) / kv_scales[l])  for an fp8 cache, with
+ *           round-to-nearest-even and saturation to +-max (448 for e4m3, 57344
+ *           for e5m2), the quotient an IEEE fp32 division.
+ *
+ *   kv_c, k_pe          bf16; element (l, t, i) at l * layer_stride +
+ *                       t * token_stride + i.  Both [L, T, .] layer-major
+ *                       buffers and the DSpark projection output [T, L, 576]
+ *                       (kv_c = base, k_pe = base + 512) are accepted as is.
+ *   kv_lora_rank, pe_dim  must be 512 and 64 (else MLA_ERR_UNSUPPORTED).
+ *   slot_mapping        int64 device array.
+ *   kv_cache_ptrs       int64 device array [num_layers] of cache base
+ *                       addresses (each 16-byte aligned).
+ *   kv_scales           fp32 device array [num_layers]: required for an fp8
+ *                       cache, must be NULL for a bf16 cache.
+ *   num_blocks, block_size, block_stride, entry_stride
+ *                       the paged layout shared by every layer's cache
+ *                       (elements of the cache type).
+ *   norm_rope           NULL, or the optional RMSNorm / RoPE (above).
+ *   err_word            NULL, or a device uint32 that receives MLA_ERRBIT_*.
+ * Valid slots must be distinct within a layer (else the row written last is
+ * unspecified).
+ */
+mla_status_t mla_cache_insert_grouped(
+    const void* kv_c, int64_t kvc_token_stride, int64_t kvc_layer_stride,
+    const void* k_pe, int64_t kpe_token_stride, int64_t kpe_layer_stride,
+    int32_t num_tokens, int32_t num_layers, int32_t kv_lora_rank, int32_t pe_dim,
+    const int64_t* slot_mapping, int64_t slot_layer_stride, const int64_t* kv_cache_ptrs,
+    const float* kv_scales, mla_dtype_t cache_dtype, int64_t num_blocks, int32_t block_size,
+    int64_t block_stride, int64_t entry_stride, const mla_norm_rope_t* norm_rope,
+    uint32_t* err_word, mla_stream_t stream);
+
+/*
+ * Gather latent rows of context chunks from a paged cache, with the optional
+ * exact widening fp8 -> bf16 ("PR #51772", Implementation item 2:
+ * _gather_context_latent, then the conditional .to() of item 5; no scale is
+ * applied, a plain fp8 gather returns fp8).
+ *
+ * Sequence s < num_seqs owns output rows [cu_chunk_lens[s], cu_chunk_lens[s+1]);
+ * output row i of sequence s holds context position
+ *   p = chunk_starts[s] + (i - cu_chunk_lens[s]),
+ * stored in block blk = block_table[s * block_table_stride + p / block_size]
+ * at offset p % block_size:
+ *   out[i * out_row_stride + e] = cache[blk * block_stride +
+ *                                       (p % block_size) * entry_stride + e],
+ * for e < entry_dim, copied raw (out_dtype == cache_dtype) or widened exactly
+ * to bf16 (cache fp8, out_dtype MLA_BF16).
+ *
+ *   block_table         int32 device [num_seqs, block_table_stride]; the row
+ *                       width is block_table_stride.  A table index outside
+ *                       the row or a block id outside [0, num_blocks) skips the
+ *                       output row (MLA_ERRBIT_BLOCK_OOB).
+ *   cu_chunk_lens       int32 device [num_seqs + 1], non-decreasing.
+ *   chunk_starts        int32 device [num_seqs].
+ *   num_tokens          output rows; rows owned by no sequence are untouched.
+ */
+mla_status_t mla_context_gather(
+    const void* kv_cache, mla_dtype_t cache_dtype, int64_t num_blocks, int32_t block_size,
+    int64_t block_stride, int64_t entry_stride, int32_t entry_dim, const int32_t* block_table,
+    int64_t block_table_stride, const int32_t* cu_chunk_lens, const int32_t* chunk_starts,
+    int32_t num_seqs, int32_t num_tokens, void* out, int64_t out_row_stride,
+    mla_dtype_t out_dtype, uint32_t* err_word, mla_stream_t stream);
+
+/*
+ * Chunked-context K/V pack: one launch writes the contiguous full key
+ * [k_nope | k_pe] and V from the strided kv_b_proj output and a k_pe that may
+ * still be in the fp8 cache layout ("PR #51772", Source snippets:
+ * fused_mla_kv_concat and fused_mla_kv_concat_quant_fp8; Implementation item 1:
+ * strided inputs, k_pe broadcast over heads, fp8 cast by the native pairwise
+ * converters, capped grid with a grid-stride loop).
+ *
+ *   key_out[t, h, i]          = conv(k_nope[t, h, i])        i < nope_dim
+ *   key_out[t, h, nope_dim+j] = kpe(k_pe[t, j])               j < rope_dim
+ *   v_out[t, h, i]            = conv(v[t, h, i])              i < v_dim
+ * with conv = identity for MLA_BF16 output and
+ * fp8(float(e) / *out_scale) (round to nearest even, saturating) for fp8
+ * output; kpe = conv for a bf16 k_pe, the raw byte for an fp8 k_pe into an fp8
+ * key of the same format (no rescale), and the exact unscaled widening for an
+ * fp8 k_pe into a bf16 key.
+ *
+ *   k_nope, v           bf16, element (t, h, i) at t * token_stride +
+ *                       h * head_stride + i (e.g. the two halves of a
+ *                       [T, H, nope + v] kv_b_proj output, row stride 4160).
+ *   k_pe                [T, rope_dim] with row stride kpe_token_stride, of type
+ *                       kpe_dtype (bf16 or the cache's fp8).
+ *   nope_dim, rope_dim, v_dim  must be 128, 64, 128 (else UNSUPPORTED).
+ *   key_out             contiguous [T, H, nope_dim + rope_dim] of out_dtype.
+ *   v_out               contiguous [T, H, v_dim] of out_dtype, or NULL = no V.
+ *   out_scale           device fp32 scalar for fp8 output (NULL = 1.0); must be
+ *                       NULL for bf16 output.
+ */
+mla_status_t mla_context_kv_pack(
+    const void* k_nope, int64_t kn_token_stride, int64_t kn_head_stride, const void* v,
+    int64_t v_token_stride, int64_t v_head_stride, const void* k_pe, int64_t kpe_token_stride,
+    mla_dtype_t kpe_dtype, int32_t num_tokens, int32_t num_heads, int32_t nope_dim,
+    int32_t rope_dim, int32_t v_dim, void* key_out, void* v_out, mla_dtype_t out_dtype,
+    const float* out_scale, mla_stream_t stream);
+
+/*
+ * Fill the rotary cos/sin table the insert's RoPE reads ("PR #50585", Source
+ * snippets: the k_pe rotation; the table is the rotary embedding's cached
+ * cos/sin): out[p * rot_dim + i] = cos(p * base^(-2i/rot_dim)) and
+ * out[p * rot_dim + rot_dim/2 + i] = sin(same), for p < max_position and
+ * i < rot_dim/2, evaluated in double precision and rounded to fp32.
+ *   out  fp32 device [max_position, rot_dim], 16-byte aligned; rot_dim even.
+ */
+mla_status_t mla_rope_cos_sin_cache(float* out, int64_t max_position, int32_t rot_dim,
+                                    double base, mla_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MLA_CACHE_H */

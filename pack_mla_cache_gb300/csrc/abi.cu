@@ -1,0 +1,381 @@
+// abi.cu -- the extern "C" entry points of libmla_cache (include/mla_cache.h):
+// argument validation, conversion of element strides to byte strides, and
+// dispatch to the template instance of each kernel.
+//
+// Validation follows the host checks of the grouped insert ("PR #55356 [Kimi
+// Perf] Group fp8 mla cache insertion", Source snippets: the dtype whitelist,
+// "FP8 ... requires kv_scales", "BF16 ... does not use kv_scales", scales on
+// the same CUDA device) and adds the alignment and layout checks that the
+// vectorised kernels need.  Every check that needs no CUDA call runs first, so
+// an invalid call is rejected identically on a machine without a GPU.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <atomic>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "mla_cache.h"
+#include "mla_device.cuh"
+#include "mla_internal.h"
+
+namespace {
+
+thread_local std::string g_err;
+std::atomic<int> g_pdl{1};
+
+mla_status_t fail(mla_status_t st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return st;
+}
+
+inline bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool m16(int64_t bytes) { return (bytes & 15) == 0; }
+inline bool valid_dtype(int d) { return d == MLA_BF16 || d == MLA_FP8_E4M3 || d == MLA_FP8_E5M2; }
+inline int elt_size(int d) { return d == MLA_BF16 ? 2 : 1; }
+inline int log2_exact(int64_t v) {
+  if (v <= 0 || (v & (v - 1))) return -1;
+  int s = 0;
+  while ((int64_t(1) << s) < v) ++s;
+  return s;
+}
+
+// The pointer must be device (or managed) memory of the current device.
+mla_status_t check_device_ptr(const void* p, const char* name) {
+  cudaPointerAttributes attr;
+  cudaError_t e = cudaPointerGetAttributes(&attr, p);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return fail(MLA_ERR_CUDA, "%s: cudaPointerGetAttributes failed: %s", name,
+                cudaGetErrorString(e));
+  }
+  if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+    return fail(MLA_ERR_INVALID_ARG, "%s must be device memory on the same CUDA device", name);
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return fail(MLA_ERR_CUDA, "cudaGetDevice failed");
+  }
+  if (attr.device != dev)
+    return fail(MLA_ERR_INVALID_ARG,
+                "%s must be on the same CUDA device as the launch (it is on device %d, the "
+                "current device is %d)",
+                name, attr.device, dev);
+  return MLA_OK;
+}
+
+mla_status_t launched(cudaError_t e, const char* what) {
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return fail(MLA_ERR_CUDA, "%s: launch failed: %s", what, cudaGetErrorString(e));
+  }
+  return MLA_OK;
+}
+
+mla::LaunchCfg cfg_for(mla_stream_t stream) {
+  return mla::LaunchCfg{reinterpret_cast<cudaStream_t>(stream), g_pdl.load() != 0};
+}
+
+#define MLA_TRY(expr)                  \
+  do {                                 \
+    mla_status_t st_ = (expr);         \
+    if (st_ != MLA_OK) return st_;     \
+  } while (0)
+
+}  // namespace
+
+namespace mla {
+
+int capped_grid(const void* kernel, int threads, int64_t work_ctas) {
+  struct Entry {
+    int dev;
+    const void* kernel;
+    int threads;
+    int resident;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> cache;
+  int dev = 0;
+  (void)cudaGetDevice(&dev);
+  int resident = 0;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    for (const Entry& e : cache)
+      if (e.dev == dev && e.kernel == kernel && e.threads == threads) resident = e.resident;
+    if (resident == 0) {
+      int sms = 0, occ = 0;
+      (void)cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      (void)cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, threads, 0);
+      (void)cudaGetLastError();
+      resident = (sms > 0 ? sms : 1) * (occ > 0 ? occ : 1);
+      cache.push_back(Entry{dev, kernel, threads, resident});
+    }
+  }
+  if (work_ctas < 1) work_ctas = 1;
+  return static_cast<int>(work_ctas < resident ? work_ctas : resident);
+}
+
+}  // namespace mla
+
+extern "C" {
+
+int mla_dtype_from_string(const char* s) {
+  if (!s) return -1;
+  if (!strcmp(s, "auto") || !strcmp(s, "bfloat16")) return MLA_BF16;
+  if (!strcmp(s, "fp8") || !strcmp(s, "fp8_e4m3")) return MLA_FP8_E4M3;
+  if (!strcmp(s, "fp8_e5m2")) return MLA_FP8_E5M2;
+  return -1;
+}
+
+const char* mla_last_error(void) { return g_err.c_str(); }
+
+const char* mla_version(void) { return "mla_cache 1.0 sm_103a"; }
+
+int mla_set_pdl(int enable) { return g_pdl.exchange(enable ? 1 : 0); }
+
+mla_status_t mla_cache_insert_grouped(
+    const void* kv_c, int64_t kvc_token_stride, int64_t kvc_layer_stride, const void* k_pe,
+    int64_t kpe_token_stride, int64_t kpe_layer_stride, int32_t num_tokens, int32_t num_layers,
+    int32_t kv_lora_rank, int32_t pe_dim, const int64_t* slot_mapping, int64_t slot_layer_stride,
+    const int64_t* kv_cache_ptrs, const float* kv_scales, mla_dtype_t cache_dtype,
+    int64_t num_blocks, int32_t block_size, int64_t block_stride, int64_t entry_stride,
+    const mla_norm_rope_t* norm_rope, uint32_t* err_word, mla_stream_t stream) {
+  if (num_tokens < 0) return fail(MLA_ERR_INVALID_ARG, "num_tokens must be >= 0");
+  if (num_layers <= 0) return fail(MLA_ERR_INVALID_ARG, "num_layers must be >= 1");
+  if (!valid_dtype(cache_dtype))
+    return fail(MLA_ERR_INVALID_ARG,
+                "cache_dtype must be MLA_BF16, MLA_FP8_E4M3 or MLA_FP8_E5M2; got %d",
+                (int)cache_dtype);
+  if (kv_lora_rank != 512 || pe_dim != 64)
+    return fail(MLA_ERR_UNSUPPORTED,
+                "only kv_lora_rank 512 and pe_dim 64 are built (got %d, %d)", kv_lora_rank,
+                pe_dim);
+  const bool fp8 = cache_dtype != MLA_BF16;
+  if (fp8 && !kv_scales) return fail(MLA_ERR_INVALID_ARG, "FP8 grouped cache insert requires kv_scales");
+  if (!fp8 && kv_scales)
+    return fail(MLA_ERR_INVALID_ARG, "BF16 grouped cache insert does not use kv_scales");
+  if (slot_layer_stride < 0) return fail(MLA_ERR_INVALID_ARG, "slot_layer_stride must be >= 0");
+  if (block_size <= 0 || num_blocks <= 0)
+    return fail(MLA_ERR_INVALID_ARG, "block_size and num_blocks must be >= 1");
+  if (num_blocks > INT64_MAX / block_size)
+    return fail(MLA_ERR_INVALID_ARG, "num_blocks * block_size overflows int64");
+  if (entry_stride < kv_lora_rank + pe_dim)
+    return fail(MLA_ERR_INVALID_ARG, "entry_stride must be >= kv_lora_rank + pe_dim");
+  if (block_stride < (int64_t)(block_size - 1) * entry_stride + kv_lora_rank + pe_dim)
+    return fail(MLA_ERR_INVALID_ARG, "block_stride is too small for block_size entries");
+  const int ce = elt_size(cache_dtype);
+  if (!a16(kv_c) || !m16(kvc_token_stride * 2) || !m16(kvc_layer_stride * 2))
+    return fail(MLA_ERR_MISALIGNED, "kv_c rows must start on 16-byte boundaries");
+  if (!a16(k_pe) || !m16(kpe_token_stride * 2) || !m16(kpe_layer_stride * 2))
+    return fail(MLA_ERR_MISALIGNED, "k_pe rows must start on 16-byte boundaries");
+  if (!m16(block_stride * ce) || !m16(entry_stride * ce))
+    return fail(MLA_ERR_MISALIGNED, "cache block_stride / entry_stride must be multiples of 16 bytes");
+  if ((reinterpret_cast<uintptr_t>(slot_mapping) & 7) || (reinterpret_cast<uintptr_t>(kv_cache_ptrs) & 7))
+    return fail(MLA_ERR_MISALIGNED, "slot_mapping and kv_cache_ptrs must be 8-byte aligned");
+  if (err_word && (reinterpret_cast<uintptr_t>(err_word) & 3))
+    return fail(MLA_ERR_MISALIGNED, "err_word must be 4-byte aligned");
+  bool norm = false, rope = false;
+  if (norm_rope) {
+    norm = norm_rope->gamma != nullptr;
+    rope = norm_rope->positions != nullptr;
+    if (norm) {
+      if (!a16(norm_rope->gamma) || !m16(norm_rope->gamma_layer_stride * 2))
+        return fail(MLA_ERR_MISALIGNED, "gamma rows must start on 16-byte boundaries");
+      if (!(norm_rope->eps >= 0.0f) || !(norm_rope->eps < 3.0e38f))
+        return fail(MLA_ERR_INVALID_ARG, "eps must be finite and >= 0");
+    }
+    if (rope) {
+      if (!norm_rope->cos_sin_cache || norm_rope->max_position <= 0)
+        return fail(MLA_ERR_INVALID_ARG, "RoPE needs cos_sin_cache and max_position >= 1");
+      if (!a16(norm_rope->cos_sin_cache))
+        return fail(MLA_ERR_MISALIGNED, "cos_sin_cache must be 16-byte aligned");
+      if (reinterpret_cast<uintptr_t>(norm_rope->positions) & 7)
+        return fail(MLA_ERR_MISALIGNED, "positions must be 8-byte aligned");
+    }
+  }
+  if (num_tokens == 0) return MLA_OK;  // empty inputs may have null data pointers
+  if (!kv_c || !k_pe || !slot_mapping || !kv_cache_ptrs)
+    return fail(MLA_ERR_INVALID_ARG, "kv_c, k_pe, slot_mapping and kv_cache_ptrs must be non-null");
+
+  MLA_TRY(check_device_ptr(slot_mapping, "slot_mapping"));
+  MLA_TRY(check_device_ptr(kv_cache_ptrs, "kv_cache_ptrs"));
+  if (fp8) MLA_TRY(check_device_ptr(kv_scales, "kv_scales"));
+  if (norm) MLA_TRY(check_device_ptr(norm_rope->gamma, "gamma"));
+  if (rope) {
+    MLA_TRY(check_device_ptr(norm_rope->positions, "positions"));
+    MLA_TRY(check_device_ptr(norm_rope->cos_sin_cache, "cos_sin_cache"));
+  }
+
+  mla::InsertArgs a{};
+  a.kv_c = static_cast<const uint8_t*>(kv_c);
+  a.kvc_ts = kvc_token_stride * 2;
+  a.kvc_ls = kvc_layer_stride * 2;
+  a.k_pe = static_cast<const uint8_t*>(k_pe);
+  a.kpe_ts = kpe_token_stride * 2;
+  a.kpe_ls = kpe_layer_stride * 2;
+  a.num_rows = (int64_t)num_tokens * num_layers;
+  a.num_tokens = num_tokens;
+  a.num_layers = num_layers;
+  a.slots = slot_mapping;
+  a.slot_ls = slot_layer_stride;
+  a.cache_ptrs = kv_cache_ptrs;
+  a.scales = kv_scales;
+  a.capacity = num_blocks * block_size;
+  a.block_size = block_size;
+  a.bs_shift = log2_exact(block_size);
+  a.block_stride = block_stride * ce;
+  a.entry_stride = entry_stride * ce;
+  if (norm) {
+    a.gamma = static_cast<const uint8_t*>(norm_rope->gamma);
+    a.gamma_ls = norm_rope->gamma_layer_stride * 2;
+    a.eps = norm_rope->eps;
+  }
+  if (rope) {
+    a.positions = norm_rope->positions;
+    a.cos_sin = norm_rope->cos_sin_cache;
+    a.max_position = norm_rope->max_position;
+  }
+  a.err = err_word;
+  return launched(mla::launch_insert(a, (int)cache_dtype, norm, rope, cfg_for(stream)),
+                  "mla_cache_insert_grouped");
+}
+
+mla_status_t mla_context_gather(const void* kv_cache, mla_dtype_t cache_dtype, int64_t num_blocks,
+                                int32_t block_size, int64_t block_stride, int64_t entry_stride,
+                                int32_t entry_dim, const int32_t* block_table,
+                                int64_t block_table_stride, const int32_t* cu_chunk_lens,
+                                const int32_t* chunk_starts, int32_t num_seqs, int32_t num_tokens,
+                                void* out, int64_t out_row_stride, mla_dtype_t out_dtype,
+                                uint32_t* err_word, mla_stream_t stream) {
+  if (num_tokens < 0) return fail(MLA_ERR_INVALID_ARG, "num_tokens must be >= 0");
+  if (num_seqs <= 0) return fail(MLA_ERR_INVALID_ARG, "num_seqs must be >= 1");
+  if (!valid_dtype(cache_dtype) || !valid_dtype(out_dtype))
+    return fail(MLA_ERR_INVALID_ARG, "cache_dtype / out_dtype must be an mla_dtype_t value");
+  if (out_dtype != cache_dtype && !(cache_dtype != MLA_BF16 && out_dtype == MLA_BF16))
+    return fail(MLA_ERR_UNSUPPORTED,
+                "out_dtype must equal cache_dtype (raw) or be MLA_BF16 from an fp8 cache");
+  if (block_size <= 0 || num_blocks <= 0 || block_table_stride <= 0)
+    return fail(MLA_ERR_INVALID_ARG, "block_size, num_blocks and block_table_stride must be >= 1");
+  if (entry_dim <= 0 || entry_dim > entry_stride)
+    return fail(MLA_ERR_INVALID_ARG, "entry_dim must be in [1, entry_stride]");
+  if (block_stride < (int64_t)(block_size - 1) * entry_stride + entry_dim)
+    return fail(MLA_ERR_INVALID_ARG, "block_stride is too small for block_size entries");
+  const int ce = elt_size(cache_dtype), oe = elt_size(out_dtype);
+  if (out_row_stride < entry_dim) return fail(MLA_ERR_INVALID_ARG, "out_row_stride must be >= entry_dim");
+  if (!m16((int64_t)entry_dim * ce))
+    return fail(MLA_ERR_MISALIGNED, "entry_dim must span a multiple of 16 bytes");
+  if ((int64_t)entry_dim * ce > 1536)
+    return fail(MLA_ERR_UNSUPPORTED, "rows longer than 1536 bytes are not built");
+  if (!a16(kv_cache) || !m16(block_stride * ce) || !m16(entry_stride * ce))
+    return fail(MLA_ERR_MISALIGNED, "cache rows must start on 16-byte boundaries");
+  if (!a16(out) || !m16(out_row_stride * oe))
+    return fail(MLA_ERR_MISALIGNED, "out rows must start on 16-byte boundaries");
+  if ((reinterpret_cast<uintptr_t>(block_table) | reinterpret_cast<uintptr_t>(cu_chunk_lens) |
+       reinterpret_cast<uintptr_t>(chunk_starts)) & 3)
+    return fail(MLA_ERR_MISALIGNED, "int32 index arrays must be 4-byte aligned");
+  if (err_word && (reinterpret_cast<uintptr_t>(err_word) & 3))
+    return fail(MLA_ERR_MISALIGNED, "err_word must be 4-byte aligned");
+  if (num_tokens == 0) return MLA_OK;  // empty inputs may have null data pointers
+  if (!kv_cache || !block_table || !cu_chunk_lens || !chunk_starts || !out)
+    return fail(MLA_ERR_INVALID_ARG, "kv_cache, block_table, cu_chunk_lens, chunk_starts and out must be non-null");
+
+  MLA_TRY(check_device_ptr(block_table, "block_table"));
+  MLA_TRY(check_device_ptr(cu_chunk_lens, "cu_chunk_lens"));
+  MLA_TRY(check_device_ptr(chunk_starts, "chunk_starts"));
+
+  mla::GatherArgs a{};
+  a.cache = static_cast<const uint8_t*>(kv_cache);
+  a.block_stride = block_stride * ce;
+  a.entry_stride = entry_stride * ce;
+  a.num_blocks = num_blocks;
+  a.block_size = block_size;
+  a.bs_shift = log2_exact(block_size);
+  a.row_chunks = (int32_t)((int64_t)entry_dim * ce / 16);
+  a.block_table = block_table;
+  a.bt_stride = block_table_stride;
+  a.cu = cu_chunk_lens;
+  a.starts = chunk_starts;
+  a.num_seqs = num_seqs;
+  a.num_tokens = num_tokens;
+  a.out = static_cast<uint8_t*>(out);
+  a.out_rs = out_row_stride * oe;
+  a.err = err_word;
+  const int mode = (out_dtype == cache_dtype) ? 0 : (int)cache_dtype;
+  return launched(mla::launch_gather(a, mode, cfg_for(stream)), "mla_context_gather");
+}
+
+mla_status_t mla_context_kv_pack(const void* k_nope, int64_t kn_token_stride,
+                                 int64_t kn_head_stride, const void* v, int64_t v_token_stride,
+                                 int64_t v_head_stride, const void* k_pe,
+                                 int64_t kpe_token_stride, mla_dtype_t kpe_dtype,
+                                 int32_t num_tokens, int32_t num_heads, int32_t nope_dim,
+                                 int32_t rope_dim, int32_t v_dim, void* key_out, void* v_out,
+                                 mla_dtype_t out_dtype, const float* out_scale,
+                                 mla_stream_t stream) {
+  if (num_tokens < 0) return fail(MLA_ERR_INVALID_ARG, "num_tokens must be >= 0");
+  if (num_heads <= 0) return fail(MLA_ERR_INVALID_ARG, "num_heads must be >= 1");
+  if (!valid_dtype(out_dtype) || !valid_dtype(kpe_dtype))
+    return fail(MLA_ERR_INVALID_ARG, "out_dtype / kpe_dtype must be an mla_dtype_t value");
+  if (nope_dim != 128 || rope_dim != 64 || v_dim != 128)
+    return fail(MLA_ERR_UNSUPPORTED, "only nope 128, rope 64, v 128 are built (got %d, %d, %d)",
+                nope_dim, rope_dim, v_dim);
+  if (out_dtype != MLA_BF16 && kpe_dtype != MLA_BF16 && kpe_dtype != out_dtype)
+    return fail(MLA_ERR_UNSUPPORTED,
+                "an fp8 k_pe is copied raw, so it must have the fp8 output's format");
+  if (out_dtype == MLA_BF16 && out_scale)
+    return fail(MLA_ERR_INVALID_ARG, "a bf16 pack does not use out_scale");
+  if (!a16(k_nope) || !m16(kn_token_stride * 2) || !m16(kn_head_stride * 2))
+    return fail(MLA_ERR_MISALIGNED, "k_nope rows must start on 16-byte boundaries");
+  if (v_out && (!a16(v) || !m16(v_token_stride * 2) || !m16(v_head_stride * 2)))
+    return fail(MLA_ERR_MISALIGNED, "v rows must start on 16-byte boundaries");
+  const int ke = elt_size(kpe_dtype);
+  if ((reinterpret_cast<uintptr_t>(k_pe) & (ke == 2 ? 15 : 7)) ||
+      ((kpe_token_stride * ke) & (ke == 2 ? 15 : 7)))
+    return fail(MLA_ERR_MISALIGNED, "k_pe rows must start on %d-byte boundaries", ke == 2 ? 16 : 8);
+  if (!a16(key_out) || (v_out && !a16(v_out)))
+    return fail(MLA_ERR_MISALIGNED, "key_out and v_out must be 16-byte aligned");
+  if (out_scale && (reinterpret_cast<uintptr_t>(out_scale) & 3))
+    return fail(MLA_ERR_MISALIGNED, "out_scale must be 4-byte aligned");
+  if (num_tokens == 0) return MLA_OK;  // empty inputs may have null data pointers
+  if (!k_nope || !k_pe || !key_out || (v_out && !v))
+    return fail(MLA_ERR_INVALID_ARG, "k_nope, k_pe, key_out (and v when v_out is set) must be non-null");
+
+  if (out_scale) MLA_TRY(check_device_ptr(out_scale, "out_scale"));
+
+  mla::PackArgs a{};
+  a.k_nope = static_cast<const uint8_t*>(k_nope);
+  a.kn_ts = kn_token_stride * 2;
+  a.kn_hs = kn_head_stride * 2;
+  a.v = static_cast<const uint8_t*>(v);
+  a.v_ts = v_token_stride * 2;
+  a.v_hs = v_head_stride * 2;
+  a.k_pe = static_cast<const uint8_t*>(k_pe);
+  a.kpe_ts = kpe_token_stride * ke;
+  a.num_tokens = num_tokens;
+  a.num_heads = num_heads;
+  a.key = static_cast<uint8_t*>(key_out);
+  a.vout = static_cast<uint8_t*>(v_out);
+  a.out_scale = out_scale;
+  return launched(mla::launch_pack(a, (int)out_dtype, (int)kpe_dtype, cfg_for(stream)),
+                  "mla_context_kv_pack");
+}
+
+mla_status_t mla_rope_cos_sin_cache(float* out, int64_t max_position, int32_t rot_dim,
+                                    double base, mla_stream_t stream) {
+  if (!out) return fail(MLA_ERR_INVALID_ARG, "out must be non-null");
+  if (max_position <= 0 || rot_dim <= 0 || (rot_dim & 1))
+    return fail(MLA_ERR_INVALID_ARG, "max_position must be >= 1 and rot_dim even and >= 2");
+  if (!(base > 1.0) || !(base < 1e300)) return fail(MLA_ERR_INVALID_ARG, "base must be > 1");
+  if (!a16(out)) return fail(MLA_ERR_MISALIGNED, "out must be 16-byte aligned");
+  MLA_TRY(check_device_ptr(out, "out"));
+  return launched(mla::launch_rope_table(out, max_position, rot_dim, base, cfg_for(stream)),
+                  "mla_rope_cos_sin_cache");
+}
+
+}  // extern "C"

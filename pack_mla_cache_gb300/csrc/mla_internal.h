@@ -1,0 +1,82 @@
+// mla_internal.h -- launch descriptors shared by the C-ABI layer (abi.cu) and
+// the kernel translation units.  All strides here are in BYTES; the ABI layer
+// converts the element strides of the public header.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mla {
+
+struct InsertArgs {
+  const uint8_t* kv_c;
+  int64_t kvc_ts, kvc_ls;  // token / layer strides
+  const uint8_t* k_pe;
+  int64_t kpe_ts, kpe_ls;
+  int64_t num_rows;  // num_tokens * num_layers
+  int32_t num_tokens, num_layers;
+  const int64_t* slots;
+  int64_t slot_ls;  // elements (0 = shared)
+  const int64_t* cache_ptrs;
+  const float* scales;
+  int64_t capacity;  // num_blocks * block_size
+  int32_t block_size;
+  int32_t bs_shift;  // log2(block_size) if a power of two, else -1
+  int64_t block_stride, entry_stride;
+  const uint8_t* gamma;
+  int64_t gamma_ls;
+  float eps;
+  const int64_t* positions;
+  const float* cos_sin;
+  int64_t max_position;
+  uint32_t* err;
+};
+
+struct GatherArgs {
+  const uint8_t* cache;
+  int64_t block_stride, entry_stride;
+  int64_t num_blocks;
+  int32_t block_size, bs_shift;
+  int32_t row_chunks;  // 16-byte chunks of the copied part of a cache row
+  const int32_t* block_table;
+  int64_t bt_stride;  // elements
+  const int32_t* cu;
+  const int32_t* starts;
+  int32_t num_seqs, num_tokens;
+  uint8_t* out;
+  int64_t out_rs;
+  uint32_t* err;
+};
+
+struct PackArgs {
+  const uint8_t* k_nope;
+  int64_t kn_ts, kn_hs;
+  const uint8_t* v;
+  int64_t v_ts, v_hs;
+  const uint8_t* k_pe;
+  int64_t kpe_ts;
+  int32_t num_tokens, num_heads;
+  uint8_t* key;
+  uint8_t* vout;  // may be null
+  const float* out_scale;  // may be null (1.0)
+};
+
+struct LaunchCfg {
+  cudaStream_t stream;
+  bool pdl;
+};
+
+// Each returns cudaSuccess or the launch error.  cache_fmt / out_fmt / kpe_fmt
+// take the values of mla::Fmt.
+cudaError_t launch_insert(const InsertArgs& a, int cache_fmt, bool norm, bool rope,
+                          const LaunchCfg& cfg);
+cudaError_t launch_gather(const GatherArgs& a, int mode, const LaunchCfg& cfg);
+cudaError_t launch_pack(const PackArgs& a, int out_fmt, int kpe_fmt, const LaunchCfg& cfg);
+cudaError_t launch_rope_table(float* out, int64_t max_position, int32_t rot_dim, double base,
+                              const LaunchCfg& cfg);
+
+// Grid size for a grid-stride kernel: enough CTAs to cover `work_ctas`, capped
+// at the number that can be resident at once on the current device.
+int capped_grid(const void* kernel, int threads, int64_t work_ctas);
+
+}  // namespace mla

@@ -1,0 +1,175 @@
+"""Thin Python binding of libmla_cache (include/mla_cache.h).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  Each function has the name of the C entry point it calls, takes
+torch tensors (device memory) and forwards their data pointers, element
+strides and the current CUDA stream.  A failing call raises ``MlaError`` with
+the library's status and message.  There is no fallback: if the library is
+not built, ``lib()`` raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB_PATH
+
+MLA_BF16, MLA_FP8_E4M3, MLA_FP8_E5M2 = 0, 1, 2
+MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_MISALIGNED, MLA_ERR_CUDA = range(5)
+MLA_ERRBIT_SLOT_OOB, MLA_ERRBIT_BLOCK_OOB, MLA_ERRBIT_POS_OOB, MLA_ERRBIT_MISALIGNED = 1, 2, 4, 8
+
+_TORCH_DTYPE = {MLA_BF16: torch.bfloat16, MLA_FP8_E4M3: torch.float8_e4m3fn,
+                MLA_FP8_E5M2: torch.float8_e5m2}
+
+
+class MlaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"[mla status {status}] {message}")
+        self.status = status
+
+
+class NormRope(ctypes.Structure):
+    _fields_ = [("gamma", ctypes.c_void_p), ("gamma_layer_stride", ctypes.c_int64),
+                ("eps", ctypes.c_float), ("positions", ctypes.c_void_p),
+                ("cos_sin_cache", ctypes.c_void_p), ("max_position", ctypes.c_int64)]
+
+
+_lib = None
+
+# C signatures of every entry point declared in include/mla_cache.h
+_i32, _i64, _u32, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_void_p
+SIGNATURES = {
+    "mla_dtype_from_string": (ctypes.c_int, [ctypes.c_char_p]),
+    "mla_last_error": (ctypes.c_char_p, []),
+    "mla_version": (ctypes.c_char_p, []),
+    "mla_set_pdl": (ctypes.c_int, [ctypes.c_int]),
+    "mla_cache_insert_grouped": (ctypes.c_int, [
+        _vp, _i64, _i64, _vp, _i64, _i64, _i32, _i32, _i32, _i32, _vp, _i64, _vp, _vp,
+        ctypes.c_int, _i64, _i32, _i64, _i64, ctypes.POINTER(NormRope), _vp, _vp]),
+    "mla_context_gather": (ctypes.c_int, [
+        _vp, ctypes.c_int, _i64, _i32, _i64, _i64, _i32, _vp, _i64, _vp, _vp, _i32, _i32, _vp,
+        _i64, ctypes.c_int, _vp, _vp]),
+    "mla_context_kv_pack": (ctypes.c_int, [
+        _vp, _i64, _i64, _vp, _i64, _i64, _vp, _i64, ctypes.c_int, _i32, _i32, _i32, _i32, _i32,
+        _vp, _vp, ctypes.c_int, _vp, _vp]),
+    "mla_rope_cos_sin_cache": (ctypes.c_int, [_vp, _i64, _i32, ctypes.c_double, _vp]),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmla_cache.so (built in-tree by pack_mla_cache_gb300.build)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"libmla_cache.so is not built ({LIB_PATH} missing): run "
+                "pack_mla_cache_gb300.build.build() first; there is no fallback path")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(status: int) -> None:
+    if status != MLA_OK:
+        raise MlaError(status, lib().mla_last_error().decode())
+
+
+def dtype_code(d) -> int:
+    if isinstance(d, int):
+        return d
+    if isinstance(d, torch.dtype):
+        for k, v in _TORCH_DTYPE.items():
+            if v == d:
+                return k
+        raise ValueError(f"unsupported dtype {d}")
+    code = lib().mla_dtype_from_string(str(d).encode())
+    if code < 0:
+        raise MlaError(MLA_ERR_INVALID_ARG, f"unknown kv cache dtype string {d!r}")
+    return code
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def mla_dtype_from_string(s: str) -> int:
+    return lib().mla_dtype_from_string(s.encode())
+
+
+def mla_last_error() -> str:
+    return lib().mla_last_error().decode()
+
+
+def mla_version() -> str:
+    return lib().mla_version().decode()
+
+
+def mla_set_pdl(enable: bool) -> bool:
+    return bool(lib().mla_set_pdl(1 if enable else 0))
+
+
+def mla_cache_insert_grouped(kv_c, k_pe, slot_mapping, kv_cache_ptrs, kv_scales, cache_dtype,
+                             num_blocks, block_size, block_stride, entry_stride, *,
+                             slot_layer_stride=None, gamma=None, eps=1e-6, positions=None,
+                             cos_sin_cache=None, err_word=None, stream=None):
+    """kv_c [L, T, R] and k_pe [L, T, P] bf16 views (any strides, unit last
+    stride); slot_mapping int64 [L, T] or [T] (shared); kv_cache_ptrs int64 [L];
+    kv_scales fp32 [L] or None."""
+    L, T, R = kv_c.shape
+    P = k_pe.shape[2]
+    if slot_layer_stride is None:
+        slot_layer_stride = 0 if slot_mapping.dim() == 1 else slot_mapping.stride(0)
+    nr = None
+    if gamma is not None or positions is not None:
+        nr = NormRope(_ptr(gamma), 0 if gamma is None else gamma.stride(0), float(eps),
+                      _ptr(positions), _ptr(cos_sin_cache),
+                      0 if cos_sin_cache is None else cos_sin_cache.shape[0])
+    _check(lib().mla_cache_insert_grouped(
+        _ptr(kv_c), kv_c.stride(1), kv_c.stride(0), _ptr(k_pe), k_pe.stride(1), k_pe.stride(0),
+        T, L, R, P, _ptr(slot_mapping), slot_layer_stride, _ptr(kv_cache_ptrs), _ptr(kv_scales),
+        dtype_code(cache_dtype), num_blocks, block_size, block_stride, entry_stride,
+        ctypes.byref(nr) if nr is not None else None, _ptr(err_word), _stream(stream)))
+
+
+def mla_context_gather(kv_cache, cache_dtype, num_blocks, block_size, block_stride,
+                       entry_stride, entry_dim, block_table, cu_chunk_lens, chunk_starts, out,
+                       out_dtype, *, num_tokens=None, err_word=None, stream=None):
+    """kv_cache: the cache base (any tensor over its bytes); block_table int32
+    [S, W]; out [num_tokens, >= entry_dim] with unit last stride."""
+    S = chunk_starts.shape[0]
+    n = out.shape[0] if num_tokens is None else num_tokens
+    _check(lib().mla_context_gather(
+        _ptr(kv_cache), dtype_code(cache_dtype), num_blocks, block_size, block_stride,
+        entry_stride, entry_dim, _ptr(block_table), block_table.stride(0), _ptr(cu_chunk_lens),
+        _ptr(chunk_starts), S, n, _ptr(out), out.stride(0), dtype_code(out_dtype),
+        _ptr(err_word), _stream(stream)))
+
+
+def mla_context_kv_pack(k_nope, v, k_pe, key_out, v_out, out_dtype, *, kpe_dtype=None,
+                        out_scale=None, stream=None):
+    """k_nope / v: [T, H, 128] bf16 views (strided); k_pe [T, 64] (bf16 or fp8,
+    strided rows); key_out [T, H, 192] and v_out [T, H, 128] (or None)."""
+    T, H, N = k_nope.shape
+    kd = dtype_code(kpe_dtype if kpe_dtype is not None else k_pe.dtype)
+    _check(lib().mla_context_kv_pack(
+        _ptr(k_nope), k_nope.stride(0), k_nope.stride(1), _ptr(v), v.stride(0), v.stride(1),
+        _ptr(k_pe), k_pe.stride(0), kd, T, H, N, k_pe.shape[-1], v.shape[2], _ptr(key_out),
+        _ptr(v_out), dtype_code(out_dtype), _ptr(out_scale), _stream(stream)))
+
+
+def mla_rope_cos_sin_cache(out, base=10000.0, *, stream=None):
+    """Fill out (fp32 [max_position, rot_dim]) with the rotary cos/sin table."""
+    _check(lib().mla_rope_cos_sin_cache(_ptr(out), out.shape[0], out.shape[1], float(base),
+                                        _stream(stream)))

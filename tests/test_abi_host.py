@@ -1,0 +1,209 @@
+"""Host-side checks of the C ABI (no GPU needed, no kernel launched).
+
+* the library builds, loads, and exports every entry point include/mla_cache.h
+  declares;
+* the vLLM cache-dtype strings map as the grouped insert's host whitelist does
+  ("PR #55356 [Kimi Perf] Group fp8 mla cache insertion", Source snippets:
+  "auto"/"bfloat16", "fp8"/"fp8_e4m3", "fp8_e5m2");
+* every argument check rejects its case with the documented status before any
+  CUDA call (fake, never-dereferenced addresses are used), including the
+  pages' "FP8 ... requires kv_scales" and "BF16 ... does not use kv_scales";
+* a call that passes validation on a machine without a GPU fails with
+  MLA_ERR_CUDA instead of crashing.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+import torch
+
+from pack_mla_cache_gb300 import build as B
+from pack_mla_cache_gb300 import ops
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "mla_cache.h")
+A = 0x7F0000000000  # a 16-byte aligned fake device address (never dereferenced)
+
+
+@pytest.fixture(scope="module")
+def L():
+    B.build()
+    return ops.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_expected_entry_points():
+    assert declared_functions() == sorted(ops.SIGNATURES)
+
+
+def test_library_exports_every_declared_symbol(L):
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (mla_[a-z0-9_]+)$", out, flags=re.M))
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(L, name)
+
+
+def test_version_and_dtype_strings(L):
+    assert "sm_103a" in ops.mla_version()
+    m = {"auto": 0, "bfloat16": 0, "fp8": 1, "fp8_e4m3": 1, "fp8_e5m2": 2}
+    for s, code in m.items():
+        assert ops.mla_dtype_from_string(s) == code
+    for s in ("fp16", "fp8_ds_mla", "", "FP8"):
+        assert ops.mla_dtype_from_string(s) == -1
+
+
+def test_pdl_toggle(L):
+    prev = ops.mla_set_pdl(False)
+    assert ops.mla_set_pdl(True) is False
+    ops.mla_set_pdl(prev)
+
+
+def insert(L, **kw):
+    args = dict(kv_c=A, kvc_ts=512, kvc_ls=512 * 8, k_pe=A + 4096, kpe_ts=64, kpe_ls=64 * 8,
+                T=8, nl=5, R=512, P=64, slots=A + 8192, sls=0, ptrs=A + 16384, scales=A + 32768,
+                dtype=1, nb=64, bs=64, bstride=64 * 576, estride=576, nr=None, err=None)
+    args.update(kw)
+    return L.mla_cache_insert_grouped(
+        args["kv_c"], args["kvc_ts"], args["kvc_ls"], args["k_pe"], args["kpe_ts"],
+        args["kpe_ls"], args["T"], args["nl"], args["R"], args["P"], args["slots"], args["sls"],
+        args["ptrs"], args["scales"], args["dtype"], args["nb"], args["bs"], args["bstride"],
+        args["estride"], args["nr"], args["err"], None)
+
+
+@pytest.mark.parametrize("kw,status,msg", [
+    (dict(T=-1), ops.MLA_ERR_INVALID_ARG, "num_tokens"),
+    (dict(nl=0), ops.MLA_ERR_INVALID_ARG, "num_layers"),
+    (dict(dtype=7), ops.MLA_ERR_INVALID_ARG, "cache_dtype"),
+    (dict(R=256), ops.MLA_ERR_UNSUPPORTED, "kv_lora_rank"),
+    (dict(P=32), ops.MLA_ERR_UNSUPPORTED, "pe_dim"),
+    (dict(scales=None), ops.MLA_ERR_INVALID_ARG, "FP8 grouped cache insert requires kv_scales"),
+    (dict(dtype=0, bstride=64 * 576), ops.MLA_ERR_INVALID_ARG, "BF16 grouped cache insert does not use kv_scales"),
+    (dict(kv_c=None), ops.MLA_ERR_INVALID_ARG, "non-null"),
+    (dict(slots=None), ops.MLA_ERR_INVALID_ARG, "non-null"),
+    (dict(ptrs=None), ops.MLA_ERR_INVALID_ARG, "non-null"),
+    (dict(sls=-1), ops.MLA_ERR_INVALID_ARG, "slot_layer_stride"),
+    (dict(bs=0), ops.MLA_ERR_INVALID_ARG, "block_size"),
+    (dict(estride=500), ops.MLA_ERR_INVALID_ARG, "entry_stride"),
+    (dict(bstride=576), ops.MLA_ERR_INVALID_ARG, "block_stride"),
+    (dict(kv_c=A + 8), ops.MLA_ERR_MISALIGNED, "kv_c"),
+    (dict(kvc_ts=500), ops.MLA_ERR_MISALIGNED, "kv_c"),
+    (dict(k_pe=A + 2), ops.MLA_ERR_MISALIGNED, "k_pe"),
+    (dict(kpe_ls=100), ops.MLA_ERR_MISALIGNED, "k_pe"),
+    (dict(estride=580, bstride=64 * 580), ops.MLA_ERR_MISALIGNED, "entry_stride"),
+    (dict(slots=A + 4), ops.MLA_ERR_MISALIGNED, "8-byte"),
+    (dict(err=A + 2), ops.MLA_ERR_MISALIGNED, "err_word"),
+])
+def test_insert_argument_checks(L, kw, status, msg):
+    assert insert(L, **kw) == status
+    assert msg in ops.mla_last_error()
+
+
+def test_insert_norm_rope_checks(L):
+    nr = ops.NormRope(A + 8, 512, 1e-6, None, None, 0)
+    assert insert(L, nr=ctypes.byref(nr)) == ops.MLA_ERR_MISALIGNED
+    nr = ops.NormRope(A, 512, -1.0, None, None, 0)
+    assert insert(L, nr=ctypes.byref(nr)) == ops.MLA_ERR_INVALID_ARG
+    nr = ops.NormRope(None, 0, 1e-6, A, None, 0)
+    assert insert(L, nr=ctypes.byref(nr)) == ops.MLA_ERR_INVALID_ARG
+    assert "cos_sin_cache" in ops.mla_last_error()
+    nr = ops.NormRope(None, 0, 1e-6, A, A + 4, 32768)
+    assert insert(L, nr=ctypes.byref(nr)) == ops.MLA_ERR_MISALIGNED
+
+
+def test_zero_tokens_is_a_no_op_without_cuda(L):
+    assert insert(L, T=0) == ops.MLA_OK
+    assert L.mla_context_kv_pack(A, 4160, 256, A, 4160, 256, A, 576, 1, 0, 16, 128, 64, 128, A,
+                                 A, 1, None, None) == ops.MLA_OK
+
+
+def test_validated_call_without_gpu_reports_cuda_error(L):
+    if torch.cuda.is_available():
+        pytest.skip("this check is for machines without a GPU")
+    assert insert(L) == ops.MLA_ERR_CUDA
+    assert "cudaPointerGetAttributes" in ops.mla_last_error()
+
+
+def gather(L, **kw):
+    a = dict(cache=A, cdt=1, nb=1024, bs=64, bstride=64 * 576, estride=576, edim=576, bt=A,
+             bts=512, cu=A + 4096, st=A + 8192, S=1, T=8192, out=A + 65536, ors=576, odt=1,
+             err=None)
+    a.update(kw)
+    return L.mla_context_gather(a["cache"], a["cdt"], a["nb"], a["bs"], a["bstride"],
+                                a["estride"], a["edim"], a["bt"], a["bts"], a["cu"], a["st"],
+                                a["S"], a["T"], a["out"], a["ors"], a["odt"], a["err"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(T=-1), ops.MLA_ERR_INVALID_ARG),
+    (dict(S=0), ops.MLA_ERR_INVALID_ARG),
+    (dict(cdt=0, odt=1), ops.MLA_ERR_UNSUPPORTED),
+    (dict(cdt=1, odt=2), ops.MLA_ERR_UNSUPPORTED),
+    (dict(bt=None), ops.MLA_ERR_INVALID_ARG),
+    (dict(edim=600), ops.MLA_ERR_INVALID_ARG),
+    (dict(edim=570, estride=576), ops.MLA_ERR_MISALIGNED),
+    (dict(ors=500), ops.MLA_ERR_INVALID_ARG),
+    (dict(out=A + 8), ops.MLA_ERR_MISALIGNED),
+    (dict(cache=A + 4), ops.MLA_ERR_MISALIGNED),
+    (dict(bts=0), ops.MLA_ERR_INVALID_ARG),
+    (dict(cdt=0, odt=0, edim=1024, estride=1024, bstride=64 * 1024, ors=1024), ops.MLA_ERR_UNSUPPORTED),
+])
+def test_gather_argument_checks(L, kw, status):
+    assert gather(L, **kw) == status
+
+
+def pack(L, **kw):
+    a = dict(kn=A, kts=4160, khs=256, v=A + 256, vts=4160, vhs=256, kpe=A + 1024, kpets=576,
+             kdt=1, T=8192, H=16, N=128, R=64, V=128, key=A + (1 << 30), vout=A + (2 << 30), odt=1,
+             scale=None)
+    a.update(kw)
+    return L.mla_context_kv_pack(a["kn"], a["kts"], a["khs"], a["v"], a["vts"], a["vhs"],
+                                 a["kpe"], a["kpets"], a["kdt"], a["T"], a["H"], a["N"], a["R"],
+                                 a["V"], a["key"], a["vout"], a["odt"], a["scale"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(T=-1), ops.MLA_ERR_INVALID_ARG),
+    (dict(H=0), ops.MLA_ERR_INVALID_ARG),
+    (dict(N=64), ops.MLA_ERR_UNSUPPORTED),
+    (dict(V=64), ops.MLA_ERR_UNSUPPORTED),
+    (dict(kdt=2, odt=1), ops.MLA_ERR_UNSUPPORTED),
+    (dict(odt=0, kdt=0, scale=A), ops.MLA_ERR_INVALID_ARG),
+    (dict(kn=None), ops.MLA_ERR_INVALID_ARG),
+    (dict(kn=A + 2), ops.MLA_ERR_MISALIGNED),
+    (dict(khs=100), ops.MLA_ERR_MISALIGNED),
+    (dict(v=A + 8), ops.MLA_ERR_MISALIGNED),
+    (dict(kpe=A + 4), ops.MLA_ERR_MISALIGNED),
+    (dict(kdt=0, kpe=A + 8, odt=0), ops.MLA_ERR_MISALIGNED),
+    (dict(key=A + 8), ops.MLA_ERR_MISALIGNED),
+    (dict(odt=9), ops.MLA_ERR_INVALID_ARG),
+])
+def test_pack_argument_checks(L, kw, status):
+    assert pack(L, **kw) == status
+
+
+def test_rope_table_argument_checks(L):
+    assert L.mla_rope_cos_sin_cache(None, 10, 64, 1e4, None) == ops.MLA_ERR_INVALID_ARG
+    assert L.mla_rope_cos_sin_cache(A, 10, 63, 1e4, None) == ops.MLA_ERR_INVALID_ARG
+    assert L.mla_rope_cos_sin_cache(A, 0, 64, 1e4, None) == ops.MLA_ERR_INVALID_ARG
+    assert L.mla_rope_cos_sin_cache(A, 10, 64, 0.5, None) == ops.MLA_ERR_INVALID_ARG
+    assert L.mla_rope_cos_sin_cache(A + 4, 10, 64, 1e4, None) == ops.MLA_ERR_MISALIGNED
+
+
+def test_error_message_is_thread_local(L):
+    import threading
+    insert(L, T=-1)
+    seen = []
+    t = threading.Thread(target=lambda: seen.append(ops.mla_last_error()))
+    t.start()
+    t.join()
+    assert seen == [""]
+    assert "num_tokens" in ops.mla_last_error()

@@ -1,0 +1,281 @@
+"""GPU parity of the context gather and the K/V pack against the CPU oracle,
+through the C ABI -- all bit-exact ("PR #51772 [Attention][MLA] Fuse Kimi-K3
+chunked-context K/V packing": the fused loop must equal the generic one
+chunk by chunk with atol=0/rtol=0, and the fp8 cast must be bit-identical).
+
+Covers: 32768 context tokens in 4 chunks of 8192 from an fp8 e4m3 cache
+(1024 blocks, random block table), raw and bf16-widened gathers, kv_b_proj
+output [8192, 4160] bf16 packed to fp8 e4m3 (scale 0.01) and to bf16, head
+counts 16 / 3 / 4 (runtime), 0 and ragged token counts, e5m2 output, bf16
+k_pe into fp8, no-V packs, several sequences per gather, bad block ids, the
+16-chunk programmatic-dependent-launch chain, and one 131072-token launch of
+the grid-capped grid-stride loop (sampled).
+"""
+import numpy as np
+import pytest
+import torch
+
+import devutil as D
+import refmath as R
+from pack_mla_cache_gb300 import ops
+from pack_mla_cache_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+ENTRY = 576
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from pack_mla_cache_gb300 import build
+    build.build()
+    ops.lib()
+
+
+def dev_cache(pw):
+    if pw.cache_dtype == 0:
+        return D.dev_bf16(pw.cache)
+    return D.dev(pw.cache)
+
+
+def gpu_gather(pw, cache_t, table, cu, starts, T, out_dtype, err=None):
+    out = torch.full((T, ENTRY), 0x3F if out_dtype else 0x3F3F, dtype=torch.int16 if out_dtype == 0 else torch.uint8,
+                     device="cuda")
+    if out_dtype == 0:
+        out = out.view(torch.bfloat16)
+    ops.mla_context_gather(cache_t, pw.cache_dtype, pw.num_blocks, pw.block_size,
+                           pw.block_size * ENTRY, ENTRY, ENTRY, D.dev(table), D.dev(cu),
+                           D.dev(starts), out, out_dtype, err_word=err)
+    torch.cuda.synchronize()
+    return D.host_u16(out) if out_dtype == 0 else D.host_u8(out)
+
+
+def oracle_gather(orc, pw, table, cu, starts, T, out_dtype):
+    out = np.full((T, ENTRY), 0x3F if out_dtype else 0x3F3F, np.uint8 if out_dtype else np.uint16)
+    err = orc.context_gather(pw.cache, pw.cache_dtype, pw.num_blocks, pw.block_size,
+                             pw.block_size * ENTRY, ENTRY, ENTRY, table, cu, starts, out, out_dtype)
+    return out, err
+
+
+@pytest.mark.parametrize("out_dtype", [1, 0])
+def test_gather_four_chunks_of_8192(orc, out_dtype):
+    pw = W.pack_workload(32768, 8192, num_blocks=1024, seed=1)
+    cache_t = dev_cache(pw)
+    for c in range(4):
+        cu = np.array([0, 8192], np.int32)
+        st = np.array([c * 8192], np.int32)
+        g = gpu_gather(pw, cache_t, pw.block_table, cu, st, 8192, out_dtype)
+        r, err = oracle_gather(orc, pw, pw.block_table, cu, st, 8192, out_dtype)
+        assert err == 0
+        np.testing.assert_array_equal(g, r)
+
+
+def test_gather_many_sequences_and_bad_blocks(orc):
+    pw = W.pack_workload(4096, 4096, num_blocks=128, seed=2)
+    cache_t = dev_cache(pw)
+    rng = np.random.default_rng(0)
+    S = 37
+    table = rng.integers(0, 128, size=(S, 8)).astype(np.int32)
+    table[5, 1] = 128    # block id out of range
+    table[9, 0] = -3
+    lens = rng.integers(0, 200, size=S)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    starts = rng.integers(0, 300, size=S).astype(np.int32)  # positions up to 500 < 8 * 64
+    T = int(cu[-1]) + 5  # 5 trailing rows owned by no sequence
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    g = gpu_gather(pw, cache_t, table, cu, starts, T, 1, err=err)
+    r, oerr = oracle_gather(orc, pw, table, cu, starts, T, 1)
+    np.testing.assert_array_equal(g, r)
+    assert int(err.item()) == oerr
+    assert oerr in (0, ops.MLA_ERRBIT_BLOCK_OOB)
+
+
+def test_gather_bf16_cache_raw(orc):
+    pw = W.pack_workload(3000, 3000, num_blocks=64, cache_dtype=0, seed=3)
+    cu = np.array([0, 3000], np.int32)
+    st = np.array([0], np.int32)
+    g = gpu_gather(pw, dev_cache(pw), pw.block_table, cu, st, 3000, 0)
+    r, _ = oracle_gather(orc, pw, pw.block_table, cu, st, 3000, 0)
+    np.testing.assert_array_equal(g, r)
+
+
+@pytest.mark.parametrize("fmt", [1, 2])
+def test_gather_widens_every_fp8_code(orc, fmt):
+    """A cache row holding every byte value: the widening is exact for all 256
+    codes (NaNs become the signed quiet NaN)."""
+    pw = W.pack_workload(64, 64, num_blocks=1, cache_dtype=fmt, seed=4)
+    pw.cache[:] = (np.arange(pw.cache.size) % 256).astype(np.uint8)
+    cu = np.array([0, 64], np.int32)
+    st = np.array([0], np.int32)
+    g = gpu_gather(pw, dev_cache(pw), pw.block_table, cu, st, 64, 0)
+    r, _ = oracle_gather(orc, pw, pw.block_table, cu, st, 64, 0)
+    np.testing.assert_array_equal(g, r)
+
+
+# -------------------------------------------------------------------------- pack
+def pack_io(kvb, ws, H, out_dtype, kpe_fp8, with_v=True):
+    """Device views of a kv_b_proj output [T, >= H*256] and a gather workspace
+    [T, 576] (k_pe = columns 512:576), and fresh outputs."""
+    T = kvb.shape[0]
+    kvb_t = D.dev_bf16(kvb)
+    heads = kvb_t[:, : H * 256].view(T, H, 256)
+    k_nope, v = heads[:, :, :128], heads[:, :, 128:]
+    ws_t = D.dev(ws) if kpe_fp8 else D.dev_bf16(ws)
+    k_pe = ws_t[:, 512:]
+    odt = torch.bfloat16 if out_dtype == 0 else torch.uint8
+    key = torch.zeros((T, H, 192), dtype=odt, device="cuda")
+    vout = torch.zeros((T, H, 128), dtype=odt, device="cuda") if with_v else None
+    return k_nope, v, k_pe, key, vout
+
+
+def run_pack(kvb, ws, H, out_dtype, kpe_dtype, scale=0.01, with_v=True):
+    k_nope, v, k_pe, key, vout = pack_io(kvb, ws, H, out_dtype, kpe_dtype != 0, with_v)
+    sc = torch.tensor([scale], dtype=torch.float32, device="cuda") if out_dtype != 0 else None
+    ops.mla_context_kv_pack(k_nope, v, k_pe, key, vout, out_dtype, kpe_dtype=kpe_dtype,
+                            out_scale=sc)
+    torch.cuda.synchronize()
+    conv = D.host_u16 if out_dtype == 0 else D.host_u8
+    return conv(key), (conv(vout) if with_v else None)
+
+
+def oracle_pack(orc, kvb, ws, H, out_dtype, kpe_dtype, scale=0.01, with_v=True):
+    T, rs = kvb.shape
+    return orc.context_kv_pack(kvb, rs, 256, kvb[:, 128:], rs, 256, ws[:, 512:], ENTRY,
+                               kpe_dtype, T, H, 128, 64, 128, out_dtype,
+                               scale if out_dtype != 0 else 1.0, with_v)
+
+
+def workspace(orc, pw, T, start, out_dtype):
+    ws = np.zeros((T, ENTRY), np.uint8 if out_dtype else np.uint16)
+    orc.context_gather(pw.cache, 1, pw.num_blocks, pw.block_size, pw.block_size * ENTRY, ENTRY,
+                       ENTRY, pw.block_table, np.array([0, T], np.int32),
+                       np.array([start], np.int32), ws, out_dtype)
+    return ws
+
+
+@pytest.mark.parametrize("out_dtype,kpe_dtype", [(1, 1), (0, 0), (0, 1), (1, 0), (2, 0)])
+def test_pack_8192_token_chunk(orc, out_dtype, kpe_dtype):
+    pw = W.pack_workload(8192, 8192, num_blocks=256, seed=5)
+    ws = workspace(orc, pw, 8192, 0, 1 if kpe_dtype else 0)
+    kvb = pw.kv_b_proj[0]
+    gk, gv = run_pack(kvb, ws, 16, out_dtype, kpe_dtype)
+    rk, rv = oracle_pack(orc, kvb, ws, 16, out_dtype, kpe_dtype)
+    np.testing.assert_array_equal(gk, rk)
+    np.testing.assert_array_equal(gv, rv)
+
+
+@pytest.mark.parametrize("H", [1, 3, 4, 20])
+@pytest.mark.parametrize("T", [1, 77])
+def test_pack_runtime_heads_and_ragged_tokens(orc, H, T):
+    pw = W.pack_workload(T, T, num_blocks=4, seed=6, num_heads=H)
+    ws = workspace(orc, pw, T, 0, 1)
+    kvb = pw.kv_b_proj[0]
+    for out_dtype in (1, 0):
+        gk, gv = run_pack(kvb, ws, H, out_dtype, 1)
+        rk, rv = oracle_pack(orc, kvb, ws, H, out_dtype, 1)
+        np.testing.assert_array_equal(gk, rk)
+        np.testing.assert_array_equal(gv, rv)
+
+
+def test_pack_without_v(orc):
+    pw = W.pack_workload(500, 500, num_blocks=8, seed=7)
+    ws = workspace(orc, pw, 500, 0, 0)
+    gk, gv = run_pack(pw.kv_b_proj[0], ws, 16, 0, 0, with_v=False)
+    rk, _ = oracle_pack(orc, pw.kv_b_proj[0], ws, 16, 0, 0, with_v=False)
+    assert gv is None
+    np.testing.assert_array_equal(gk, rk)
+
+
+def test_pack_zero_tokens():
+    kvb = np.zeros((0, 4160), np.uint16)
+    ws = np.zeros((0, ENTRY), np.uint8)
+    gk, gv = run_pack(kvb, ws, 16, 1, 1)
+    assert gk.size == 0 and gv.size == 0
+
+
+def test_fused_pack_equals_stepwise_chain_on_gpu(orc):
+    """GPU gather -> GPU pack on the gathered fp8 k_pe equals the oracle's
+    step-by-step chain gather -> cast -> concat -> cast, for both outputs."""
+    pw = W.pack_workload(8192, 8192, num_blocks=256, seed=8)
+    cache_t = dev_cache(pw)
+    cu = np.array([0, 8192], np.int32)
+    st = np.array([0], np.int32)
+    ws_g = gpu_gather(pw, cache_t, pw.block_table, cu, st, 8192, 1)
+    kvb = pw.kv_b_proj[0]
+    T, rs = kvb.shape
+    ws_o, _ = oracle_gather(orc, pw, pw.block_table, cu, st, 8192, 1)
+    latent = orc.cast_rows(ws_o, 1, 0)
+    key_bf16 = orc.concat_key(kvb, rs, 256, np.ascontiguousarray(latent[:, 512:]), 64, T, 16,
+                              128, 64)
+    v_bf16 = np.ascontiguousarray(kvb[:, :4096].reshape(T, 16, 256)[:, :, 128:])
+    # bf16 output from the widened k_pe
+    gk, gv = run_pack(kvb, orc.cast_rows(ws_g, 1, 0), 16, 0, 0)
+    np.testing.assert_array_equal(gk, key_bf16)
+    np.testing.assert_array_equal(gv, v_bf16)
+    # fp8 output: k_nope / v cast with the scale, k_pe bytes copied raw
+    gk, gv = run_pack(kvb, ws_g, 16, 1, 1)
+    enc = lambda a: orc.fp8_encode((R.bf16_to_f32(a) / np.float32(0.01)).astype(np.float32), 1).reshape(a.shape)
+    ref_key = enc(key_bf16)
+    ref_key[:, :, 128:] = ws_o[:, None, 512:]
+    np.testing.assert_array_equal(gk, ref_key)
+    np.testing.assert_array_equal(gv, enc(v_bf16))
+
+
+def test_sixteen_chunk_pdl_chain(orc):
+    """16 chunks x 8192 tokens, each a gather into ONE reused workspace then a
+    pack, back to back on one stream with programmatic dependent launch: every
+    chunk's outputs equal the oracle's (sampled rows), so no kernel read a
+    workspace before the previous one finished writing it."""
+    pw = W.pack_workload(131072, 8192, num_blocks=2048, seed=9, distinct_chunks=False)
+    cache_t = dev_cache(pw)
+    table_t = D.dev(pw.block_table)
+    kvb = pw.kv_b_proj[0]
+    k_nope, v, _, _, _ = pack_io(kvb, np.zeros((8192, ENTRY), np.uint8), 16, 1, True)
+    ws = torch.empty((8192, ENTRY), dtype=torch.uint8, device="cuda")
+    keys = torch.empty((16, 8192, 16, 192), dtype=torch.uint8, device="cuda")
+    vs = torch.empty((16, 8192, 16, 128), dtype=torch.uint8, device="cuda")
+    sc = torch.tensor([0.01], dtype=torch.float32, device="cuda")
+    cu = D.dev(np.array([0, 8192], np.int32))
+    starts = [D.dev(np.array([c * 8192], np.int32)) for c in range(16)]
+    ops.mla_set_pdl(True)
+    for c in range(16):
+        ops.mla_context_gather(cache_t, 1, pw.num_blocks, 64, 64 * ENTRY, ENTRY, ENTRY, table_t,
+                               cu, starts[c], ws, 1)
+        ops.mla_context_kv_pack(k_nope, v, ws[:, 512:], keys[c], vs[c], 1, kpe_dtype=1,
+                                out_scale=sc)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(1)
+    keys_h, vs_h = D.host_u8(keys), D.host_u8(vs)
+    for c in range(16):
+        ws_o = workspace(orc, pw, 8192, c * 8192, 1)
+        rows = np.sort(rng.choice(8192, 256, replace=False))
+        sub = np.ascontiguousarray(kvb[rows])
+        rk, rv = oracle_pack(orc, sub, np.ascontiguousarray(ws_o[rows]), 16, 1, 1)
+        np.testing.assert_array_equal(keys_h[c][rows], rk)
+        np.testing.assert_array_equal(vs_h[c][rows], rv)
+
+
+def test_one_launch_of_131072_tokens_sampled(orc):
+    """One 131072-token pack launch (the grid is capped at the resident CTAs,
+    so every warp loops over many tokens): 4096 sampled tokens equal the
+    oracle and the output is written exactly once (guard bands intact)."""
+    T = 131072
+    g = torch.Generator().manual_seed(10)
+    kvb_t = (torch.randn((T, 4160), generator=g)).to(torch.bfloat16).cuda()
+    ws_t = torch.randint(0, 256, (T, ENTRY), generator=g, dtype=torch.int32).to(torch.uint8)
+    ws_t[(ws_t & 0x7F) == 0x7F] = 0  # finite codes only
+    ws_t = ws_t.cuda()
+    heads = kvb_t[:, :4096].view(T, 16, 256)
+    key = D.Guarded(T * 16 * 192)
+    vo = D.Guarded(T * 16 * 128)
+    sc = torch.tensor([0.01], dtype=torch.float32, device="cuda")
+    ops.mla_context_kv_pack(heads[:, :, :128], heads[:, :, 128:], ws_t[:, 512:],
+                            key.t.view(T, 16, 192), vo.t.view(T, 16, 128), 1, kpe_dtype=1,
+                            out_scale=sc)
+    torch.cuda.synchronize()
+    assert key.guards_intact() and vo.guards_intact()
+    rows = np.sort(np.random.default_rng(2).choice(T, 4096, replace=False))
+    kvb = D.host_u16(kvb_t[rows])
+    ws = D.host_u8(ws_t[rows])
+    rk, rv = oracle_pack(orc, kvb, ws, 16, 1, 1)
+    np.testing.assert_array_equal(key.host().reshape(T, 16, 192)[rows], rk)
+    np.testing.assert_array_equal(vo.host().reshape(T, 16, 128)[rows], rv)
