@@ -94,15 +94,17 @@ static fp8_format fp8_params(int fmt) {
  * (and of +-inf) to +-max: the conversion the grouped insert applies to
  * value/k_scale and the pack applies to value/out_scale ("PR #55356" Source
  * snippets, the scaled_convert branch; "PR #51772" Implementation item 1, the
- * pairwise fp8 cast).  NaN keeps its sign and becomes the all-ones NaN code.
- * The rounding is done on the exact fp32 value, never through an intermediate
- * format.
+ * pairwise fp8 cast).  Every NaN, whatever its sign, becomes the canonical
+ * NaN code 0x7F: the pages route the cast through the native pairwise
+ * converters ("PR #51772" Implementation item 1), which produce that code for
+ * a NaN input, and the OFP8 definition leaves the NaN sign open.  The rounding
+ * is done on the exact fp32 value, never through an intermediate format.
  */
 uint8_t orc_fp8_from_f32(float xf, int fmt) {
   fp8_format F = fp8_params(fmt);
   double x = (double)xf;
+  if (isnan(x)) return 0x7Fu;
   uint8_t sign = signbit(x) ? 0x80u : 0u;
-  if (isnan(x)) return (uint8_t)(sign | 0x7Fu);
   double a = fabs(x);
   double r = isinf(a) ? a : round_to_precision(a, F.p, F.emin);
   if (r > F.maxfin) r = F.maxfin; /* saturate */

@@ -7,7 +7,7 @@ are brute force or exact-rational definitions, or call library routines:
   float8 dtypes (a library routine).
 * ``fp8_nearest(x, fmt)``: round-to-nearest-even with saturation by brute force
   -- for every input, the finite code at the smallest distance, the even
-  mantissa on a tie, the sign of the input on zero.
+  mantissa on a tie, the sign of the input on zero, 0x7F for any NaN.
 * ``bf16_round_exact(x)``: the bf16 value nearest to each double, found by
   comparing exact rationals (``fractions.Fraction``) against neighbouring bf16
   candidates; ties go to the even pattern.
@@ -56,7 +56,7 @@ def fp8_nearest(x: np.ndarray, fmt: int) -> np.ndarray:
         idx = np.where(has_even, pick_even.argmax(axis=1), cand.argmax(axis=1))
         out[s:s + chunk] = pos_codes[idx].astype(np.uint8)
     out = np.where(sign, out | 0x80, out).astype(np.uint8)
-    out = np.where(nan, np.where(sign, 0xFF, 0x7F), out).astype(np.uint8)
+    out = np.where(nan, 0x7F, out).astype(np.uint8)  # canonical NaN code
     return out
 
 
