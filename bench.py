@@ -259,15 +259,18 @@ def graph_of(fn, stream):
 
 
 def time_graph(g, stream, reps):
+    """ms per replay; replay() launches on the current stream, so the replays
+    and both events run on `stream`."""
     import torch
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
-    s.record(stream)
-    for _ in range(reps):
-        g.replay()
-    e.record(stream)
+    with torch.cuda.stream(stream):
+        s.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e.record(stream)
     e.synchronize()
-    return s.elapsed_time(e) / reps  # ms per replay
+    return s.elapsed_time(e) / reps
 
 
 # ----------------------------------------------------------- CPU oracle leg
@@ -362,8 +365,9 @@ def run(args):
             w.step()
     torch.cuda.synchronize()
     step_graph = graph_of(w.step, stream)
-    for _ in range(args.warmup):
-        step_graph.replay()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step_graph.replay()
     torch.cuda.synchronize()
 
     def barrier():
@@ -375,10 +379,11 @@ def run(args):
     with ClockSampler(local) as clk:
         barrier()
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        start.record(stream)
-        for _ in range(args.steps):
-            step_graph.replay()
-        end.record(stream)
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for _ in range(args.steps):
+                step_graph.replay()
+            end.record(stream)
         end.synchronize()
         barrier()
         ms = start.elapsed_time(end) / args.steps
@@ -497,13 +502,94 @@ def run_e2e(w, stream, steps):
     return {"ms": ms, "h2d": h2d, "d2h": d2h}
 
 
+def run_profile_case(name: str, launches: int) -> int:
+    """A few launches of ONE kernel on a mid-size case (inputs larger than L2,
+    a few hundred MB on the device), for ncu captures:
+      insert  32768 tokens x 5 layers, e4m3, RMSNorm+RoPE, 2048-block caches
+      gather  262144 context rows from a 4096-block fp8 cache, raw
+      pack    32768 tokens, 16 heads, fp8 e4m3 out, fp8 k_pe
+      pack_bf16  the same with bf16 output and a bf16 k_pe"""
+    import torch
+    from pack_mla_cache_gb300 import ops
+    from pack_mla_cache_gb300 import workloads as W
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = torch.device("cuda")
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
+    if name == "insert":
+        T = 32768
+        kv_c = torch.randn((L_LAYERS, T, 512), generator=g, device=dev).to(torch.bfloat16)
+        k_pe = torch.randn((L_LAYERS, T, 64), generator=g, device=dev).to(torch.bfloat16)
+        slots = torch.randperm(NB_INSERT * BS, generator=g, device=dev)[:T]
+        pos = torch.randint(0, W.MAX_POSITION, (T,), generator=g, device=dev)
+        gamma = (1 + 0.1 * torch.randn((L_LAYERS, 512), generator=g, device=dev)).to(torch.bfloat16)
+        scales = torch.rand(L_LAYERS, generator=g, device=dev) * 0.015 + 0.005
+        caches = [torch.zeros(NB_INSERT * BS * ENTRY, dtype=torch.uint8, device=dev)
+                  for _ in range(L_LAYERS)]
+        ptrs = torch.tensor([c.data_ptr() for c in caches], dtype=torch.int64, device=dev)
+        table = torch.empty((W.MAX_POSITION, 64), dtype=torch.float32, device=dev)
+        ops.mla_rope_cos_sin_cache(table, W.ROPE_BASE)
+        fn = lambda: ops.mla_cache_insert_grouped(kv_c, k_pe, slots, ptrs, scales, 1, NB_INSERT,
+                                                  BS, BS * ENTRY, ENTRY, gamma=gamma, eps=1e-6,
+                                                  positions=pos, cos_sin_cache=table)
+        nbytes = insert_bytes(T, L_LAYERS)
+    elif name == "gather":
+        T, nb = 262144, 4096
+        cache = torch.randint(0, 126, (nb * BS * ENTRY,), generator=g, device=dev, dtype=torch.int32).to(torch.uint8)
+        table = torch.randperm(nb, generator=g, device=dev).to(torch.int32)[None, :].contiguous()
+        cu = torch.tensor([0, T], dtype=torch.int32, device=dev)
+        st = torch.tensor([0], dtype=torch.int32, device=dev)
+        out = torch.empty((T, ENTRY), dtype=torch.uint8, device=dev)
+        fn = lambda: ops.mla_context_gather(cache, 1, nb, BS, BS * ENTRY, ENTRY, ENTRY, table,
+                                            cu, st, out, 1)
+        nbytes = T * B_GATHER_TOK + (T // BS) * 4
+    elif name in ("pack", "pack_bf16"):
+        T = 32768
+        bf = name == "pack_bf16"
+        kvb = torch.randn((T, ROW_STRIDE), generator=g, device=dev).to(torch.bfloat16)
+        heads = kvb[:, :HEADS * 256].view(T, HEADS, 256)
+        if bf:
+            ws = torch.randn((T, ENTRY), generator=g, device=dev).to(torch.bfloat16)
+        else:
+            ws = torch.randint(0, 126, (T, ENTRY), generator=g, device=dev, dtype=torch.int32).to(torch.uint8)
+        odt = torch.bfloat16 if bf else torch.uint8
+        key = torch.empty((T, HEADS, 192), dtype=odt, device=dev)
+        vo = torch.empty((T, HEADS, 128), dtype=odt, device=dev)
+        sc = None if bf else torch.tensor([OUT_SCALE], dtype=torch.float32, device=dev)
+        fn = lambda: ops.mla_context_kv_pack(heads[:, :, :128], heads[:, :, 128:], ws[:, 512:],
+                                             key, vo, 0 if bf else 1, kpe_dtype=0 if bf else 1,
+                                             out_scale=sc)
+        nbytes = T * (HEADS * 512 + (128 if bf else 64) + HEADS * 320 * (2 if bf else 1))
+    else:
+        raise SystemExit(f"unknown profile case {name}")
+    for _ in range(2):
+        fn()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(launches):
+        fn()
+    e.record()
+    e.synchronize()
+    us = s.elapsed_time(e) / launches * 1e3
+    print(json.dumps({"profile_case": name, "launches": launches, "us_per_launch": us,
+                      "bytes_per_launch": nbytes, "gbs": nbytes / us / 1e3}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["mine", "reference"], default="mine")
+    ap.add_argument("--profile-case", default=None,
+                    help="run a few launches of one kernel (insert, gather, pack, pack_bf16)")
+    ap.add_argument("--launches", type=int, default=3)
     args = ap.parse_args()
+    if args.profile_case:
+        return run_profile_case(args.profile_case, args.launches)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -19,7 +19,9 @@
 //     warp stores, the bf16 stores two 512-byte ones (576 / 1152-byte cache
 //     rows are whole 32-byte sectors);
 //   * k_pe with RoPE: lanes 0-3 hold the neox pairs (8l+i, 32+8l+i), so the
-//     rotation needs no shuffle;
+//     rotation needs no shuffle; each rotated element is a difference of two
+//     products evaluated with an FMA error correction (two-ulp accurate even
+//     when the products cancel);
 //   * RMSNorm: 16 squares per lane, a 5-step xor-shuffle sum, a correctly
 //     rounded reciprocal square root;
 //   * fp8: one correctly rounded division per element (ScaledDiv, one
@@ -186,8 +188,10 @@ __global__ void __launch_bounds__(kThreads) insert_kernel(const InsertArgs a) {
             const float u0 = bf16lo(a1[i]), u1 = bf16hi(a1[i]);
             const float w0 = bf16lo(a2[i]), w1 = bf16hi(a2[i]);
             const float cA = c[2 * i], cB = c[2 * i + 1], sA = sn[2 * i], sB = sn[2 * i + 1];
-            o1[i] = pack_bf16x2(fmaf(u0, cA, -(w0 * sA)), fmaf(u1, cB, -(w1 * sB)));
-            o2[i] = pack_bf16x2(fmaf(w0, cA, u0 * sA), fmaf(w1, cB, u1 * sB));
+            o1[i] = pack_bf16x2(diff_of_products(u0, cA, w0, sA),
+                                diff_of_products(u1, cB, w1, sB));
+            o2[i] = pack_bf16x2(diff_of_products(w0, cA, -u0, sA),
+                                diff_of_products(w1, cB, -u1, sB));
           }
           q0 = make_uint4(o1[0], o1[1], o1[2], o1[3]);
           q1 = make_uint4(o2[0], o2[1], o2[2], o2[3]);

@@ -71,7 +71,7 @@ __device__ __forceinline__ uint32_t pack_fp8x2(float lo, float hi) {
 // fp8x2 (low 16 bits of `w`) -> two exact bf16 values in one 32-bit word.
 // The hardware widening to f16x2 is exact for both fp8 formats, and every
 // finite f16 obtained this way is a bf16 value, so truncating the fp32 is
-// exact.  A NaN becomes the quiet NaN 0x7FC0 with the input's sign.
+// exact.  A NaN becomes the quiet NaN 0x7FC0 with the fp8 code's sign.
 template <int F>
 __device__ __forceinline__ uint32_t fp8x2_to_bf16x2(uint32_t w) {
   uint32_t h2;
@@ -85,8 +85,9 @@ __device__ __forceinline__ uint32_t fp8x2_to_bf16x2(uint32_t w) {
   asm("{ .reg .b16 a, b; mov.b32 {a, b}, %2; cvt.f32.f16 %0, a; cvt.f32.f16 %1, b; }"
       : "=f"(f0), "=f"(f1) : "r"(h2));
   uint32_t b0 = __float_as_uint(f0) >> 16, b1 = __float_as_uint(f1) >> 16;
-  if (f0 != f0) b0 = (b0 & 0x8000u) | 0x7FC0u;
-  if (f1 != f1) b1 = (b1 & 0x8000u) | 0x7FC0u;
+  // the widening does not keep a NaN's sign: take it from the fp8 byte
+  if (f0 != f0) b0 = ((in & 0x80u) << 8) | 0x7FC0u;
+  if (f1 != f1) b1 = (in & 0x8000u) | 0x7FC0u;
   return b0 | (b1 << 16);
 }
 
@@ -134,6 +135,18 @@ __device__ __forceinline__ uint4 fp8x8_to_bf16x8(uint2 v) {
   o.z = fp8x2_to_bf16x2<F>(v.y);
   o.w = fp8x2_to_bf16x2<F>(v.y >> 16);
   return o;
+}
+
+// a*b - c*d accurate to two ulps even when the products cancel: the rounding
+// error of c*d is recovered exactly by an FMA and added back (W. Kahan's
+// algorithm; error bound by Jeannerod, Louvet and Muller, "Further analysis of
+// Kahan's algorithm for the accurate computation of 2x2 determinants", Math.
+// Comp. 82, 2013).
+__device__ __forceinline__ float diff_of_products(float a, float b, float c, float d) {
+  const float w = __fmul_rn(c, d);
+  const float e = fmaf(-c, d, w);
+  const float f = fmaf(a, b, -w);
+  return __fadd_rn(f, e);
 }
 
 __device__ __forceinline__ float warp_sum(float v) {

@@ -150,9 +150,12 @@ def mla_context_gather(kv_cache, cache_dtype, num_blocks, block_size, block_stri
     [S, W]; out [num_tokens, >= entry_dim] with unit last stride."""
     S = chunk_starts.shape[0]
     n = out.shape[0] if num_tokens is None else num_tokens
+    # row width of the table: its row stride (a one-row table's stride is not
+    # meaningful, so its width is used)
+    bt_stride = block_table.stride(0) if block_table.size(0) > 1 else block_table.size(1)
     _check(lib().mla_context_gather(
         _ptr(kv_cache), dtype_code(cache_dtype), num_blocks, block_size, block_stride,
-        entry_stride, entry_dim, _ptr(block_table), block_table.stride(0), _ptr(cu_chunk_lens),
+        entry_stride, entry_dim, _ptr(block_table), bt_stride, _ptr(cu_chunk_lens),
         _ptr(chunk_starts), S, n, _ptr(out), out.stride(0), dtype_code(out_dtype),
         _ptr(err_word), _stream(stream)))
 

@@ -165,7 +165,7 @@ def pack_workload(num_tokens: int, chunk: int, num_blocks: int, block_size: int 
     g = _gen(seed)
     nblk_ctx = (num_tokens + block_size - 1) // block_size
     assert nblk_ctx <= num_blocks
-    table = torch.randperm(num_blocks, generator=g)[:nblk_ctx].to(torch.int32).numpy()[None, :]
+    table = torch.randperm(num_blocks, generator=g)[:nblk_ctx].to(torch.int32).numpy()[None, :].copy()
     vals = torch.randn((num_blocks * block_size * ENTRY,), generator=g, dtype=torch.float32)
     if cache_dtype == 0:
         cache = vals.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)

@@ -218,11 +218,16 @@ def test_rotation_arithmetic_on_a_shared_random_table(orc):
 
 
 def test_rope_table_matches_oracle(orc):
+    """Both tables evaluate the angle in double precision, but the device's and
+    the host library's pow() may differ in the last double bit, which moves an
+    angle of up to ~3.3e4 rad by up to ~2e-11.  So each entry is within one fp32
+    ulp of the oracle's, or within 2^-35 absolute (near the zeros of cos/sin)."""
     t = D.gpu_rope_table().cpu().numpy()
     r = orc.rope_cos_sin_cache(W.MAX_POSITION, 64, W.ROPE_BASE)
-    d = np.abs(t.view(np.int32).astype(np.int64) - r.view(np.int32).astype(np.int64))
-    assert d.max() <= 1  # at most one fp32 ulp
-    assert (d != 0).mean() < 1e-3
+    diff = np.abs(t.astype(np.float64) - r.astype(np.float64))
+    bound = np.maximum(np.spacing(np.abs(r)).astype(np.float64), 2.0 ** -35)
+    assert (diff <= bound).all(), diff[diff > bound][:10]
+    assert (t != r).mean() < 1e-3
 
 
 # ----------------------------------------------------- full size, as benchmarked
