@@ -508,6 +508,7 @@ def run_profile_case(name: str, launches: int) -> int:
       insert  32768 tokens x 5 layers, e4m3, RMSNorm+RoPE, 2048-block caches
       gather  262144 context rows from a 4096-block fp8 cache, raw
       pack    32768 tokens, 16 heads, fp8 e4m3 out, fp8 k_pe
+      pack_plain the same with the bulk-copy pipeline variant disabled
       pack_bf16  the same with bf16 output and a bf16 k_pe"""
     import torch
     from pack_mla_cache_gb300 import ops
@@ -544,9 +545,10 @@ def run_profile_case(name: str, launches: int) -> int:
         fn = lambda: ops.mla_context_gather(cache, 1, nb, BS, BS * ENTRY, ENTRY, ENTRY, table,
                                             cu, st, out, 1)
         nbytes = T * B_GATHER_TOK + (T // BS) * 4
-    elif name in ("pack", "pack_bf16"):
+    elif name in ("pack", "pack_bf16", "pack_plain"):
         T = 32768
         bf = name == "pack_bf16"
+        ops.mla_set_bulk_copy(name != "pack_plain")
         kvb = torch.randn((T, ROW_STRIDE), generator=g, device=dev).to(torch.bfloat16)
         heads = kvb[:, :HEADS * 256].view(T, HEADS, 256)
         if bf:
@@ -585,7 +587,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["mine", "reference"], default="mine")
     ap.add_argument("--profile-case", default=None,
-                    help="run a few launches of one kernel (insert, gather, pack, pack_bf16)")
+                    help="run a few launches of one kernel (insert, gather, pack, pack_plain, pack_bf16)")
     ap.add_argument("--launches", type=int, default=3)
     args = ap.parse_args()
     if args.profile_case:

@@ -74,7 +74,8 @@ enum {
   MLA_ERRBIT_SLOT_OOB = 1u,   /* slot >= num_blocks * block_size */
   MLA_ERRBIT_BLOCK_OOB = 2u,  /* block table index or block id out of range */
   MLA_ERRBIT_POS_OOB = 4u,    /* position outside [0, max_position) */
-  MLA_ERRBIT_MISALIGNED = 8u  /* a per-layer cache base not 16-byte aligned */
+  MLA_ERRBIT_MISALIGNED = 8u, /* a per-layer cache base not 16-byte aligned */
+  MLA_ERRBIT_TIMEOUT = 16u     /* a pipeline wait gave up (see mla_context_kv_pack) */
 };
 
 /* Map a vLLM kv-cache-dtype string to mla_dtype_t; -1 if it is not one of
@@ -91,6 +92,13 @@ const char* mla_version(void);
 /* Enable (1, the default) or disable (0) programmatic dependent launch for
  * every later launch from this process.  Returns the previous setting. */
 int mla_set_pdl(int enable);
+
+/* Enable (1, the default) or disable (0) the bulk-copy pipeline variants of
+ * the kernels (shared-memory staging by cp.async.bulk) for every later launch
+ * from this process; when disabled, or when a call's layout does not qualify,
+ * the plain vectorised variant runs.  Both compute identical results.
+ * Returns the previous setting. */
+int mla_set_bulk_copy(int enable);
 
 /*
  * Optional pre-processing of the grouped insert ("PR #50585", Source snippets:
@@ -155,8 +163,14 @@ typedef struct {
  *                       (elements of the cache type).
  *   norm_rope           NULL, or the optional RMSNorm / RoPE (above).
  *   err_word            NULL, or a device uint32 that receives MLA_ERRBIT_*.
+ * num_layers must be at most 128 (else MLA_ERR_UNSUPPORTED).
  * Valid slots must be distinct within a layer (else the row written last is
  * unspecified).
+ * For 4096 or more rows with dense layer-major inputs (token strides 512 and
+ * 64), a 16-byte aligned slot mapping (and positions) and an even
+ * slot_layer_stride, the bulk-copy pipeline shape runs (see mla_set_bulk_copy);
+ * err_word then also receives MLA_ERRBIT_TIMEOUT if a pipeline wait ever gave
+ * up (bounded at 2 s).
  */
 mla_status_t mla_cache_insert_grouped(
     const void* kv_c, int64_t kvc_token_stride, int64_t kvc_layer_stride,
@@ -225,13 +239,20 @@ mla_status_t mla_context_gather(
  *   v_out               contiguous [T, H, v_dim] of out_dtype, or NULL = no V.
  *   out_scale           device fp32 scalar for fp8 output (NULL = 1.0); must be
  *                       NULL for bf16 output.
+ *   err_word            NULL, or a device uint32 that receives MLA_ERRBIT_TIMEOUT
+ *                       if a wait of the bulk-copy pipeline ever gave up (its
+ *                       waits are bounded at 2 s, so a fault elsewhere cannot
+ *                       hang the kernel); the outputs are then incomplete.
+ * When k_nope and v are the two halves of one [T, H, 256] buffer (head stride
+ * 256, v = k_nope + 128), v_out is set, H <= 16 and the k_pe rows are 16-byte
+ * aligned, the bulk-copy pipeline variant runs (see mla_set_bulk_copy).
  */
 mla_status_t mla_context_kv_pack(
     const void* k_nope, int64_t kn_token_stride, int64_t kn_head_stride, const void* v,
     int64_t v_token_stride, int64_t v_head_stride, const void* k_pe, int64_t kpe_token_stride,
     mla_dtype_t kpe_dtype, int32_t num_tokens, int32_t num_heads, int32_t nope_dim,
     int32_t rope_dim, int32_t v_dim, void* key_out, void* v_out, mla_dtype_t out_dtype,
-    const float* out_scale, mla_stream_t stream);
+    const float* out_scale, uint32_t* err_word, mla_stream_t stream);
 
 /*
  * Fill the rotary cos/sin table the insert's RoPE reads ("PR #50585", Source

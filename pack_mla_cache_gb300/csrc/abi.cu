@@ -24,6 +24,7 @@ namespace {
 
 thread_local std::string g_err;
 std::atomic<int> g_pdl{1};
+std::atomic<int> g_bulk{1};
 
 mla_status_t fail(mla_status_t st, const char* fmt, ...) {
   char buf[512];
@@ -92,11 +93,12 @@ mla::LaunchCfg cfg_for(mla_stream_t stream) {
 
 namespace mla {
 
-int capped_grid(const void* kernel, int threads, int64_t work_ctas) {
+int capped_grid(const void* kernel, int threads, int64_t work_ctas, int dyn_smem) {
   struct Entry {
     int dev;
     const void* kernel;
     int threads;
+    int smem;
     int resident;
   };
   static std::mutex mu;
@@ -107,14 +109,15 @@ int capped_grid(const void* kernel, int threads, int64_t work_ctas) {
   {
     std::lock_guard<std::mutex> lk(mu);
     for (const Entry& e : cache)
-      if (e.dev == dev && e.kernel == kernel && e.threads == threads) resident = e.resident;
+      if (e.dev == dev && e.kernel == kernel && e.threads == threads && e.smem == dyn_smem)
+        resident = e.resident;
     if (resident == 0) {
       int sms = 0, occ = 0;
       (void)cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-      (void)cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, threads, 0);
+      (void)cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, threads, dyn_smem);
       (void)cudaGetLastError();
       resident = (sms > 0 ? sms : 1) * (occ > 0 ? occ : 1);
-      cache.push_back(Entry{dev, kernel, threads, resident});
+      cache.push_back(Entry{dev, kernel, threads, dyn_smem, resident});
     }
   }
   if (work_ctas < 1) work_ctas = 1;
@@ -139,6 +142,8 @@ const char* mla_version(void) { return "mla_cache 1.0 sm_103a"; }
 
 int mla_set_pdl(int enable) { return g_pdl.exchange(enable ? 1 : 0); }
 
+int mla_set_bulk_copy(int enable) { return g_bulk.exchange(enable ? 1 : 0); }
+
 mla_status_t mla_cache_insert_grouped(
     const void* kv_c, int64_t kvc_token_stride, int64_t kvc_layer_stride, const void* k_pe,
     int64_t kpe_token_stride, int64_t kpe_layer_stride, int32_t num_tokens, int32_t num_layers,
@@ -148,6 +153,7 @@ mla_status_t mla_cache_insert_grouped(
     const mla_norm_rope_t* norm_rope, uint32_t* err_word, mla_stream_t stream) {
   if (num_tokens < 0) return fail(MLA_ERR_INVALID_ARG, "num_tokens must be >= 0");
   if (num_layers <= 0) return fail(MLA_ERR_INVALID_ARG, "num_layers must be >= 1");
+  if (num_layers > 128) return fail(MLA_ERR_UNSUPPORTED, "at most 128 layers per call are built");
   if (!valid_dtype(cache_dtype))
     return fail(MLA_ERR_INVALID_ARG,
                 "cache_dtype must be MLA_BF16, MLA_FP8_E4M3 or MLA_FP8_E5M2; got %d",
@@ -242,6 +248,7 @@ mla_status_t mla_cache_insert_grouped(
     a.max_position = norm_rope->max_position;
   }
   a.err = err_word;
+  a.use_tma = g_bulk.load() != 0;
   return launched(mla::launch_insert(a, (int)cache_dtype, norm, rope, cfg_for(stream)),
                   "mla_cache_insert_grouped");
 }
@@ -317,7 +324,7 @@ mla_status_t mla_context_kv_pack(const void* k_nope, int64_t kn_token_stride,
                                  int32_t num_tokens, int32_t num_heads, int32_t nope_dim,
                                  int32_t rope_dim, int32_t v_dim, void* key_out, void* v_out,
                                  mla_dtype_t out_dtype, const float* out_scale,
-                                 mla_stream_t stream) {
+                                 uint32_t* err_word, mla_stream_t stream) {
   if (num_tokens < 0) return fail(MLA_ERR_INVALID_ARG, "num_tokens must be >= 0");
   if (num_heads <= 0) return fail(MLA_ERR_INVALID_ARG, "num_heads must be >= 1");
   if (!valid_dtype(out_dtype) || !valid_dtype(kpe_dtype))
@@ -342,6 +349,8 @@ mla_status_t mla_context_kv_pack(const void* k_nope, int64_t kn_token_stride,
     return fail(MLA_ERR_MISALIGNED, "key_out and v_out must be 16-byte aligned");
   if (out_scale && (reinterpret_cast<uintptr_t>(out_scale) & 3))
     return fail(MLA_ERR_MISALIGNED, "out_scale must be 4-byte aligned");
+  if (err_word && (reinterpret_cast<uintptr_t>(err_word) & 3))
+    return fail(MLA_ERR_MISALIGNED, "err_word must be 4-byte aligned");
   if (num_tokens == 0) return MLA_OK;  // empty inputs may have null data pointers
   if (!k_nope || !k_pe || !key_out || (v_out && !v))
     return fail(MLA_ERR_INVALID_ARG, "k_nope, k_pe, key_out (and v when v_out is set) must be non-null");
@@ -362,6 +371,8 @@ mla_status_t mla_context_kv_pack(const void* k_nope, int64_t kn_token_stride,
   a.key = static_cast<uint8_t*>(key_out);
   a.vout = static_cast<uint8_t*>(v_out);
   a.out_scale = out_scale;
+  a.err = err_word;
+  a.use_tma = g_bulk.load() != 0;
   return launched(mla::launch_pack(a, (int)out_dtype, (int)kpe_dtype, cfg_for(stream)),
                   "mla_context_kv_pack");
 }

@@ -9,25 +9,26 @@
 // kv", Source snippets: _precompute_fused_context_kv).
 //
 // Design (not the pages' one-CTA-per-(token, layer) scalar loop):
-//   * one warp per row, ROWS rows per warp per iteration, rows in token-major
-//     order (a warp's rows share a token's slot / position / cos-sin), and a
-//     grid-stride loop over a grid capped at the resident-CTA count;
-//   * every global load of the ROWS rows is issued before the first row is
-//     processed (memory-level parallelism: 1152 B per row in flight);
-//   * kv_c: lane l holds elements [8l, 8l+8) and [256+8l, 256+8l+8) -- two
-//     fully coalesced 512-byte warp loads; the fp8 stores are two 256-byte
-//     warp stores, the bf16 stores two 512-byte ones (576 / 1152-byte cache
-//     rows are whole 32-byte sectors);
-//   * k_pe with RoPE: lanes 0-3 hold the neox pairs (8l+i, 32+8l+i), so the
-//     rotation needs no shuffle; each rotated element is a difference of two
-//     products evaluated with an FMA error correction (two-ulp accurate even
-//     when the products cancel);
-//   * RMSNorm: 16 squares per lane, a 5-step xor-shuffle sum, a correctly
-//     rounded reciprocal square root;
-//   * fp8: one correctly rounded division per element (ScaledDiv, one
-//     reciprocal per row) then the hardware .satfinite pairwise converter;
-//   * dtype, norm, rope and ROWS are template parameters: the hot loop has no
-//     runtime format branches.
+//   * one warp per row.  kv_c: lane l holds elements [8l, 8l+8) and
+//     [256+8l, 256+8l+8) -- two fully coalesced 512-byte warp loads; the fp8
+//     stores are two 256-byte warp stores, the bf16 stores two 512-byte ones.
+//     k_pe: lane l holds the neox pair (l, l+32), so the rotation needs no
+//     shuffle and every lane does one pair;
+//   * RMSNorm: 16 squares per lane on packed fp32x2 FMAs, a 5-step xor-shuffle
+//     sum, a correctly rounded reciprocal square root;
+//   * RoPE: each rotated element is a difference of two products with an FMA
+//     error correction (two-ulp accurate even when the products cancel);
+//   * fp8: a correctly rounded division per element on packed fp32x2 pairs
+//     (one reciprocal per row), then the hardware .satfinite pairwise
+//     converter;
+//   * three launch shapes: small batches run one warp per (token, layer) row
+//     so the few rows spread over the most SMs (latency); large batches of
+//     dense layer-major rows run the bulk-copy pipeline (below); other large
+//     batches (e.g. the [T, L, 576] projection read in place) run one warp per
+//     token over its layers, kLG rows' loads issued before the first is
+//     processed; all loop over a grid capped at the resident-CTA count;
+//   * dtype, norm and rope are template parameters: no runtime format branches
+//     in the hot loop.
 #include "mla_device.cuh"
 #include "mla_internal.h"
 
@@ -37,205 +38,437 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kR = 512;  // kv_lora_rank
 constexpr int kP = 64;   // pe_dim
+constexpr int kLG = 4;   // rows of one token loaded together (token-loop shape)
 
-template <int F, bool NORM, bool ROPE, int ROWS>
-__global__ void __launch_bounds__(kThreads) insert_kernel(const InsertArgs a) {
+struct RowIn {
+  uint4 x0, x1;     // kv_c elements [8l, 8l+8) and [256+8l, 256+8l+8)
+  uint32_t pe;      // k_pe elements l (low half) and l+32 (high half)
+  int64_t slot;
+  int64_t cptr;     // cache base of the row's layer
+  float scale;      // k_scale of the row's layer (fp8 caches)
+};
+
+__device__ __forceinline__ uint32_t ld_u16(const uint8_t* p) {
+  return __ldcs(reinterpret_cast<const unsigned short*>(p));
+}
+__device__ __forceinline__ void st_u16(uint8_t* p, uint32_t v) {
+  *reinterpret_cast<unsigned short*>(p) = static_cast<unsigned short>(v);
+}
+__device__ __forceinline__ void st_u8(uint8_t* p, uint32_t v) { *p = static_cast<uint8_t>(v); }
+
+template <int F, bool ROPE>
+__device__ __forceinline__ void load_row(const InsertArgs& a, int64_t t, int l, int lane,
+                                         RowIn& r) {
+  const uint8_t* src = a.kv_c + t * a.kvc_ts + (int64_t)l * a.kvc_ls;
+  r.x0 = ld_stream16(src + lane * 16);
+  r.x1 = ld_stream16(src + 512 + lane * 16);
+  const uint8_t* pe = a.k_pe + t * a.kpe_ts + (int64_t)l * a.kpe_ls;
+  r.pe = ld_u16(pe + lane * 2) | (ld_u16(pe + 64 + lane * 2) << 16);
+  r.slot = a.slots[(int64_t)l * a.slot_ls + t];
+  r.cptr = a.cache_ptrs[l];
+  r.scale = 1.0f;
+  if constexpr (F != kBF16) r.scale = a.scales[l];
+}
+
+// Store one finished row: bf16 words y0 / y1 (kv_c) and p (k_pe pair), raw
+// into a bf16 cache or divided by `scale` and converted into an fp8 cache.
+template <int F, bool FAST>
+__device__ __forceinline__ void write_row_k(uint8_t* dst, int lane, const uint4& y0,
+                                            const uint4& y1, uint32_t p, const DivConst& k) {
+  if constexpr (F == kBF16) {
+    st16(dst + lane * 16, y0);
+    st16(dst + 512 + lane * 16, y1);
+    st_u16(dst + 2 * kR + lane * 2, p);
+    st_u16(dst + 2 * kR + kP + lane * 2, p >> 16);
+  } else {
+    st8(dst + lane * 8, bf16x8_to_fp8x8<F, FAST>(y0, k));
+    st8(dst + 256 + lane * 8, bf16x8_to_fp8x8<F, FAST>(y1, k));
+    const uint32_t q = bf16x2_to_fp8x2<F, FAST>(p, k);
+    st_u8(dst + kR + lane, q);
+    st_u8(dst + kR + kP / 2 + lane, q >> 8);
+  }
+}
+
+template <int F>
+__device__ __forceinline__ void write_row_dc(uint8_t* dst, int lane, const uint4& y0,
+                                             const uint4& y1, uint32_t p, const DivConst& k) {
+  if (F == kBF16 || k.fast) write_row_k<F, true>(dst, lane, y0, y1, p, k);
+  else write_row_k<F, false>(dst, lane, y0, y1, p, k);
+}
+
+template <int F>
+__device__ __forceinline__ void write_row(uint8_t* dst, int lane, const uint4& y0,
+                                          const uint4& y1, uint32_t p, float scale) {
+  DivConst k{};
+  if constexpr (F != kBF16) k = div_const(scale);
+  write_row_dc<F>(dst, lane, y0, y1, p, k);
+}
+
+// RMSNorm of this lane's 16 kv_c elements (words x0 / x1) with the row's
+// gamma words g0 / g1: returns the bf16-rounded results in y0 / y1.
+__device__ __forceinline__ void rms_norm16(const uint4& x0, const uint4& x1, const uint4& g0,
+                                           const uint4& g1, float eps, uint4& y0, uint4& y1) {
+  const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+  uint64_t acc = f2(0.f, 0.f);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint64_t v = f2(bf16lo(w[i]), bf16hi(w[i]));
+    acc = fma2(v, v, acc);
+  }
+  const float2 acc2 = unf2(acc);
+  const float ss = warp_sum(acc2.x + acc2.y);
+  // mean over 512 (exact power-of-two scaling) + eps, one rounding
+  const float rstd = __frsqrt_rn(fmaf(ss, 1.0f / kR, eps));
+  const uint64_t rstd2 = f2(rstd, rstd);
+  const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+  uint32_t o[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint64_t v = f2(bf16lo(w[i]), bf16hi(w[i]));
+    const float2 y = unf2(mul2(mul2(v, rstd2), f2(bf16lo(gw[i]), bf16hi(gw[i]))));
+    o[i] = pack_bf16x2(y.x, y.y);
+  }
+  y0 = make_uint4(o[0], o[1], o[2], o[3]);
+  y1 = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// The neox rotation of this lane's k_pe pair (element lane in the low half,
+// lane+32 in the high half) by (cos, sin).
+__device__ __forceinline__ uint32_t rope_pair(uint32_t pe, float2 cs) {
+  const float u = bf16lo(pe), v = bf16hi(pe);
+  return pack_bf16x2(diff_of_products(u, cs.x, v, cs.y), diff_of_products(v, cs.x, -u, cs.y));
+}
+
+// Normalise / rotate / convert one loaded row and store it.  `cs` = (cos, sin)
+// of this lane's rotary pair.  Returns the error bits of a skipped row.
+template <int F, bool NORM, bool ROPE>
+__device__ __forceinline__ uint32_t store_row(const InsertArgs& a, int l, int lane, const RowIn& r,
+                                              bool pos_ok, float2 cs) {
+  const int64_t s = r.slot;
+  if (s < 0) return 0;  // padding slot (uniform across the warp)
+  if (s >= a.capacity) return kErrSlotOOB;
+  if (ROPE && !pos_ok) return kErrPosOOB;
+  if (r.cptr & 15) return kErrMisaligned;
+  int64_t blk, off;
+  if (a.bs_shift >= 0) {
+    blk = s >> a.bs_shift;
+    off = s & (a.block_size - 1);
+  } else {
+    blk = s / a.block_size;
+    off = s - blk * a.block_size;
+  }
+  uint8_t* dst = reinterpret_cast<uint8_t*>(r.cptr) + blk * a.block_stride + off * a.entry_stride;
+
+  // kv_c (optionally RMSNorm-ed) as bf16 words
+  uint4 y0 = r.x0, y1 = r.x1;
+  if constexpr (NORM) {
+    const uint8_t* g = a.gamma + (int64_t)l * a.gamma_ls;
+    rms_norm16(r.x0, r.x1, ld_shared_ro16(g + lane * 16), ld_shared_ro16(g + 512 + lane * 16),
+               a.eps, y0, y1);
+  }
+  // k_pe pair (l, l+32), optionally rotated
+  uint32_t p = r.pe;
+  if constexpr (ROPE) p = rope_pair(r.pe, cs);
+
+  write_row<F>(dst, lane, y0, y1, p, r.scale);
+  return 0;
+}
+
+template <bool ROPE>
+__device__ __forceinline__ bool load_rope(const InsertArgs& a, int64_t t, int lane, float2& cs) {
+  cs = make_float2(1.f, 0.f);
+  if constexpr (!ROPE) return true;
+  const int64_t pos = a.positions[t];
+  if (pos < 0 || pos >= a.max_position) return false;
+  const float* row = a.cos_sin + pos * kP;
+  cs = make_float2(__ldg(row + lane), __ldg(row + kP / 2 + lane));
+  return true;
+}
+
+// Shape 1: one warp per (token, layer) row, rows in token-major order.
+template <int F, bool NORM, bool ROPE>
+__global__ void __launch_bounds__(kThreads) insert_row_kernel(const InsertArgs a) {
   pdl_wait();
   const int lane = threadIdx.x & 31;
-  const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
   uint32_t errbits = 0;
+  for (int64_t r = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5; r < a.num_rows;
+       r += nwarps) {
+    const int64_t t = r / a.num_layers;
+    const int l = (int)(r - t * a.num_layers);
+    RowIn in;
+    load_row<F, ROPE>(a, t, l, lane, in);
+    float2 cs;
+    const bool pos_ok = load_rope<ROPE>(a, t, lane, cs);
+    errbits |= store_row<F, NORM, ROPE>(a, l, lane, in, pos_ok, cs);
+  }
+  if (errbits && lane == 0 && a.err) atomicOr(a.err, errbits);
+  pdl_trigger();
+}
 
-  for (int64_t r0 = warp * ROWS; r0 < a.num_rows; r0 += nwarps * ROWS) {
-    int32_t tok[ROWS], lay[ROWS];
-    bool live[ROWS];
-    {
-      int32_t t = (int32_t)(r0 / a.num_layers);
-      int32_t l = (int32_t)(r0 - (int64_t)t * a.num_layers);
+// Shape 2: one warp per token, its layers kLG rows at a time.
+template <int F, bool NORM, bool ROPE>
+__global__ void __launch_bounds__(kThreads) insert_token_kernel(const InsertArgs a) {
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
+  uint32_t errbits = 0;
+  for (int64_t t = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5; t < a.num_tokens;
+       t += nwarps) {
+    float2 cs;
+    const bool pos_ok = load_rope<ROPE>(a, t, lane, cs);
+    for (int l0 = 0; l0 < a.num_layers; l0 += kLG) {
+      RowIn in[kLG];
 #pragma unroll
-      for (int k = 0; k < ROWS; ++k) {
-        tok[k] = t;
-        lay[k] = l;
-        live[k] = (r0 + k) < a.num_rows;
-        if (++l == a.num_layers) {
-          l = 0;
-          ++t;
-        }
+      for (int k = 0; k < kLG; ++k) {
+        if (l0 + k < a.num_layers) load_row<F, ROPE>(a, t, l0 + k, lane, in[k]);
+        else in[k].slot = -1;
       }
-    }
-
-    // ---- issue all loads of the ROWS rows --------------------------------
-    uint4 x0[ROWS], x1[ROWS], p0[ROWS], p1[ROWS];
-    int64_t slot[ROWS], cptr[ROWS], pos[ROWS];
-    float scale[ROWS];
 #pragma unroll
-    for (int k = 0; k < ROWS; ++k) {
-      slot[k] = -1;
-      cptr[k] = 0;
-      pos[k] = 0;
-      scale[k] = 1.0f;
-      p0[k] = make_uint4(0, 0, 0, 0);
-      p1[k] = make_uint4(0, 0, 0, 0);
-      if (live[k]) {
-        const uint8_t* src = a.kv_c + (int64_t)tok[k] * a.kvc_ts + (int64_t)lay[k] * a.kvc_ls;
-        x0[k] = ld_stream16(src + lane * 16);
-        x1[k] = ld_stream16(src + 512 + lane * 16);
-        const uint8_t* pe = a.k_pe + (int64_t)tok[k] * a.kpe_ts + (int64_t)lay[k] * a.kpe_ls;
-        if constexpr (ROPE) {
-          if (lane < 4) {
-            p0[k] = ld_stream16(pe + lane * 16);       // x_i,      i in [8l, 8l+8)
-            p1[k] = ld_stream16(pe + 64 + lane * 16);  // x_{i+32}
-          }
-          pos[k] = a.positions[tok[k]];
-        } else if (lane < 8) {
-          p0[k] = ld_stream16(pe + lane * 16);
-        }
-        slot[k] = a.slots[(int64_t)lay[k] * a.slot_ls + tok[k]];
-        cptr[k] = a.cache_ptrs[lay[k]];
-        if constexpr (F != kBF16) scale[k] = a.scales[lay[k]];
-      } else {
-        x0[k] = make_uint4(0, 0, 0, 0);
-        x1[k] = make_uint4(0, 0, 0, 0);
-      }
-    }
-
-    // cos / sin of each row's position (a small L2-resident table)
-    float4 c0[ROWS], c1[ROWS], s0[ROWS], s1[ROWS];
-    if constexpr (ROPE) {
-#pragma unroll
-      for (int k = 0; k < ROWS; ++k) {
-        c0[k] = c1[k] = s0[k] = s1[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (lane < 4 && slot[k] >= 0 && pos[k] >= 0 && pos[k] < a.max_position) {
-          const float* cs = a.cos_sin + pos[k] * kP + lane * 8;
-          c0[k] = __ldg(reinterpret_cast<const float4*>(cs));
-          c1[k] = __ldg(reinterpret_cast<const float4*>(cs + 4));
-          s0[k] = __ldg(reinterpret_cast<const float4*>(cs + 32));
-          s1[k] = __ldg(reinterpret_cast<const float4*>(cs + 36));
-        }
-      }
-    }
-
-    // ---- process and store -------------------------------------------------
-#pragma unroll
-    for (int k = 0; k < ROWS; ++k) {
-      const int64_t s = slot[k];
-      if (s < 0) continue;  // padding slot (uniform across the warp)
-      if (s >= a.capacity) {
-        errbits |= kErrSlotOOB;
-        continue;
-      }
-      if constexpr (ROPE) {
-        if (pos[k] < 0 || pos[k] >= a.max_position) {
-          errbits |= kErrPosOOB;
-          continue;
-        }
-      }
-      if (cptr[k] & 15) {
-        errbits |= kErrMisaligned;
-        continue;
-      }
-      int64_t blk, off;
-      if (a.bs_shift >= 0) {
-        blk = s >> a.bs_shift;
-        off = s & (a.block_size - 1);
-      } else {
-        blk = s / a.block_size;
-        off = s - blk * a.block_size;
-      }
-      uint8_t* dst = reinterpret_cast<uint8_t*>(cptr[k]) + blk * a.block_stride + off * a.entry_stride;
-
-      // kv_c (optionally RMSNorm-ed) as bf16 words
-      uint4 y0 = x0[k], y1 = x1[k];
-      if constexpr (NORM) {
-        const uint32_t w[8] = {x0[k].x, x0[k].y, x0[k].z, x0[k].w,
-                               x1[k].x, x1[k].y, x1[k].z, x1[k].w};
-        float v[16];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          v[2 * i] = bf16lo(w[i]);
-          v[2 * i + 1] = bf16hi(w[i]);
-        }
-        float ss = 0.f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) ss = fmaf(v[i], v[i], ss);
-        ss = warp_sum(ss);
-        // mean over 512 (exact power-of-two scaling) + eps, one rounding
-        const float rstd = __frsqrt_rn(fmaf(ss, 1.0f / kR, a.eps));
-        const uint8_t* g = a.gamma + (int64_t)lay[k] * a.gamma_ls;
-        const uint4 g0 = ld_shared_ro16(g + lane * 16);
-        const uint4 g1 = ld_shared_ro16(g + 512 + lane * 16);
-        const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-        uint32_t o[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          o[i] = pack_bf16x2((v[2 * i] * rstd) * bf16lo(gw[i]),
-                             (v[2 * i + 1] * rstd) * bf16hi(gw[i]));
-        y0 = make_uint4(o[0], o[1], o[2], o[3]);
-        y1 = make_uint4(o[4], o[5], o[6], o[7]);
-      }
-
-      // k_pe (optionally rotated) as bf16 words: q0 first half, q1 second half
-      uint4 q0 = p0[k], q1 = p1[k];
-      if constexpr (ROPE) {
-        if (lane < 4) {
-          const uint32_t a1[4] = {p0[k].x, p0[k].y, p0[k].z, p0[k].w};
-          const uint32_t a2[4] = {p1[k].x, p1[k].y, p1[k].z, p1[k].w};
-          const float c[8] = {c0[k].x, c0[k].y, c0[k].z, c0[k].w, c1[k].x, c1[k].y, c1[k].z, c1[k].w};
-          const float sn[8] = {s0[k].x, s0[k].y, s0[k].z, s0[k].w, s1[k].x, s1[k].y, s1[k].z, s1[k].w};
-          uint32_t o1[4], o2[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float u0 = bf16lo(a1[i]), u1 = bf16hi(a1[i]);
-            const float w0 = bf16lo(a2[i]), w1 = bf16hi(a2[i]);
-            const float cA = c[2 * i], cB = c[2 * i + 1], sA = sn[2 * i], sB = sn[2 * i + 1];
-            o1[i] = pack_bf16x2(diff_of_products(u0, cA, w0, sA),
-                                diff_of_products(u1, cB, w1, sB));
-            o2[i] = pack_bf16x2(diff_of_products(w0, cA, -u0, sA),
-                                diff_of_products(w1, cB, -u1, sB));
-          }
-          q0 = make_uint4(o1[0], o1[1], o1[2], o1[3]);
-          q1 = make_uint4(o2[0], o2[1], o2[2], o2[3]);
-        }
-      }
-
-      if constexpr (F == kBF16) {
-        st16(dst + lane * 16, y0);
-        st16(dst + 512 + lane * 16, y1);
-        if constexpr (ROPE) {
-          if (lane < 4) {
-            st16(dst + 2 * kR + lane * 16, q0);
-            st16(dst + 2 * kR + 64 + lane * 16, q1);
-          }
-        } else if (lane < 8) {
-          st16(dst + 2 * kR + lane * 16, q0);
-        }
-      } else {
-        const ScaledDiv d(scale[k]);
-        st8(dst + lane * 8, bf16x8_to_fp8x8<F>(y0, d));
-        st8(dst + 256 + lane * 8, bf16x8_to_fp8x8<F>(y1, d));
-        if constexpr (ROPE) {
-          if (lane < 4) {
-            st8(dst + kR + lane * 8, bf16x8_to_fp8x8<F>(q0, d));
-            st8(dst + kR + 32 + lane * 8, bf16x8_to_fp8x8<F>(q1, d));
-          }
-        } else if (lane < 8) {
-          st8(dst + kR + lane * 8, bf16x8_to_fp8x8<F>(q0, d));
-        }
-      }
+      for (int k = 0; k < kLG; ++k)
+        errbits |= store_row<F, NORM, ROPE>(a, l0 + k, lane, in[k], pos_ok, cs);
     }
   }
   if (errbits && lane == 0 && a.err) atomicOr(a.err, errbits);
   pdl_trigger();
 }
 
-template <int F, bool NORM, bool ROPE, int ROWS>
-cudaError_t launch_t(const InsertArgs& a, const LaunchCfg& cfg) {
-  auto kern = insert_kernel<F, NORM, ROPE, ROWS>;
-  const int64_t warps = (a.num_rows + ROWS - 1) / ROWS;
-  const int64_t ctas = (warps + kThreads / 32 - 1) / (kThreads / 32);
+// Shape 3 (bulk-copy pipeline): for dense per-layer rows (kv_c token stride
+// 512, k_pe token stride 64 -- the layer-major [L, T, .] buffers), one layer's
+// run of kRun consecutive tokens is contiguous.  A work item is such a run: a
+// producer warp streams its kv_c rows, k_pe rows, slots and positions into a
+// ring of 32 shared-memory stages with cp.async.bulk (byte-counted on a
+// per-stage mbarrier; lane s of the producer fills stage s), and 16 consumer
+// warps process the rows from shared memory (the
+// rotary cos/sin of the item's rows are loaded together, the layer's gamma once
+// per item).  Each consumer owns the stages s == warp (mod kIConsumers) and
+// takes their fills in order, so no parity wait can alias an older phase.
+constexpr int kRun = 4;
+constexpr int kIConsumers = 16;
+constexpr int kIStages = kIConsumers * 2;
+static_assert(kIStages == 32, "producer lane s owns stage s");
+constexpr int kIThreads = (kIConsumers + 1) * 32;
+constexpr int kOffPe = kRun * 2 * kR;              // k_pe rows after the kv_c rows
+constexpr int kOffSlot = kOffPe + kRun * 2 * kP;   // then the slots
+constexpr int kOffPos = kOffSlot + kRun * 8;       // then the positions
+constexpr int kIStageBytes = kOffPos + kRun * 8;   // 4672
+constexpr int kMaxLayers = 128;
+constexpr int kOffBars = kIStages * kIStageBytes;
+constexpr int kOffLayers = kOffBars + 2 * kIStages * 8 + 16;
+constexpr int kISmem = kOffLayers + kMaxLayers * (8 + 4 + 4 + 4);
+constexpr uint64_t kIWaitLimitNs = 2000000000ull;  // 2 s: a wait that long means a fault
+
+template <int F, bool NORM, bool ROPE, bool FAST>
+__device__ __forceinline__ uint32_t insert_consume_item(
+    const InsertArgs& a, uint32_t src, const uint8_t* stage, int64_t t0, int nt, int l,
+    int lane, int64_t cptr, const DivConst& k) {
+  uint32_t err = 0;
+  // per-row metadata: from the stage for a full run, from global for the tail
+  int64_t slot[kRun], pos[kRun];
+#pragma unroll
+  for (int r = 0; r < kRun; ++r) {
+    slot[r] = -1;
+    pos[r] = 0;
+    if (r < nt) {
+      if (nt == kRun) {
+        slot[r] = reinterpret_cast<const int64_t*>(stage + kOffSlot)[r];
+        if (ROPE) pos[r] = reinterpret_cast<const int64_t*>(stage + kOffPos)[r];
+      } else {
+        slot[r] = a.slots[(int64_t)l * a.slot_ls + t0 + r];
+        if (ROPE) pos[r] = a.positions[t0 + r];
+      }
+    }
+  }
+  float2 cs[kRun];
+#pragma unroll
+  for (int r = 0; r < kRun; ++r) {
+    cs[r] = make_float2(1.f, 0.f);
+    if (ROPE && slot[r] >= 0 && pos[r] >= 0 && pos[r] < a.max_position) {
+      const float* row = a.cos_sin + pos[r] * kP;
+      cs[r] = make_float2(__ldg(row + lane), __ldg(row + kP / 2 + lane));
+    }
+  }
+  uint4 g0 = make_uint4(0, 0, 0, 0), g1 = g0;
+  if constexpr (NORM) {
+    const uint8_t* g = a.gamma + (int64_t)l * a.gamma_ls;
+    g0 = ld_shared_ro16(g + lane * 16);
+    g1 = ld_shared_ro16(g + 512 + lane * 16);
+  }
+#pragma unroll
+  for (int r = 0; r < kRun; ++r) {
+    const int64_t s = slot[r];
+    if (r >= nt || s < 0) continue;  // padding slot
+    if (s >= a.capacity) { err |= kErrSlotOOB; continue; }
+    if (ROPE && (pos[r] < 0 || pos[r] >= a.max_position)) { err |= kErrPosOOB; continue; }
+    if (cptr & 15) { err |= kErrMisaligned; continue; }
+    int64_t blk, off;
+    if (a.bs_shift >= 0) {
+      blk = s >> a.bs_shift;
+      off = s & (a.block_size - 1);
+    } else {
+      blk = s / a.block_size;
+      off = s - blk * a.block_size;
+    }
+    uint8_t* dst = reinterpret_cast<uint8_t*>(cptr) + blk * a.block_stride + off * a.entry_stride;
+    const uint32_t row = src + r * 2 * kR;
+    const uint4 x0 = lds16(row + lane * 16), x1 = lds16(row + 512 + lane * 16);
+    uint32_t pe;
+    {
+      const uint32_t pr = src + kOffPe + r * 2 * kP + lane * 2;
+      uint32_t lo, hi;
+      asm volatile("ld.shared.u16 %0, [%1];" : "=r"(lo) : "r"(pr));
+      asm volatile("ld.shared.u16 %0, [%1];" : "=r"(hi) : "r"(pr + kP));
+      pe = lo | (hi << 16);
+    }
+    uint4 y0 = x0, y1 = x1;
+    if constexpr (NORM) rms_norm16(x0, x1, g0, g1, a.eps, y0, y1);
+    uint32_t p = pe;
+    if constexpr (ROPE) p = rope_pair(pe, cs[r]);
+    write_row_k<F, FAST>(dst, lane, y0, y1, p, k);
+  }
+  return err;
+}
+
+template <int F, bool NORM, bool ROPE>
+__global__ void __launch_bounds__(kIThreads, 1) insert_tma_kernel(const InsertArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kIStages);
+  int64_t* s_cptr = reinterpret_cast<int64_t*>(smem + kOffLayers);
+  float* s_scale = reinterpret_cast<float*>(s_cptr + kMaxLayers);
+  float* s_rcp = s_scale + kMaxLayers;
+  int* s_fast = reinterpret_cast<int*>(s_rcp + kMaxLayers);
+  const uint32_t stage0 = smem_addr(smem);
+  const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + kIStages);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kIStages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  pdl_wait();
+  for (int l = threadIdx.x; l < a.num_layers; l += kIThreads) {
+    s_cptr[l] = a.cache_ptrs[l];
+    float sc = 1.0f;
+    if constexpr (F != kBF16) sc = a.scales[l];
+    const DivConst k = div_const(sc);
+    s_scale[l] = sc;
+    s_rcp[l] = k.y;
+    s_fast[l] = k.fast ? 1 : 0;
+  }
+  __syncthreads();
+
+  const int L = a.num_layers;
+  const int64_t runs = ((int64_t)a.num_tokens + kRun - 1) / kRun;
+  const int64_t n_items = runs * L;
+  const int64_t G = gridDim.x, b = blockIdx.x;
+  const int64_t n_local = n_items > b ? (n_items - 1 - b) / G + 1 : 0;
+  int64_t fills = 0;  // producer lane: fills issued to its stage
+  uint32_t errbits = 0;
+
+  if (warp == kIConsumers) {
+    // ---------------- producer: lane s fills stage s -----------------------------
+    // (one issuing lane sustains only about one bulk copy per ~270 cycles, so
+    // all 32 lanes issue, each for its own stage)
+    {
+      const int s = lane;
+      for (int64_t i = lane; i < n_local; i += kIStages) {
+        const int64_t n = i / kIStages;
+        if (n > 0 && !mbar_wait(empty0 + 8 * s, (uint32_t)((n - 1) & 1), kIWaitLimitNs)) {
+          *abort_flag = 1;
+          break;
+        }
+        if (*abort_flag) break;
+        const int64_t j = b + G * i;
+        const int64_t run = j / L;
+        const int l = (int)(j - run * L);
+        const int64_t t0 = run * kRun;
+        const int nt = (int)min((int64_t)kRun, (int64_t)a.num_tokens - t0);
+        const uint32_t dst = stage0 + (uint32_t)(s * kIStageBytes);
+        const uint32_t meta = nt == kRun ? (ROPE ? 2u : 1u) * kRun * 8u : 0u;
+        mbar_arrive_expect_tx(full0 + 8 * s, (uint32_t)nt * (2 * kR + 2 * kP) + meta);
+        bulk_g2s(dst, a.kv_c + t0 * a.kvc_ts + (int64_t)l * a.kvc_ls, (uint32_t)nt * 2 * kR,
+                 full0 + 8 * s);
+        bulk_g2s(dst + kOffPe, a.k_pe + t0 * a.kpe_ts + (int64_t)l * a.kpe_ls,
+                 (uint32_t)nt * 2 * kP, full0 + 8 * s);
+        if (nt == kRun) {
+          bulk_g2s(dst + kOffSlot, a.slots + (int64_t)l * a.slot_ls + t0, kRun * 8, full0 + 8 * s);
+          if (ROPE) bulk_g2s(dst + kOffPos, a.positions + t0, kRun * 8, full0 + 8 * s);
+        }
+        fills = n + 1;
+      }
+    }
+  } else {
+    // ---------------- consumers --------------------------------------------------
+    for (int64_t i = warp; i < n_local; i += kIConsumers) {
+      const int s = (int)(i % kIStages);
+      if (!mbar_wait(full0 + 8 * s, (uint32_t)((i / kIStages) & 1), kIWaitLimitNs)) {
+        *abort_flag = 1;
+        break;
+      }
+      const int64_t j = b + G * i;
+      const int64_t run = j / L;
+      const int l = (int)(j - run * L);
+      const int64_t t0 = run * kRun;
+      const int nt = (int)min((int64_t)kRun, (int64_t)a.num_tokens - t0);
+      const uint32_t src = stage0 + (uint32_t)(s * kIStageBytes);
+      const uint8_t* stage = smem + (size_t)s * kIStageBytes;
+      DivConst k;
+      k.b = s_scale[l];
+      k.y = s_rcp[l];
+      k.fast = s_fast[l] != 0;
+      k.y2 = f2(k.y, k.y);
+      k.nb2 = f2(-k.b, -k.b);
+      const int64_t cptr = s_cptr[l];
+      if (F == kBF16 || k.fast)
+        errbits |= insert_consume_item<F, NORM, ROPE, true>(a, src, stage, t0, nt, l, lane, cptr, k);
+      else
+        errbits |= insert_consume_item<F, NORM, ROPE, false>(a, src, stage, t0, nt, l, lane, cptr, k);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * s);
+    }
+  }
+  __syncthreads();
+  if (*abort_flag) {
+    // Let every copy this CTA issued land before its shared memory is released.
+    if (warp == kIConsumers && fills > 0)
+      (void)mbar_wait(full0 + 8 * lane, (uint32_t)((fills - 1) & 1), kIWaitLimitNs / 8);
+    errbits |= kErrTimeout;
+  }
+  if (errbits && lane == 0 && a.err) atomicOr(a.err, errbits);
+  pdl_trigger();
+}
+
+// The bulk-copy shape needs dense per-layer token rows and 16-byte aligned
+// slot / position runs.
+bool insert_tma_layout(const InsertArgs& a, bool rope) {
+  return a.use_tma && a.kvc_ts == 2 * kR && a.kpe_ts == 2 * kP && a.num_layers <= kMaxLayers &&
+         (reinterpret_cast<uintptr_t>(a.slots) & 15) == 0 && ((a.slot_ls * 8) & 15) == 0 &&
+         (!rope || (reinterpret_cast<uintptr_t>(a.positions) & 15) == 0);
+}
+
+// Below this many rows the row-per-warp shape wins (more SMs on few rows).
+constexpr int64_t kTokenShapeMinRows = 4096;
+
+template <int F, bool NORM, bool ROPE>
+cudaError_t launch_tma(const InsertArgs& a, const LaunchCfg& cfg) {
+  auto kern = insert_tma_kernel<F, NORM, ROPE>;
+  static bool configured = false;  // per instance
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kISmem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int64_t items = ((int64_t)a.num_tokens + kRun - 1) / kRun * a.num_layers;
   cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3(capped_grid(reinterpret_cast<const void*>(kern), kThreads, ctas));
-  lc.blockDim = dim3(kThreads);
+  lc.gridDim = dim3(capped_grid(reinterpret_cast<const void*>(kern), kIThreads,
+                                (items + kIConsumers - 1) / kIConsumers, kISmem));
+  lc.blockDim = dim3(kIThreads);
+  lc.dynamicSmemBytes = kISmem;
   lc.stream = cfg.stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -246,19 +479,33 @@ cudaError_t launch_t(const InsertArgs& a, const LaunchCfg& cfg) {
 }
 
 template <int F, bool NORM, bool ROPE>
-cudaError_t launch_rows(const InsertArgs& a, const LaunchCfg& cfg) {
-  // Few rows: one row per warp spreads them over the most SMs (latency);
-  // many rows: several rows per warp keep more bytes in flight per SM.
-  if (a.num_rows >= (int64_t)1 << 15) return launch_t<F, NORM, ROPE, (NORM || ROPE) ? 2 : 4>(a, cfg);
-  return launch_t<F, NORM, ROPE, 1>(a, cfg);
+cudaError_t launch_t(const InsertArgs& a, const LaunchCfg& cfg) {
+  if (a.num_rows >= kTokenShapeMinRows && insert_tma_layout(a, ROPE))
+    return launch_tma<F, NORM, ROPE>(a, cfg);
+  const bool token_shape = a.num_rows >= kTokenShapeMinRows;
+  const void* kern = token_shape ? reinterpret_cast<const void*>(insert_token_kernel<F, NORM, ROPE>)
+                                 : reinterpret_cast<const void*>(insert_row_kernel<F, NORM, ROPE>);
+  const int64_t warps = token_shape ? a.num_tokens : a.num_rows;
+  const int64_t ctas = (warps + kThreads / 32 - 1) / (kThreads / 32);
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(capped_grid(kern, kThreads, ctas));
+  lc.blockDim = dim3(kThreads);
+  lc.stream = cfg.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = cfg.pdl ? 1 : 0;
+  if (token_shape) return cudaLaunchKernelEx(&lc, insert_token_kernel<F, NORM, ROPE>, a);
+  return cudaLaunchKernelEx(&lc, insert_row_kernel<F, NORM, ROPE>, a);
 }
 
 template <int F>
 cudaError_t launch_fmt(const InsertArgs& a, bool norm, bool rope, const LaunchCfg& cfg) {
-  if (norm && rope) return launch_rows<F, true, true>(a, cfg);
-  if (norm) return launch_rows<F, true, false>(a, cfg);
-  if (rope) return launch_rows<F, false, true>(a, cfg);
-  return launch_rows<F, false, false>(a, cfg);
+  if (norm && rope) return launch_t<F, true, true>(a, cfg);
+  if (norm) return launch_t<F, true, false>(a, cfg);
+  if (rope) return launch_t<F, false, true>(a, cfg);
+  return launch_t<F, false, false>(a, cfg);
 }
 
 }  // namespace

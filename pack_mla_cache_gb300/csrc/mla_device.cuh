@@ -18,6 +18,7 @@ constexpr uint32_t kErrSlotOOB = 1u;
 constexpr uint32_t kErrBlockOOB = 2u;
 constexpr uint32_t kErrPosOOB = 4u;
 constexpr uint32_t kErrMisaligned = 8u;
+constexpr uint32_t kErrTimeout = 16u;
 
 // ---- programmatic dependent launch ---------------------------------------
 // Wait until every grid this one depends on has completed and its memory
@@ -115,14 +116,82 @@ struct ScaledDiv {
   }
 };
 
+// ---- packed fp32x2 arithmetic (sm_100+) --------------------------------------
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 unf2(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+// Division constants of one scale b: y = RN(1/b) (correctly rounded), and
+// whether the packed fast path below is valid for b (b and y normal).
+struct DivConst {
+  float b, y;
+  uint64_t y2, nb2;
+  bool fast;
+};
+__device__ __forceinline__ DivConst div_const(float scale) {
+  DivConst k;
+  k.b = scale;
+  k.y = __frcp_rn(scale);
+  const float ab = fabsf(scale), ay = fabsf(k.y);
+  k.fast = ab >= 1.1754944e-38f && ab <= 8.5e37f && ay >= 1.1754944e-38f && ay <= 8.5e37f;
+  k.y2 = f2(k.y, k.y);
+  k.nb2 = f2(-scale, -scale);
+  return k;
+}
+
+// Two correctly rounded quotients a/b at once.  FAST: the division theorem of
+// ScaledDiv on packed fp32x2 pairs (q = a*y, r = a - q*b, q' = q + r*y), then
+// per element the two special cases -- a NaN second step (the first quotient
+// overflowed, or a was NaN / inf) keeps the first quotient, and a zero keeps
+// the first quotient's sign.  !FAST: IEEE division (scales outside the range
+// where the theorem's assumptions hold).
+template <bool FAST>
+__device__ __forceinline__ float2 div2(float a0, float a1, const DivConst& k) {
+  if constexpr (!FAST) {
+    return make_float2(__fdiv_rn(a0, k.b), __fdiv_rn(a1, k.b));
+  } else {
+    const uint64_t a = f2(a0, a1);
+    const uint64_t q = mul2(a, k.y2);
+    const uint64_t r = fma2(q, k.nb2, a);
+    const float2 qq = unf2(q), c = unf2(fma2(r, k.y2, q));
+    const float o0 = (c.x != c.x) ? qq.x : c.x;
+    const float o1 = (c.y != c.y) ? qq.y : c.y;
+    return make_float2(
+        __uint_as_float((__float_as_uint(o0) & 0x7FFFFFFFu) | (__float_as_uint(qq.x) & 0x80000000u)),
+        __uint_as_float((__float_as_uint(o1) & 0x7FFFFFFFu) | (__float_as_uint(qq.y) & 0x80000000u)));
+  }
+}
+
+// Two bf16 in a 32-bit word -> two fp8 (low 16 bits), divided by the scale.
+template <int F, bool FAST>
+__device__ __forceinline__ uint32_t bf16x2_to_fp8x2(uint32_t w, const DivConst& k) {
+  const float2 q = div2<FAST>(bf16lo(w), bf16hi(w), k);
+  return pack_fp8x2<F>(q.x, q.y);
+}
+
 // 8 bf16 (one uint4) -> 8 fp8 (one uint2), each value divided by the scale.
-template <int F>
-__device__ __forceinline__ uint2 bf16x8_to_fp8x8(uint4 v, const ScaledDiv& d) {
+template <int F, bool FAST>
+__device__ __forceinline__ uint2 bf16x8_to_fp8x8(uint4 v, const DivConst& k) {
   uint2 o;
-  o.x = pack_fp8x2<F>(d(bf16lo(v.x)), d(bf16hi(v.x))) |
-        (pack_fp8x2<F>(d(bf16lo(v.y)), d(bf16hi(v.y))) << 16);
-  o.y = pack_fp8x2<F>(d(bf16lo(v.z)), d(bf16hi(v.z))) |
-        (pack_fp8x2<F>(d(bf16lo(v.w)), d(bf16hi(v.w))) << 16);
+  o.x = bf16x2_to_fp8x2<F, FAST>(v.x, k) | (bf16x2_to_fp8x2<F, FAST>(v.y, k) << 16);
+  o.y = bf16x2_to_fp8x2<F, FAST>(v.z, k) | (bf16x2_to_fp8x2<F, FAST>(v.w, k) << 16);
   return o;
 }
 
@@ -147,6 +216,71 @@ __device__ __forceinline__ float diff_of_products(float a, float b, float c, flo
   const float e = fmaf(-c, d, w);
   const float f = fmaf(a, b, -w);
   return __fadd_rn(f, e);
+}
+
+// ---- mbarrier + bulk asynchronous copies (sm_90+ PTX) ------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+// Make barrier initialisation visible to the async (bulk-copy) proxy.
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; "
+      "selp.u32 %0, 1, 0, p; }"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Wait for the phase of `bar` with the given parity to complete, giving up
+// after `limit_ns` (returns false then): no wait in this library can hang.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t spin = 1;; ++spin) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((spin & 255u) == 0 && global_ns() - t0 > limit_ns) return false;
+  }
+}
+// One bulk copy global -> this CTA's shared memory, completing on `bar`
+// (16-byte aligned addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ uint4 lds16(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint2 lds8(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
 }
 
 __device__ __forceinline__ float warp_sum(float v) {

@@ -30,6 +30,7 @@ struct InsertArgs {
   const float* cos_sin;
   int64_t max_position;
   uint32_t* err;
+  bool use_tma;  // allow the bulk-copy pipeline shape
 };
 
 struct GatherArgs {
@@ -59,6 +60,8 @@ struct PackArgs {
   uint8_t* key;
   uint8_t* vout;  // may be null
   const float* out_scale;  // may be null (1.0)
+  uint32_t* err;  // may be null
+  bool use_tma;   // allow the bulk-copy pipeline variant
 };
 
 struct LaunchCfg {
@@ -77,6 +80,6 @@ cudaError_t launch_rope_table(float* out, int64_t max_position, int32_t rot_dim,
 
 // Grid size for a grid-stride kernel: enough CTAs to cover `work_ctas`, capped
 // at the number that can be resident at once on the current device.
-int capped_grid(const void* kernel, int threads, int64_t work_ctas);
+int capped_grid(const void* kernel, int threads, int64_t work_ctas, int dyn_smem = 0);
 
 }  // namespace mla

@@ -19,6 +19,7 @@ from .build import LIB_PATH
 MLA_BF16, MLA_FP8_E4M3, MLA_FP8_E5M2 = 0, 1, 2
 MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_MISALIGNED, MLA_ERR_CUDA = range(5)
 MLA_ERRBIT_SLOT_OOB, MLA_ERRBIT_BLOCK_OOB, MLA_ERRBIT_POS_OOB, MLA_ERRBIT_MISALIGNED = 1, 2, 4, 8
+MLA_ERRBIT_TIMEOUT = 16
 
 _TORCH_DTYPE = {MLA_BF16: torch.bfloat16, MLA_FP8_E4M3: torch.float8_e4m3fn,
                 MLA_FP8_E5M2: torch.float8_e5m2}
@@ -45,6 +46,7 @@ SIGNATURES = {
     "mla_last_error": (ctypes.c_char_p, []),
     "mla_version": (ctypes.c_char_p, []),
     "mla_set_pdl": (ctypes.c_int, [ctypes.c_int]),
+    "mla_set_bulk_copy": (ctypes.c_int, [ctypes.c_int]),
     "mla_cache_insert_grouped": (ctypes.c_int, [
         _vp, _i64, _i64, _vp, _i64, _i64, _i32, _i32, _i32, _i32, _vp, _i64, _vp, _vp,
         ctypes.c_int, _i64, _i32, _i64, _i64, ctypes.POINTER(NormRope), _vp, _vp]),
@@ -53,7 +55,7 @@ SIGNATURES = {
         _i64, ctypes.c_int, _vp, _vp]),
     "mla_context_kv_pack": (ctypes.c_int, [
         _vp, _i64, _i64, _vp, _i64, _i64, _vp, _i64, ctypes.c_int, _i32, _i32, _i32, _i32, _i32,
-        _vp, _vp, ctypes.c_int, _vp, _vp]),
+        _vp, _vp, ctypes.c_int, _vp, _vp, _vp]),
     "mla_rope_cos_sin_cache": (ctypes.c_int, [_vp, _i64, _i32, ctypes.c_double, _vp]),
 }
 
@@ -120,6 +122,10 @@ def mla_set_pdl(enable: bool) -> bool:
     return bool(lib().mla_set_pdl(1 if enable else 0))
 
 
+def mla_set_bulk_copy(enable: bool) -> bool:
+    return bool(lib().mla_set_bulk_copy(1 if enable else 0))
+
+
 def mla_cache_insert_grouped(kv_c, k_pe, slot_mapping, kv_cache_ptrs, kv_scales, cache_dtype,
                              num_blocks, block_size, block_stride, entry_stride, *,
                              slot_layer_stride=None, gamma=None, eps=1e-6, positions=None,
@@ -161,7 +167,7 @@ def mla_context_gather(kv_cache, cache_dtype, num_blocks, block_size, block_stri
 
 
 def mla_context_kv_pack(k_nope, v, k_pe, key_out, v_out, out_dtype, *, kpe_dtype=None,
-                        out_scale=None, stream=None):
+                        out_scale=None, err_word=None, stream=None):
     """k_nope / v: [T, H, 128] bf16 views (strided); k_pe [T, 64] (bf16 or fp8,
     strided rows); key_out [T, H, 192] and v_out [T, H, 128] (or None)."""
     T, H, N = k_nope.shape
@@ -169,7 +175,7 @@ def mla_context_kv_pack(k_nope, v, k_pe, key_out, v_out, out_dtype, *, kpe_dtype
     _check(lib().mla_context_kv_pack(
         _ptr(k_nope), k_nope.stride(0), k_nope.stride(1), _ptr(v), v.stride(0), v.stride(1),
         _ptr(k_pe), k_pe.stride(0), kd, T, H, N, k_pe.shape[-1], v.shape[2], _ptr(key_out),
-        _ptr(v_out), dtype_code(out_dtype), _ptr(out_scale), _stream(stream)))
+        _ptr(v_out), dtype_code(out_dtype), _ptr(out_scale), _ptr(err_word), _stream(stream)))
 
 
 def mla_rope_cos_sin_cache(out, base=10000.0, *, stream=None):

@@ -21,3 +21,15 @@ def orc():
 
     oracle.lib()
     return oracle
+
+
+@pytest.fixture(params=[True, False], ids=["bulk", "plain"])
+def bulk(request):
+    """Run a GPU test with the bulk-copy pipeline variants allowed, then with
+    only the plain variants (both must give identical results)."""
+    from pack_mla_cache_gb300 import build, ops
+
+    build.build()
+    prev = ops.mla_set_bulk_copy(request.param)
+    yield request.param
+    ops.mla_set_bulk_copy(prev)

@@ -61,10 +61,13 @@ def test_version_and_dtype_strings(L):
         assert ops.mla_dtype_from_string(s) == -1
 
 
-def test_pdl_toggle(L):
+def test_pdl_and_bulk_copy_toggles(L):
     prev = ops.mla_set_pdl(False)
     assert ops.mla_set_pdl(True) is False
     ops.mla_set_pdl(prev)
+    prev = ops.mla_set_bulk_copy(False)
+    assert ops.mla_set_bulk_copy(True) is False
+    ops.mla_set_bulk_copy(prev)
 
 
 def insert(L, **kw):
@@ -122,7 +125,7 @@ def test_insert_norm_rope_checks(L):
 def test_zero_tokens_is_a_no_op_without_cuda(L):
     assert insert(L, T=0) == ops.MLA_OK
     assert L.mla_context_kv_pack(A, 4160, 256, A, 4160, 256, A, 576, 1, 0, 16, 128, 64, 128, A,
-                                 A, 1, None, None) == ops.MLA_OK
+                                 A, 1, None, None, None) == ops.MLA_OK
 
 
 def test_validated_call_without_gpu_reports_cuda_error(L):
@@ -163,11 +166,12 @@ def test_gather_argument_checks(L, kw, status):
 def pack(L, **kw):
     a = dict(kn=A, kts=4160, khs=256, v=A + 256, vts=4160, vhs=256, kpe=A + 1024, kpets=576,
              kdt=1, T=8192, H=16, N=128, R=64, V=128, key=A + (1 << 30), vout=A + (2 << 30), odt=1,
-             scale=None)
+             scale=None, err=None)
     a.update(kw)
     return L.mla_context_kv_pack(a["kn"], a["kts"], a["khs"], a["v"], a["vts"], a["vhs"],
                                  a["kpe"], a["kpets"], a["kdt"], a["T"], a["H"], a["N"], a["R"],
-                                 a["V"], a["key"], a["vout"], a["odt"], a["scale"], None)
+                                 a["V"], a["key"], a["vout"], a["odt"], a["scale"], a["err"],
+                                 None)
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -185,6 +189,7 @@ def pack(L, **kw):
     (dict(kdt=0, kpe=A + 8, odt=0), ops.MLA_ERR_MISALIGNED),
     (dict(key=A + 8), ops.MLA_ERR_MISALIGNED),
     (dict(odt=9), ops.MLA_ERR_INVALID_ARG),
+    (dict(err=A + 1), ops.MLA_ERR_MISALIGNED),
 ])
 def test_pack_argument_checks(L, kw, status):
     assert pack(L, **kw) == status

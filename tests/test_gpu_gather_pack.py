@@ -153,7 +153,7 @@ def workspace(orc, pw, T, start, out_dtype):
 
 
 @pytest.mark.parametrize("out_dtype,kpe_dtype", [(1, 1), (0, 0), (0, 1), (1, 0), (2, 0)])
-def test_pack_8192_token_chunk(orc, out_dtype, kpe_dtype):
+def test_pack_8192_token_chunk(orc, bulk, out_dtype, kpe_dtype):
     pw = W.pack_workload(8192, 8192, num_blocks=256, seed=5)
     ws = workspace(orc, pw, 8192, 0, 1 if kpe_dtype else 0)
     kvb = pw.kv_b_proj[0]
@@ -164,9 +164,9 @@ def test_pack_8192_token_chunk(orc, out_dtype, kpe_dtype):
 
 
 @pytest.mark.parametrize("H", [1, 3, 4, 20])
-@pytest.mark.parametrize("T", [1, 77])
-def test_pack_runtime_heads_and_ragged_tokens(orc, H, T):
-    pw = W.pack_workload(T, T, num_blocks=4, seed=6, num_heads=H)
+@pytest.mark.parametrize("T", [1, 77, 1000])
+def test_pack_runtime_heads_and_ragged_tokens(orc, bulk, H, T):
+    pw = W.pack_workload(T, T, num_blocks=16, seed=6, num_heads=H)
     ws = workspace(orc, pw, T, 0, 1)
     kvb = pw.kv_b_proj[0]
     for out_dtype in (1, 0):
@@ -174,6 +174,30 @@ def test_pack_runtime_heads_and_ragged_tokens(orc, H, T):
         rk, rv = oracle_pack(orc, kvb, ws, H, out_dtype, 1)
         np.testing.assert_array_equal(gk, rk)
         np.testing.assert_array_equal(gv, rv)
+
+
+def test_pack_separate_k_nope_and_v_buffers(orc):
+    """k_nope and v from two different tensors with their own strides (not
+    the interleaved kv_b_proj halves): the plain variant handles them."""
+    T, H = 600, 16
+    pw = W.pack_workload(T, T, num_blocks=16, seed=13)
+    ws = workspace(orc, pw, T, 0, 1)
+    g = torch.Generator().manual_seed(3)
+    kn_h = torch.randn((T, H, 160), generator=g).to(torch.bfloat16)   # head stride 160
+    v_h = torch.randn((H, T, 128), generator=g).to(torch.bfloat16)    # head-major
+    k_nope = kn_h.cuda()[:, :, :128]
+    v = v_h.cuda().permute(1, 0, 2)
+    key = torch.zeros((T, H, 192), dtype=torch.uint8, device="cuda")
+    vo = torch.zeros((T, H, 128), dtype=torch.uint8, device="cuda")
+    sc = torch.tensor([0.01], dtype=torch.float32, device="cuda")
+    ops.mla_context_kv_pack(k_nope, v, D.dev(ws)[:, 512:], key, vo, 1, kpe_dtype=1, out_scale=sc)
+    torch.cuda.synchronize()
+    kn_np = kn_h.view(torch.int16).numpy().view(np.uint16)
+    v_np = v_h.view(torch.int16).numpy().view(np.uint16)
+    rk, rv = orc.context_kv_pack(kn_np.reshape(-1), H * 160, 160, v_np.reshape(-1), 128, T * 128,
+                                 ws[:, 512:], ENTRY, 1, T, H, 128, 64, 128, 1, 0.01)
+    np.testing.assert_array_equal(D.host_u8(key), rk)
+    np.testing.assert_array_equal(D.host_u8(vo), rv)
 
 
 def test_pack_without_v(orc):
@@ -254,7 +278,7 @@ def test_sixteen_chunk_pdl_chain(orc):
         np.testing.assert_array_equal(vs_h[c][rows], rv)
 
 
-def test_one_launch_of_131072_tokens_sampled(orc):
+def test_one_launch_of_131072_tokens_sampled(orc, bulk):
     """One 131072-token pack launch (the grid is capped at the resident CTAs,
     so every warp loops over many tokens): 4096 sampled tokens equal the
     oracle and the output is written exactly once (guard bands intact)."""

@@ -114,16 +114,42 @@ def test_ragged_non_power_of_two_blocks_and_large_rows(orc):
     assert_exact(gpu, ref)
 
 
-def test_dspark_projection_layout_input(orc):
+@pytest.mark.parametrize("T", [257, 1000])
+def test_dspark_projection_layout_input(orc, T):
     """kv_c / k_pe read straight from a [T, L, 576] projection output (no
-    permute().contiguous()), as strided views."""
-    wl = W.insert_workload(5, 257, 1, num_blocks=8, block_size=64, seed=12)
+    permute().contiguous()), as strided views: the row-per-warp shape below
+    4096 rows, the token-loop shape above."""
+    wl = W.insert_workload(5, T, 1, num_blocks=16, block_size=64, seed=12, norm=True, rope=True)
     T, L = wl.num_tokens, wl.num_layers
     proj = np.concatenate([wl.kv_c, wl.k_pe], axis=2).transpose(1, 0, 2).copy()  # [T, L, 576]
     pt = D.dev_bf16(proj)
     kv_c = pt[:, :, :512].permute(1, 0, 2)
     k_pe = pt[:, :, 512:].permute(1, 0, 2)
-    gpu, guards, _ = D.gpu_insert(wl, kv_c=kv_c, k_pe=k_pe)
+    gpu, guards, _ = D.gpu_insert(wl, kv_c=kv_c, k_pe=k_pe, cos_sin=D.gpu_rope_table())
+    ref, _ = oracle_insert(orc, wl, orc.rope_cos_sin_cache(W.MAX_POSITION, 64, W.ROPE_BASE))
+    assert guards
+    assert_within_tolerance(gpu, ref, 1)
+
+
+@pytest.mark.parametrize("dtype", [0, 1, 2])
+def test_ragged_tail_and_padding(orc, bulk, dtype):
+    """4099 tokens x 3 layers with a shared mapping (a partial last run of
+    tokens in the bulk-copy shape) and some -1 padding slots."""
+    wl = W.insert_workload(3, 4099, dtype, num_blocks=80, block_size=64, norm=True, rope=True,
+                           seed=14)
+    wl.slot_mapping[:, ::97] = -1
+    gpu, guards, _ = D.gpu_insert(wl, cos_sin=D.gpu_rope_table(), fill=0x3C)
+    ref, _ = oracle_insert(orc, wl, orc.rope_cos_sin_cache(W.MAX_POSITION, 64, W.ROPE_BASE),
+                           fill=0x3C3C if dtype == 0 else 0x3C)
+    assert guards
+    assert_within_tolerance(gpu, ref, dtype)
+
+
+def test_raw_fp8_insert_large_exact(orc, bulk):
+    """No norm / RoPE, 8192 tokens x 5 layers: the raw fp8 conversion through
+    every launch shape is bit-exact."""
+    wl = W.insert_workload(5, 8192, 1, num_blocks=256, block_size=64, seed=15)
+    gpu, guards, _ = D.gpu_insert(wl)
     ref, _ = oracle_insert(orc, wl)
     assert guards
     assert_exact(gpu, ref)
@@ -180,7 +206,7 @@ def test_host_pointer_for_scales_is_rejected():
 # ------------------------------------------------------------ norm + rope inserts
 @pytest.mark.parametrize("dtype", [1, 2])
 @pytest.mark.parametrize("shared", [True, False])
-def test_norm_rope_4096_tokens(orc, dtype, shared):
+def test_norm_rope_4096_tokens(orc, bulk, dtype, shared):
     """RMSNorm (eps 1e-6, gamma ~ N(1, 0.1)) + neox RoPE (positions in
     [0, 32768)), 4096 tokens x 5 layers into 512-block caches; each side uses
     its own cos/sin table."""
@@ -192,7 +218,7 @@ def test_norm_rope_4096_tokens(orc, dtype, shared):
     assert_within_tolerance(gpu, ref, dtype)
 
 
-def test_norm_rope_bf16_cache_within_one_ulp(orc):
+def test_norm_rope_bf16_cache_within_one_ulp(orc, bulk):
     """A bf16 cache exposes the pre-quantisation values: within 1 bf16 ulp."""
     wl = W.insert_workload(5, 4096, 0, num_blocks=512, block_size=64, norm=True, rope=True,
                            seed=30)
@@ -231,7 +257,7 @@ def test_rope_table_matches_oracle(orc):
 
 
 # ----------------------------------------------------- full size, as benchmarked
-def test_large_insert_65536_tokens_sampled(orc):
+def test_large_insert_65536_tokens_sampled(orc, bulk):
     """65536 tokens x 5 layers, e4m3, RMSNorm + RoPE, caches of 2048 blocks x
     64, one shared mapping -- the benchmarked launch.  The oracle recomputes
     2048 sampled tokens; every row no slot names must stay untouched."""
