@@ -502,10 +502,11 @@ def run_e2e(w, stream, steps):
     return {"ms": ms, "h2d": h2d, "d2h": d2h}
 
 
-def run_profile_case(name: str, launches: int) -> int:
+def run_profile_case(name: str, launches: int, tokens: int | None = None) -> int:
     """A few launches of ONE kernel on a mid-size case (inputs larger than L2,
     a few hundred MB on the device), for ncu captures:
       insert  32768 tokens x 5 layers, e4m3, RMSNorm+RoPE, 2048-block caches
+      insert_raw the same without RMSNorm / RoPE
       gather  262144 context rows from a 4096-block fp8 cache, raw
       pack    32768 tokens, 16 heads, fp8 e4m3 out, fp8 k_pe
       pack_plain the same with the bulk-copy pipeline variant disabled
@@ -518,8 +519,9 @@ def run_profile_case(name: str, launches: int) -> int:
     dev = torch.device("cuda")
     g = torch.Generator(device="cuda")
     g.manual_seed(0)
-    if name == "insert":
-        T = 32768
+    if name in ("insert", "insert_raw"):
+        T = tokens or 32768
+        raw = name == "insert_raw"
         kv_c = torch.randn((L_LAYERS, T, 512), generator=g, device=dev).to(torch.bfloat16)
         k_pe = torch.randn((L_LAYERS, T, 64), generator=g, device=dev).to(torch.bfloat16)
         slots = torch.randperm(NB_INSERT * BS, generator=g, device=dev)[:T]
@@ -532,11 +534,13 @@ def run_profile_case(name: str, launches: int) -> int:
         table = torch.empty((W.MAX_POSITION, 64), dtype=torch.float32, device=dev)
         ops.mla_rope_cos_sin_cache(table, W.ROPE_BASE)
         fn = lambda: ops.mla_cache_insert_grouped(kv_c, k_pe, slots, ptrs, scales, 1, NB_INSERT,
-                                                  BS, BS * ENTRY, ENTRY, gamma=gamma, eps=1e-6,
-                                                  positions=pos, cos_sin_cache=table)
+                                                  BS, BS * ENTRY, ENTRY,
+                                                  gamma=None if raw else gamma, eps=1e-6,
+                                                  positions=None if raw else pos,
+                                                  cos_sin_cache=None if raw else table)
         nbytes = insert_bytes(T, L_LAYERS)
     elif name == "gather":
-        T, nb = 262144, 4096
+        T, nb = tokens or 262144, 4096
         cache = torch.randint(0, 126, (nb * BS * ENTRY,), generator=g, device=dev, dtype=torch.int32).to(torch.uint8)
         table = torch.randperm(nb, generator=g, device=dev).to(torch.int32)[None, :].contiguous()
         cu = torch.tensor([0, T], dtype=torch.int32, device=dev)
@@ -546,7 +550,7 @@ def run_profile_case(name: str, launches: int) -> int:
                                             cu, st, out, 1)
         nbytes = T * B_GATHER_TOK + (T // BS) * 4
     elif name in ("pack", "pack_bf16", "pack_plain"):
-        T = 32768
+        T = tokens or 32768
         bf = name == "pack_bf16"
         ops.mla_set_bulk_copy(name != "pack_plain")
         kvb = torch.randn((T, ROW_STRIDE), generator=g, device=dev).to(torch.bfloat16)
@@ -575,7 +579,7 @@ def run_profile_case(name: str, launches: int) -> int:
     e.record()
     e.synchronize()
     us = s.elapsed_time(e) / launches * 1e3
-    print(json.dumps({"profile_case": name, "launches": launches, "us_per_launch": us,
+    print(json.dumps({"profile_case": name, "tokens": T, "launches": launches, "us_per_launch": us,
                       "bytes_per_launch": nbytes, "gbs": nbytes / us / 1e3}), flush=True)
     return 0
 
@@ -589,9 +593,10 @@ def main():
     ap.add_argument("--profile-case", default=None,
                     help="run a few launches of one kernel (insert, gather, pack, pack_plain, pack_bf16)")
     ap.add_argument("--launches", type=int, default=3)
+    ap.add_argument("--tokens", type=int, default=None, help="tokens of the profile case")
     args = ap.parse_args()
     if args.profile_case:
-        return run_profile_case(args.profile_case, args.launches)
+        return run_profile_case(args.profile_case, args.launches, args.tokens)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

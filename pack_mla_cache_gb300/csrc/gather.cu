@@ -8,9 +8,10 @@
 // kv_b_proj input dtype, fused here into the gather).
 //
 // Design: one warp per output row, 4 rows per warp per iteration with all
-// their 16-byte loads issued before any store; the per-sequence prefix sums
-// and chunk starts are staged once per CTA in shared memory (binary search
-// there), so a row costs one block-table load and its cache row.
+// their 16-byte loads issued before any store.  With fewer than 32 sequences
+// each warp keeps the prefix sums and chunk starts in its lanes and finds a
+// row's sequence with one ballot, so a row costs one block-table load and its
+// cache row; more sequences use a binary search in global memory.
 #include "mla_device.cuh"
 #include "mla_internal.h"
 
@@ -20,7 +21,6 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kRows = 4;
 constexpr int kMaxChunks = 3;        // up to 96 x 16 B = 1536-byte rows
-constexpr int kSmemSeqs = 1024;      // sequences staged in shared memory
 
 // Largest s with cu[s] <= i, searched in cu[0..n]; -1 if none.
 __device__ __forceinline__ int find_seq(const int32_t* cu, int n, int64_t i) {
@@ -35,21 +35,19 @@ __device__ __forceinline__ int find_seq(const int32_t* cu, int n, int64_t i) {
 
 template <int MODE>  // 0: raw copy; kE4M3 / kE5M2: widen that fp8 format to bf16
 __global__ void __launch_bounds__(kThreads) gather_kernel(const GatherArgs a) {
-  __shared__ int32_t s_cu[kSmemSeqs + 1];
-  __shared__ int32_t s_st[kSmemSeqs];
+  pdl_trigger();
   pdl_wait();
-  const bool staged = a.num_seqs <= kSmemSeqs;
-  if (staged) {
-    for (int i = threadIdx.x; i <= a.num_seqs; i += kThreads) s_cu[i] = a.cu[i];
-    for (int i = threadIdx.x; i < a.num_seqs; i += kThreads) s_st[i] = a.starts[i];
-    __syncthreads();
-  }
-  const int32_t* cu = staged ? s_cu : a.cu;
-  const int32_t* st = staged ? s_st : a.starts;
-
   const int lane = threadIdx.x & 31;
   const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
+  // Up to 31 sequences: lane l holds cu[l] and starts[l], and a row's sequence
+  // is found with one ballot (no shared-memory staging, no block barrier).
+  const bool few = a.num_seqs < 32;
+  int32_t my_cu = 0, my_st = 0;
+  if (few) {
+    if (lane <= a.num_seqs) my_cu = a.cu[lane];
+    if (lane < a.num_seqs) my_st = a.starts[lane];
+  }
   uint32_t errbits = 0;
 
   for (int64_t r0 = warp * kRows; r0 < a.num_tokens; r0 += nwarps * kRows) {
@@ -59,9 +57,22 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const GatherArgs a) {
       src[k] = nullptr;
       const int64_t i = r0 + k;
       if (i >= a.num_tokens) continue;
-      const int s = find_seq(cu, a.num_seqs, i);
-      if (s < 0 || s >= a.num_seqs || i >= (int64_t)cu[s + 1]) continue;  // owned by no sequence
-      const int64_t p = (int64_t)st[s] + (i - cu[s]);
+      int s;
+      int64_t c0, c1, st;
+      if (few) {
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, lane <= a.num_seqs && (int64_t)my_cu <= i);
+        s = __popc(m) - 1;  // the largest s with cu[s] <= i (cu non-decreasing)
+        c0 = __shfl_sync(0xFFFFFFFFu, my_cu, s < 0 ? 0 : s);
+        c1 = __shfl_sync(0xFFFFFFFFu, my_cu, s + 1 > 31 ? 31 : s + 1);
+        st = __shfl_sync(0xFFFFFFFFu, my_st, s < 0 ? 0 : s);
+      } else {
+        s = find_seq(a.cu, a.num_seqs, i);
+        c0 = s >= 0 ? a.cu[s] : 0;
+        c1 = (s >= 0 && s < a.num_seqs) ? a.cu[s + 1] : 0;
+        st = (s >= 0 && s < a.num_seqs) ? a.starts[s] : 0;
+      }
+      if (s < 0 || s >= a.num_seqs || i >= c1) continue;  // owned by no sequence
+      const int64_t p = st + (i - c0);
       const int64_t kb = p >= 0 ? (a.bs_shift >= 0 ? (p >> a.bs_shift) : p / a.block_size) : -1;
       if (kb < 0 || kb >= a.bt_stride) {
         errbits |= kErrBlockOOB;
@@ -105,7 +116,6 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const GatherArgs a) {
   }
   errbits = __reduce_or_sync(0xFFFFFFFFu, errbits);
   if (errbits && lane == 0 && a.err) atomicOr(a.err, errbits);
-  pdl_trigger();
 }
 
 template <int MODE>

@@ -104,10 +104,8 @@ __device__ __forceinline__ void write_row(uint8_t* dst, int lane, const uint4& y
   write_row_dc<F>(dst, lane, y0, y1, p, k);
 }
 
-// RMSNorm of this lane's 16 kv_c elements (words x0 / x1) with the row's
-// gamma words g0 / g1: returns the bf16-rounded results in y0 / y1.
-__device__ __forceinline__ void rms_norm16(const uint4& x0, const uint4& x1, const uint4& g0,
-                                           const uint4& g1, float eps, uint4& y0, uint4& y1) {
+// This lane's part of a row's sum of squares (16 kv_c elements in x0 / x1).
+__device__ __forceinline__ float sum_sq16(const uint4& x0, const uint4& x1) {
   const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
   uint64_t acc = f2(0.f, 0.f);
 #pragma unroll
@@ -116,11 +114,15 @@ __device__ __forceinline__ void rms_norm16(const uint4& x0, const uint4& x1, con
     acc = fma2(v, v, acc);
   }
   const float2 acc2 = unf2(acc);
-  const float ss = warp_sum(acc2.x + acc2.y);
-  // mean over 512 (exact power-of-two scaling) + eps, one rounding
-  const float rstd = __frsqrt_rn(fmaf(ss, 1.0f / kR, eps));
-  const uint64_t rstd2 = f2(rstd, rstd);
+  return acc2.x + acc2.y;
+}
+
+// y = x * rstd * gamma for this lane's 16 elements, rounded to bf16.
+__device__ __forceinline__ void scale16(const uint4& x0, const uint4& x1, const uint4& g0,
+                                        const uint4& g1, float rstd, uint4& y0, uint4& y1) {
+  const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
   const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+  const uint64_t rstd2 = f2(rstd, rstd);
   uint32_t o[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -130,6 +132,15 @@ __device__ __forceinline__ void rms_norm16(const uint4& x0, const uint4& x1, con
   }
   y0 = make_uint4(o[0], o[1], o[2], o[3]);
   y1 = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// RMSNorm of this lane's 16 kv_c elements (words x0 / x1) with the row's
+// gamma words g0 / g1: returns the bf16-rounded results in y0 / y1.
+__device__ __forceinline__ void rms_norm16(const uint4& x0, const uint4& x1, const uint4& g0,
+                                           const uint4& g1, float eps, uint4& y0, uint4& y1) {
+  const float ss = warp_sum(sum_sq16(x0, x1));
+  // mean over 512 (exact power-of-two scaling) + eps, one rounding
+  scale16(x0, x1, g0, g1, __frsqrt_rn(fmaf(ss, 1.0f / kR, eps)), y0, y1);
 }
 
 // The neox rotation of this lane's k_pe pair (element lane in the low half,
@@ -188,6 +199,7 @@ __device__ __forceinline__ bool load_rope(const InsertArgs& a, int64_t t, int la
 // Shape 1: one warp per (token, layer) row, rows in token-major order.
 template <int F, bool NORM, bool ROPE>
 __global__ void __launch_bounds__(kThreads) insert_row_kernel(const InsertArgs a) {
+  pdl_trigger();
   pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
@@ -203,12 +215,12 @@ __global__ void __launch_bounds__(kThreads) insert_row_kernel(const InsertArgs a
     errbits |= store_row<F, NORM, ROPE>(a, l, lane, in, pos_ok, cs);
   }
   if (errbits && lane == 0 && a.err) atomicOr(a.err, errbits);
-  pdl_trigger();
 }
 
 // Shape 2: one warp per token, its layers kLG rows at a time.
 template <int F, bool NORM, bool ROPE>
 __global__ void __launch_bounds__(kThreads) insert_token_kernel(const InsertArgs a) {
+  pdl_trigger();
   pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
@@ -230,7 +242,6 @@ __global__ void __launch_bounds__(kThreads) insert_token_kernel(const InsertArgs
     }
   }
   if (errbits && lane == 0 && a.err) atomicOr(a.err, errbits);
-  pdl_trigger();
 }
 
 // Shape 3 (bulk-copy pipeline): for dense per-layer rows (kv_c token stride
@@ -244,6 +255,7 @@ __global__ void __launch_bounds__(kThreads) insert_token_kernel(const InsertArgs
 // per item).  Each consumer owns the stages s == warp (mod kIConsumers) and
 // takes their fills in order, so no parity wait can alias an older phase.
 constexpr int kRun = 4;
+constexpr int kILP = 2;  // rows of an item processed in lockstep
 constexpr int kIConsumers = 16;
 constexpr int kIStages = kIConsumers * 2;
 static_assert(kIStages == 32, "producer lane s owns stage s");
@@ -255,9 +267,14 @@ constexpr int kIStageBytes = kOffPos + kRun * 8;   // 4672
 constexpr int kMaxLayers = 128;
 constexpr int kOffBars = kIStages * kIStageBytes;
 constexpr int kOffLayers = kOffBars + 2 * kIStages * 8 + 16;
-constexpr int kISmem = kOffLayers + kMaxLayers * (8 + 4 + 4 + 4);
+constexpr int kISmem = kOffLayers + kMaxLayers * (8 + 4);
 constexpr uint64_t kIWaitLimitNs = 2000000000ull;  // 2 s: a wait that long means a fault
 
+// One item (a layer's run of up to kRun tokens) from its shared-memory stage.
+// The rows are processed in lockstep -- validity and loads of every row, then
+// every row's sum of squares, their warp reductions interleaved, then the
+// scaling, rotation and stores -- so a warp has kRun independent dependency
+// chains to issue from instead of one.
 template <int F, bool NORM, bool ROPE, bool FAST>
 __device__ __forceinline__ uint32_t insert_consume_item(
     const InsertArgs& a, uint32_t src, const uint8_t* stage, int64_t t0, int nt, int l,
@@ -279,25 +296,15 @@ __device__ __forceinline__ uint32_t insert_consume_item(
       }
     }
   }
-  float2 cs[kRun];
-#pragma unroll
-  for (int r = 0; r < kRun; ++r) {
-    cs[r] = make_float2(1.f, 0.f);
-    if (ROPE && slot[r] >= 0 && pos[r] >= 0 && pos[r] < a.max_position) {
-      const float* row = a.cos_sin + pos[r] * kP;
-      cs[r] = make_float2(__ldg(row + lane), __ldg(row + kP / 2 + lane));
-    }
-  }
-  uint4 g0 = make_uint4(0, 0, 0, 0), g1 = g0;
-  if constexpr (NORM) {
-    const uint8_t* g = a.gamma + (int64_t)l * a.gamma_ls;
-    g0 = ld_shared_ro16(g + lane * 16);
-    g1 = ld_shared_ro16(g + 512 + lane * 16);
-  }
+  // validity and destination of every row (uniform across the warp)
+  uint8_t* dst[kRun];
+  bool ok[kRun];
 #pragma unroll
   for (int r = 0; r < kRun; ++r) {
     const int64_t s = slot[r];
-    if (r >= nt || s < 0) continue;  // padding slot
+    ok[r] = false;
+    dst[r] = nullptr;
+    if (s < 0) continue;  // padding slot or past the tail
     if (s >= a.capacity) { err |= kErrSlotOOB; continue; }
     if (ROPE && (pos[r] < 0 || pos[r] >= a.max_position)) { err |= kErrPosOOB; continue; }
     if (cptr & 15) { err |= kErrMisaligned; continue; }
@@ -309,22 +316,60 @@ __device__ __forceinline__ uint32_t insert_consume_item(
       blk = s / a.block_size;
       off = s - blk * a.block_size;
     }
-    uint8_t* dst = reinterpret_cast<uint8_t*>(cptr) + blk * a.block_stride + off * a.entry_stride;
-    const uint32_t row = src + r * 2 * kR;
-    const uint4 x0 = lds16(row + lane * 16), x1 = lds16(row + 512 + lane * 16);
-    uint32_t pe;
-    {
-      const uint32_t pr = src + kOffPe + r * 2 * kP + lane * 2;
+    ok[r] = true;
+    dst[r] = reinterpret_cast<uint8_t*>(cptr) + blk * a.block_stride + off * a.entry_stride;
+  }
+  float2 cs[kRun];
+#pragma unroll
+  for (int r = 0; r < kRun; ++r) {
+    cs[r] = make_float2(1.f, 0.f);
+    if (ROPE && ok[r]) {
+      const float* row = a.cos_sin + pos[r] * kP;
+      cs[r] = make_float2(__ldg(row + lane), __ldg(row + kP / 2 + lane));
+    }
+  }
+  uint4 g0 = make_uint4(0, 0, 0, 0), g1 = g0;
+  if constexpr (NORM) {
+    const uint8_t* g = a.gamma + (int64_t)l * a.gamma_ls;
+    g0 = ld_shared_ro16(g + lane * 16);
+    g1 = ld_shared_ro16(g + 512 + lane * 16);
+  }
+  // the rows, kILP at a time in lockstep
+#pragma unroll
+  for (int h = 0; h < kRun; h += kILP) {
+    uint4 x0[kILP], x1[kILP], y0[kILP], y1[kILP];
+    uint32_t pe[kILP];
+#pragma unroll
+    for (int i = 0; i < kILP; ++i) {
+      const uint32_t row = src + (h + i) * 2 * kR;
+      x0[i] = y0[i] = lds16(row + lane * 16);
+      x1[i] = y1[i] = lds16(row + 512 + lane * 16);
+      const uint32_t pr = src + kOffPe + (h + i) * 2 * kP + lane * 2;
       uint32_t lo, hi;
       asm volatile("ld.shared.u16 %0, [%1];" : "=r"(lo) : "r"(pr));
       asm volatile("ld.shared.u16 %0, [%1];" : "=r"(hi) : "r"(pr + kP));
-      pe = lo | (hi << 16);
+      pe[i] = lo | (hi << 16);
     }
-    uint4 y0 = x0, y1 = x1;
-    if constexpr (NORM) rms_norm16(x0, x1, g0, g1, a.eps, y0, y1);
-    uint32_t p = pe;
-    if constexpr (ROPE) p = rope_pair(pe, cs[r]);
-    write_row_k<F, FAST>(dst, lane, y0, y1, p, k);
+    if constexpr (NORM) {
+      float ss[kILP];
+#pragma unroll
+      for (int i = 0; i < kILP; ++i) ss[i] = sum_sq16(x0[i], x1[i]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int i = 0; i < kILP; ++i) ss[i] += __shfl_xor_sync(0xFFFFFFFFu, ss[i], o);
+#pragma unroll
+      for (int i = 0; i < kILP; ++i) {
+        // mean over 512 (exact power-of-two scaling) + eps, one rounding
+        const float rstd = __frsqrt_rn(fmaf(ss[i], 1.0f / kR, a.eps));
+        scale16(x0[i], x1[i], g0, g1, rstd, y0[i], y1[i]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kILP; ++i) {
+      const uint32_t p = ROPE ? rope_pair(pe[i], cs[h + i]) : pe[i];
+      if (ok[h + i]) write_row_k<F, FAST>(dst[h + i], lane, y0[i], y1[i], p, k);
+    }
   }
   return err;
 }
@@ -336,8 +381,6 @@ __global__ void __launch_bounds__(kIThreads, 1) insert_tma_kernel(const InsertAr
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kIStages);
   int64_t* s_cptr = reinterpret_cast<int64_t*>(smem + kOffLayers);
   float* s_scale = reinterpret_cast<float*>(s_cptr + kMaxLayers);
-  float* s_rcp = s_scale + kMaxLayers;
-  int* s_fast = reinterpret_cast<int*>(s_rcp + kMaxLayers);
   const uint32_t stage0 = smem_addr(smem);
   const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + kIStages);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -350,15 +393,13 @@ __global__ void __launch_bounds__(kIThreads, 1) insert_tma_kernel(const InsertAr
     *abort_flag = 0;
     mbar_fence_init();
   }
+  pdl_trigger();
   pdl_wait();
   for (int l = threadIdx.x; l < a.num_layers; l += kIThreads) {
     s_cptr[l] = a.cache_ptrs[l];
     float sc = 1.0f;
     if constexpr (F != kBF16) sc = a.scales[l];
-    const DivConst k = div_const(sc);
     s_scale[l] = sc;
-    s_rcp[l] = k.y;
-    s_fast[l] = k.fast ? 1 : 0;
   }
   __syncthreads();
 
@@ -417,12 +458,7 @@ __global__ void __launch_bounds__(kIThreads, 1) insert_tma_kernel(const InsertAr
       const int nt = (int)min((int64_t)kRun, (int64_t)a.num_tokens - t0);
       const uint32_t src = stage0 + (uint32_t)(s * kIStageBytes);
       const uint8_t* stage = smem + (size_t)s * kIStageBytes;
-      DivConst k;
-      k.b = s_scale[l];
-      k.y = s_rcp[l];
-      k.fast = s_fast[l] != 0;
-      k.y2 = f2(k.y, k.y);
-      k.nb2 = f2(-k.b, -k.b);
+      const DivConst k = div_const(s_scale[l]);
       const int64_t cptr = s_cptr[l];
       if (F == kBF16 || k.fast)
         errbits |= insert_consume_item<F, NORM, ROPE, true>(a, src, stage, t0, nt, l, lane, cptr, k);
@@ -440,7 +476,6 @@ __global__ void __launch_bounds__(kIThreads, 1) insert_tma_kernel(const InsertAr
     errbits |= kErrTimeout;
   }
   if (errbits && lane == 0 && a.err) atomicOr(a.err, errbits);
-  pdl_trigger();
 }
 
 // The bulk-copy shape needs dense per-layer token rows and 16-byte aligned

@@ -24,7 +24,11 @@ constexpr uint32_t kErrTimeout = 16u;
 // Wait until every grid this one depends on has completed and its memory
 // operations are visible (a no-op when launched without the PDL attribute).
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-// Allow the next grid on the stream to start launching.
+// Allow the next grid on the stream to start launching.  Every kernel of this
+// library calls it first: its grid never exceeds the resident CTAs, so all of
+// its CTAs are running before a dependent CTA can take an SM slot, and the
+// dependent's CTAs then sit resident in their own pdl_wait() until this grid
+// has completed -- the next launch's latency overlaps this kernel's work.
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
@@ -139,10 +143,16 @@ __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
 }
 
 // Division constants of one scale b: y = RN(1/b) (correctly rounded), and
-// whether the packed fast path below is valid for b (b and y normal).
+// whether the packed fast paths below are valid for b (b and y normal).
+// thr2 holds, in both 16-bit halves, 0x8000 - (T << 7), where T is the
+// smallest bf16 exponent field whose values could make a*y overflow (|a| >=
+// 2^(T-126) and |y| < 2^(e_y-126) give |a*y| < 2^128 only for e_a + e_y <= 380)
+// -- capped at 255, so inf and NaN always count.
 struct DivConst {
   float b, y;
-  uint64_t y2, nb2;
+  uint64_t y2, nb2;  // ( y,  y), (-b, -b): guarded path
+  uint64_t ny2, b2;  // (-y, -y), ( b,  b): fast path
+  uint32_t thr2;
   bool fast;
 };
 __device__ __forceinline__ DivConst div_const(float scale) {
@@ -153,15 +163,21 @@ __device__ __forceinline__ DivConst div_const(float scale) {
   k.fast = ab >= 1.1754944e-38f && ab <= 8.5e37f && ay >= 1.1754944e-38f && ay <= 8.5e37f;
   k.y2 = f2(k.y, k.y);
   k.nb2 = f2(-scale, -scale);
+  k.ny2 = f2(-k.y, -k.y);
+  k.b2 = f2(scale, scale);
+  const int e_y = (int)((__float_as_uint(k.y) >> 23) & 0xFFu);
+  const int t = min(381 - e_y, 255);
+  const uint32_t h = 0x8000u - ((uint32_t)max(t, 1) << 7);
+  k.thr2 = h | (h << 16);
   return k;
 }
 
-// Two correctly rounded quotients a/b at once.  FAST: the division theorem of
-// ScaledDiv on packed fp32x2 pairs (q = a*y, r = a - q*b, q' = q + r*y), then
-// per element the two special cases -- a NaN second step (the first quotient
-// overflowed, or a was NaN / inf) keeps the first quotient, and a zero keeps
-// the first quotient's sign.  !FAST: IEEE division (scales outside the range
-// where the theorem's assumptions hold).
+// Two correctly rounded quotients a/b at once.  GUARDED: the division theorem
+// of ScaledDiv on packed fp32x2 pairs (q = a*y, r = a - q*b, q' = q + r*y),
+// then per element the two special cases -- a NaN second step (the first
+// quotient overflowed, or a was NaN / inf) keeps the first quotient, and a zero
+// keeps the first quotient's sign.  !FAST: IEEE division (scales outside the
+// range where the theorem's assumptions hold).
 template <bool FAST>
 __device__ __forceinline__ float2 div2(float a0, float a1, const DivConst& k) {
   if constexpr (!FAST) {
@@ -179,19 +195,66 @@ __device__ __forceinline__ float2 div2(float a0, float a1, const DivConst& k) {
   }
 }
 
+// The same two quotients of the bf16 pair in w when neither value can make
+// the first quotient non-finite (see special_pairs): with the negated inputs
+// -a, q = (-a)(-y), r' = q*b - a (exact), q' = q - r'*y is the correctly rounded
+// a/b, and the sign of a zero input survives every step (-0 -> q = -0,
+// r' = +0, q' = -0), so no per-element fix-up is needed.
+__device__ __forceinline__ float2 div2_fast(uint32_t w, const DivConst& k) {
+  const uint32_t nw = w ^ 0x80008000u;
+  const uint64_t na = f2(bf16lo(nw), bf16hi(nw));
+  const uint64_t q = mul2(na, k.ny2);
+  const uint64_t r = fma2(q, k.b2, na);
+  return unf2(fma2(r, k.ny2, q));
+}
+
+__device__ __forceinline__ uint32_t umax16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+// Whether any bf16 whose magnitude bits are folded (by max.u16x2) into m has
+// an exponent field >= T: adding 0x8000 - (T << 7) to a half carries into its
+// top bit exactly then (no carry crosses halves: a half is at most 0x7F80).
+__device__ __forceinline__ bool special_pairs(uint32_t m, uint32_t thr2) {
+  return ((m + thr2) & 0x80008000u) != 0u;
+}
+
 // Two bf16 in a 32-bit word -> two fp8 (low 16 bits), divided by the scale.
 template <int F, bool FAST>
 __device__ __forceinline__ uint32_t bf16x2_to_fp8x2(uint32_t w, const DivConst& k) {
+  if constexpr (FAST) {
+    if (!special_pairs(w & 0x7FFF7FFFu, k.thr2)) {
+      const float2 q = div2_fast(w, k);
+      return pack_fp8x2<F>(q.x, q.y);
+    }
+  }
   const float2 q = div2<FAST>(bf16lo(w), bf16hi(w), k);
   return pack_fp8x2<F>(q.x, q.y);
 }
 
 // 8 bf16 (one uint4) -> 8 fp8 (one uint2), each value divided by the scale.
+// The special-value check is done once for the 8 values.
 template <int F, bool FAST>
 __device__ __forceinline__ uint2 bf16x8_to_fp8x8(uint4 v, const DivConst& k) {
   uint2 o;
-  o.x = bf16x2_to_fp8x2<F, FAST>(v.x, k) | (bf16x2_to_fp8x2<F, FAST>(v.y, k) << 16);
-  o.y = bf16x2_to_fp8x2<F, FAST>(v.z, k) | (bf16x2_to_fp8x2<F, FAST>(v.w, k) << 16);
+  if constexpr (FAST) {
+    const uint32_t m = umax16x2(umax16x2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                                umax16x2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+    if (!special_pairs(m, k.thr2)) {
+      const float2 q0 = div2_fast(v.x, k), q1 = div2_fast(v.y, k);
+      const float2 q2 = div2_fast(v.z, k), q3 = div2_fast(v.w, k);
+      o.x = pack_fp8x2<F>(q0.x, q0.y) | (pack_fp8x2<F>(q1.x, q1.y) << 16);
+      o.y = pack_fp8x2<F>(q2.x, q2.y) | (pack_fp8x2<F>(q3.x, q3.y) << 16);
+      return o;
+    }
+  }
+  const float2 q0 = div2<FAST>(bf16lo(v.x), bf16hi(v.x), k);
+  const float2 q1 = div2<FAST>(bf16lo(v.y), bf16hi(v.y), k);
+  const float2 q2 = div2<FAST>(bf16lo(v.z), bf16hi(v.z), k);
+  const float2 q3 = div2<FAST>(bf16lo(v.w), bf16hi(v.w), k);
+  o.x = pack_fp8x2<F>(q0.x, q0.y) | (pack_fp8x2<F>(q1.x, q1.y) << 16);
+  o.y = pack_fp8x2<F>(q2.x, q2.y) | (pack_fp8x2<F>(q3.x, q3.y) << 16);
   return o;
 }
 

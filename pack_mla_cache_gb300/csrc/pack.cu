@@ -125,6 +125,7 @@ __device__ __forceinline__ void pack_plain_items(const PackArgs& a, const DivCon
 
 template <int OF, int KF>
 __global__ void __launch_bounds__(kThreads) pack_kernel(const PackArgs a) {
+  pdl_trigger();
   pdl_wait();
   float scale = 1.0f;
   if constexpr (OF != kBF16) {
@@ -137,7 +138,6 @@ __global__ void __launch_bounds__(kThreads) pack_kernel(const PackArgs a) {
     if (k.fast) pack_plain_items<OF, KF, true>(a, k);
     else pack_plain_items<OF, KF, false>(a, k);
   }
-  pdl_trigger();
 }
 
 // ---- bulk-copy pipeline variant ----------------------------------------------
@@ -219,6 +219,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) pack_tma_kernel(const PackArgs
     mbar_fence_init();
   }
   __syncthreads();
+  pdl_trigger();
   pdl_wait();
 
   const int groups = (H + kGroup - 1) / kGroup;
@@ -271,7 +272,6 @@ __global__ void __launch_bounds__(kTmaThreads, 1) pack_tma_kernel(const PackArgs
       (void)mbar_wait(full0 + 8 * lane, (uint32_t)((fills - 1) & 1), kWaitLimitNs / 8);
     if (threadIdx.x == 0 && a.err) atomicOr(a.err, kErrTimeout);
   }
-  pdl_trigger();
 }
 
 cudaLaunchConfig_t base_cfg(const LaunchCfg& cfg, cudaLaunchAttribute* attr) {

@@ -15,6 +15,7 @@ namespace {
 
 __global__ void rope_table_kernel(float* __restrict__ out, int64_t max_position, int32_t rot_dim,
                                   double base) {
+  pdl_trigger();
   pdl_wait();
   const int32_t half = rot_dim / 2;
   const int64_t n = max_position * half;
@@ -29,7 +30,6 @@ __global__ void rope_table_kernel(float* __restrict__ out, int64_t max_position,
     out[p * rot_dim + i] = (float)c;
     out[p * rot_dim + half + i] = (float)s;
   }
-  pdl_trigger();
 }
 
 }  // namespace

@@ -176,6 +176,21 @@ def test_pack_runtime_heads_and_ragged_tokens(orc, bulk, H, T):
         np.testing.assert_array_equal(gv, rv)
 
 
+@pytest.mark.parametrize("scale", [0.01, 3.0])
+def test_fp8_pack_exhaustive_over_bf16(orc, bulk, scale):
+    """kv_b_proj output holding all 2^16 bf16 patterns (16 tokens x 16 heads x
+    256): the fp8 key and V are bit-exact in every variant."""
+    T, H = 16, 16
+    pats = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16).reshape(T, H * 256)
+    kvb = np.zeros((T, 4160), np.uint16)
+    kvb[:, : H * 256] = pats
+    ws = np.random.default_rng(0).integers(0, 126, size=(T, ENTRY)).astype(np.uint8)
+    gk, gv = run_pack(kvb, ws, H, 1, 1, scale=scale)
+    rk, rv = oracle_pack(orc, kvb, ws, H, 1, 1, scale=scale)
+    np.testing.assert_array_equal(gk, rk)
+    np.testing.assert_array_equal(gv, rv)
+
+
 def test_pack_separate_k_nope_and_v_buffers(orc):
     """k_nope and v from two different tensors with their own strides (not
     the interleaved kv_b_proj halves): the plain variant handles them."""

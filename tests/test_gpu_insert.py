@@ -103,6 +103,22 @@ def test_fp8_conversion_exhaustive_over_bf16(orc, dtype, scale):
     assert_exact(gpu, ref)
 
 
+@pytest.mark.parametrize("dtype", [1, 2])
+def test_fp8_conversion_exhaustive_through_every_shape(orc, bulk, dtype):
+    """All 2^16 bf16 patterns tiled over 4096 tokens (the bulk-copy shape when
+    allowed, else the token-loop shape): bit-exact, including zeros of both
+    signs, subnormals, values whose quotient overflows, infinities and NaNs."""
+    wl = W.insert_workload(1, 4096, dtype, num_blocks=64, block_size=64, seed=16)
+    pats = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    wl.kv_c = np.tile(pats, 32).reshape(1, 4096, 512)
+    wl.k_pe = np.ascontiguousarray(np.tile(pats[::-1], 4).reshape(1, 4096, 64))
+    wl.k_scales = np.array([0.0123], np.float32)
+    gpu, guards, _ = D.gpu_insert(wl)
+    ref, _ = oracle_insert(orc, wl)
+    assert guards
+    assert_exact(gpu, ref)
+
+
 def test_ragged_non_power_of_two_blocks_and_large_rows(orc):
     """1000 tokens x 3 layers (rows not a multiple of any tile), block_size 48
     (division path), 32768+ rows so the multi-row-per-warp instance runs."""
