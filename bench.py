@@ -432,10 +432,11 @@ def run(args):
     cpu = None
     if world == 1:
         smp = OracleSample(0, 8192, 32768)
-        dt = smp.run()
-        cpu = {"value": smp.nbytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": "insert of 8192 tokens x 5 layers (RMSNorm+RoPE, e4m3) + gather and "
-                         "fp8 pack of 32768 context tokens (16 heads), single-threaded C oracle, "
+        reps = 4  # about 10 s of CPU work on the GPU machine's host
+        dt = sum(smp.run() for _ in range(reps))
+        cpu = {"value": reps * smp.nbytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"{reps} x (insert of 8192 tokens x 5 layers (RMSNorm+RoPE, e4m3) + gather and "
+                         "fp8 pack of 32768 context tokens (16 heads)), single-threaded C oracle, "
                          f"{dt:.1f} s"}
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
@@ -449,7 +450,7 @@ def run(args):
                    "peak_gbs": peak, "peak_kind": peak_kind,
                    "tokens_layers_per_s_insert": T_INSERT * L_LAYERS * world / (ms * 1e-3),
                    "context_tokens_per_s": T_CTX * world / (ms * 1e-3)},
-        "roofline": {"bound": "hbm", "kernel": "pack_kernel<e4m3,e4m3,16>", "achieved": ach,
+        "roofline": {"bound": "hbm", "kernel": "pack_kernel<e4m3,e4m3>", "achieved": ach,
                      "peak": peak, "unit": "GB/s", "frac": ach / peak,
                      "peak_source": f"{peak_kind} HBM copy bandwidth",
                      "traffic": profile_traffic("pack_fp8_h16")},
@@ -502,14 +503,15 @@ def run_e2e(w, stream, steps):
     return {"ms": ms, "h2d": h2d, "d2h": d2h}
 
 
-def run_profile_case(name: str, launches: int, tokens: int | None = None) -> int:
+def run_profile_case(name: str, launches: int, tokens: int | None = None,
+                     graph: bool = False) -> int:
     """A few launches of ONE kernel on a mid-size case (inputs larger than L2,
     a few hundred MB on the device), for ncu captures:
       insert  32768 tokens x 5 layers, e4m3, RMSNorm+RoPE, 2048-block caches
       insert_raw the same without RMSNorm / RoPE
+      insert_plain the insert with the bulk-copy pipeline shape disabled
       gather  262144 context rows from a 4096-block fp8 cache, raw
       pack    32768 tokens, 16 heads, fp8 e4m3 out, fp8 k_pe
-      pack_plain the same with the bulk-copy pipeline variant disabled
       pack_bf16  the same with bf16 output and a bf16 k_pe"""
     import torch
     from pack_mla_cache_gb300 import ops
@@ -519,9 +521,10 @@ def run_profile_case(name: str, launches: int, tokens: int | None = None) -> int
     dev = torch.device("cuda")
     g = torch.Generator(device="cuda")
     g.manual_seed(0)
-    if name in ("insert", "insert_raw"):
+    if name in ("insert", "insert_raw", "insert_plain"):
         T = tokens or 32768
         raw = name == "insert_raw"
+        ops.mla_set_bulk_copy(name != "insert_plain")
         kv_c = torch.randn((L_LAYERS, T, 512), generator=g, device=dev).to(torch.bfloat16)
         k_pe = torch.randn((L_LAYERS, T, 64), generator=g, device=dev).to(torch.bfloat16)
         slots = torch.randperm(NB_INSERT * BS, generator=g, device=dev)[:T]
@@ -549,10 +552,9 @@ def run_profile_case(name: str, launches: int, tokens: int | None = None) -> int
         fn = lambda: ops.mla_context_gather(cache, 1, nb, BS, BS * ENTRY, ENTRY, ENTRY, table,
                                             cu, st, out, 1)
         nbytes = T * B_GATHER_TOK + (T // BS) * 4
-    elif name in ("pack", "pack_bf16", "pack_plain"):
+    elif name in ("pack", "pack_bf16"):
         T = tokens or 32768
         bf = name == "pack_bf16"
-        ops.mla_set_bulk_copy(name != "pack_plain")
         kvb = torch.randn((T, ROW_STRIDE), generator=g, device=dev).to(torch.bfloat16)
         heads = kvb[:, :HEADS * 256].view(T, HEADS, 256)
         if bf:
@@ -573,13 +575,19 @@ def run_profile_case(name: str, launches: int, tokens: int | None = None) -> int
         fn()
     torch.cuda.synchronize()
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record()
-    for _ in range(launches):
-        fn()
-    e.record()
-    e.synchronize()
-    us = s.elapsed_time(e) / launches * 1e3
-    print(json.dumps({"profile_case": name, "tokens": T, "launches": launches, "us_per_launch": us,
+    if graph:  # the launches replayed from one CUDA graph: no host gaps between them
+        stream = torch.cuda.Stream()
+        g = graph_of(lambda: [fn() for _ in range(launches)], stream)
+        us = time_graph(g, stream, 3) / launches * 1e3
+    else:
+        s.record()
+        for _ in range(launches):
+            fn()
+        e.record()
+        e.synchronize()
+        us = s.elapsed_time(e) / launches * 1e3
+    print(json.dumps({"profile_case": name, "tokens": T, "graph": graph, "launches": launches,
+                      "us_per_launch": us,
                       "bytes_per_launch": nbytes, "gbs": nbytes / us / 1e3}), flush=True)
     return 0
 
@@ -591,12 +599,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["mine", "reference"], default="mine")
     ap.add_argument("--profile-case", default=None,
-                    help="run a few launches of one kernel (insert, gather, pack, pack_plain, pack_bf16)")
+                    help="run a few launches of one kernel (insert, insert_raw, insert_plain, gather, pack, pack_bf16)")
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--tokens", type=int, default=None, help="tokens of the profile case")
+    ap.add_argument("--graph", action="store_true", help="replay the profile case's launches from a CUDA graph")
     args = ap.parse_args()
     if args.profile_case:
-        return run_profile_case(args.profile_case, args.launches, args.tokens)
+        return run_profile_case(args.profile_case, args.launches, args.tokens, args.graph)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

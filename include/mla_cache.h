@@ -93,10 +93,10 @@ const char* mla_version(void);
  * every later launch from this process.  Returns the previous setting. */
 int mla_set_pdl(int enable);
 
-/* Enable (1, the default) or disable (0) the bulk-copy pipeline variants of
- * the kernels (shared-memory staging by cp.async.bulk) for every later launch
- * from this process; when disabled, or when a call's layout does not qualify,
- * the plain vectorised variant runs.  Both compute identical results.
+/* Enable (1, the default) or disable (0) the bulk-copy pipeline shape of the
+ * grouped insert (shared-memory staging by cp.async.bulk) for every later
+ * launch from this process; when disabled, or when a call's layout does not
+ * qualify, a plain vectorised shape runs.  Both compute identical results.
  * Returns the previous setting. */
 int mla_set_bulk_copy(int enable);
 
@@ -239,13 +239,8 @@ mla_status_t mla_context_gather(
  *   v_out               contiguous [T, H, v_dim] of out_dtype, or NULL = no V.
  *   out_scale           device fp32 scalar for fp8 output (NULL = 1.0); must be
  *                       NULL for bf16 output.
- *   err_word            NULL, or a device uint32 that receives MLA_ERRBIT_TIMEOUT
- *                       if a wait of the bulk-copy pipeline ever gave up (its
- *                       waits are bounded at 2 s, so a fault elsewhere cannot
- *                       hang the kernel); the outputs are then incomplete.
- * When k_nope and v are the two halves of one [T, H, 256] buffer (head stride
- * 256, v = k_nope + 128), v_out is set, H <= 16 and the k_pe rows are 16-byte
- * aligned, the bulk-copy pipeline variant runs (see mla_set_bulk_copy).
+ *   err_word            NULL, or a device uint32 for MLA_ERRBIT_* (reserved:
+ *                       the pack reads no indices, so no condition sets a bit).
  */
 mla_status_t mla_context_kv_pack(
     const void* k_nope, int64_t kn_token_stride, int64_t kn_head_stride, const void* v,

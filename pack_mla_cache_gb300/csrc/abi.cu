@@ -205,6 +205,8 @@ mla_status_t mla_cache_insert_grouped(
         return fail(MLA_ERR_MISALIGNED, "positions must be 8-byte aligned");
     }
   }
+  if ((int64_t)((num_tokens + 3) / 4) * num_layers >= (int64_t(1) << 32))
+    return fail(MLA_ERR_UNSUPPORTED, "num_tokens * num_layers is too large for one call");
   if (num_tokens == 0) return MLA_OK;  // empty inputs may have null data pointers
   if (!kv_c || !k_pe || !slot_mapping || !kv_cache_ptrs)
     return fail(MLA_ERR_INVALID_ARG, "kv_c, k_pe, slot_mapping and kv_cache_ptrs must be non-null");
@@ -372,7 +374,6 @@ mla_status_t mla_context_kv_pack(const void* k_nope, int64_t kn_token_stride,
   a.vout = static_cast<uint8_t*>(v_out);
   a.out_scale = out_scale;
   a.err = err_word;
-  a.use_tma = g_bulk.load() != 0;
   return launched(mla::launch_pack(a, (int)out_dtype, (int)kpe_dtype, cfg_for(stream)),
                   "mla_context_kv_pack");
 }

@@ -425,8 +425,8 @@ __global__ void __launch_bounds__(kIThreads, 1) insert_tma_kernel(const InsertAr
         }
         if (*abort_flag) break;
         const int64_t j = b + G * i;
-        const int64_t run = j / L;
-        const int l = (int)(j - run * L);
+        const int64_t run = (int64_t)((uint32_t)j / (uint32_t)L);
+        const int l = (int)((uint32_t)j - (uint32_t)run * (uint32_t)L);
         const int64_t t0 = run * kRun;
         const int nt = (int)min((int64_t)kRun, (int64_t)a.num_tokens - t0);
         const uint32_t dst = stage0 + (uint32_t)(s * kIStageBytes);
@@ -452,8 +452,8 @@ __global__ void __launch_bounds__(kIThreads, 1) insert_tma_kernel(const InsertAr
         break;
       }
       const int64_t j = b + G * i;
-      const int64_t run = j / L;
-      const int l = (int)(j - run * L);
+      const int64_t run = (int64_t)((uint32_t)j / (uint32_t)L);
+      const int l = (int)((uint32_t)j - (uint32_t)run * (uint32_t)L);
       const int64_t t0 = run * kRun;
       const int nt = (int)min((int64_t)kRun, (int64_t)a.num_tokens - t0);
       const uint32_t src = stage0 + (uint32_t)(s * kIStageBytes);

@@ -60,8 +60,7 @@ struct PackArgs {
   uint8_t* key;
   uint8_t* vout;  // may be null
   const float* out_scale;  // may be null (1.0)
-  uint32_t* err;  // may be null
-  bool use_tma;   // allow the bulk-copy pipeline variant
+  uint32_t* err;  // may be null (no pack condition sets a bit today)
 };
 
 struct LaunchCfg {
