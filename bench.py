@@ -344,6 +344,27 @@ def run_reference(args):
     return 0
 
 
+# ------------------------------------------------------------- multi-rank
+def max_over_ranks(value: float, world: int) -> float:
+    """The largest of every rank's value (the slowest rank's time); the
+    identity on one rank.  Works with any process-group backend: the tensor
+    lives on the GPU for NCCL and on the CPU otherwise."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(bytes_per_rank_step: float, world: int, ms_max: float) -> float:
+    """Whole-job GB/s: every rank moves its own shard (no exchange), the job
+    takes as long as its slowest rank."""
+    return bytes_per_rank_step * world / (ms_max * 1e-3) / 1e9
+
+
 # ----------------------------------------------------------------- main arm
 def run(args):
     import torch
@@ -398,21 +419,15 @@ def run(args):
         ms_pack = time_graph(g_pack, stream, reps) / nch
     clocks = clk.summary()
 
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world)
     sbytes = step_bytes()
-    value = sbytes * world / (ms * 1e-3) / 1e9
+    value = job_throughput(sbytes, world, ms)
     errs = w.err.cpu().tolist()
     assert errs == [0, 0], f"kernels reported skipped rows: {errs}"
 
     # ---- end to end through the public API with host buffers
     e2e = run_e2e(w, stream, max(2, min(args.steps, 5)))
-    if world > 1:
-        t = torch.tensor([e2e["ms"]], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e["ms"] = float(t.item())
+    e2e["ms"] = max_over_ranks(e2e["ms"], world)
 
     if rank != 0:
         dist.destroy_process_group()
@@ -458,7 +473,7 @@ def run(args):
                     "gather": kline(b_gat_launch, ms_gather),
                     "pack": kline(b_pack_launch, ms_pack)},
         "cpu_baseline": cpu,
-        "e2e": {"value": sbytes * world / (e2e["ms"] * 1e-3) / 1e9, "unit": "GB/s",
+        "e2e": {"value": job_throughput(sbytes, world, e2e["ms"]), "unit": "GB/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
         "gpu_launches": Workload.launches_per_step * args.steps,
         "clocks": clocks,

@@ -73,6 +73,27 @@ __device__ __forceinline__ uint32_t pack_fp8x2(float lo, float hi) {
   return r;
 }
 
+// Four fp32 -> four fp8 in one 32-bit word (a0 in the lowest byte): the two
+// pairwise conversions write the two halves of the result register directly.
+template <int F>
+__device__ __forceinline__ uint32_t pack_fp8x4(float a0, float a1, float a2, float a3) {
+  uint32_t r;
+  if constexpr (F == kE4M3) {
+    asm("{ .reg .b16 l, h;\n"
+        "  cvt.rn.satfinite.e4m3x2.f32 l, %2, %1;\n"
+        "  cvt.rn.satfinite.e4m3x2.f32 h, %4, %3;\n"
+        "  mov.b32 %0, {l, h}; }"
+        : "=r"(r) : "f"(a0), "f"(a1), "f"(a2), "f"(a3));
+  } else {
+    asm("{ .reg .b16 l, h;\n"
+        "  cvt.rn.satfinite.e5m2x2.f32 l, %2, %1;\n"
+        "  cvt.rn.satfinite.e5m2x2.f32 h, %4, %3;\n"
+        "  mov.b32 %0, {l, h}; }"
+        : "=r"(r) : "f"(a0), "f"(a1), "f"(a2), "f"(a3));
+  }
+  return r;
+}
+
 // fp8x2 (low 16 bits of `w`) -> two exact bf16 values in one 32-bit word.
 // The hardware widening to f16x2 is exact for both fp8 formats, and every
 // finite f16 obtained this way is a bf16 value, so truncating the fp32 is
@@ -244,8 +265,8 @@ __device__ __forceinline__ uint2 bf16x8_to_fp8x8(uint4 v, const DivConst& k) {
     if (!special_pairs(m, k.thr2)) {
       const float2 q0 = div2_fast(v.x, k), q1 = div2_fast(v.y, k);
       const float2 q2 = div2_fast(v.z, k), q3 = div2_fast(v.w, k);
-      o.x = pack_fp8x2<F>(q0.x, q0.y) | (pack_fp8x2<F>(q1.x, q1.y) << 16);
-      o.y = pack_fp8x2<F>(q2.x, q2.y) | (pack_fp8x2<F>(q3.x, q3.y) << 16);
+      o.x = pack_fp8x4<F>(q0.x, q0.y, q1.x, q1.y);
+      o.y = pack_fp8x4<F>(q2.x, q2.y, q3.x, q3.y);
       return o;
     }
   }
@@ -253,8 +274,8 @@ __device__ __forceinline__ uint2 bf16x8_to_fp8x8(uint4 v, const DivConst& k) {
   const float2 q1 = div2<FAST>(bf16lo(v.y), bf16hi(v.y), k);
   const float2 q2 = div2<FAST>(bf16lo(v.z), bf16hi(v.z), k);
   const float2 q3 = div2<FAST>(bf16lo(v.w), bf16hi(v.w), k);
-  o.x = pack_fp8x2<F>(q0.x, q0.y) | (pack_fp8x2<F>(q1.x, q1.y) << 16);
-  o.y = pack_fp8x2<F>(q2.x, q2.y) | (pack_fp8x2<F>(q3.x, q3.y) << 16);
+  o.x = pack_fp8x4<F>(q0.x, q0.y, q1.x, q1.y);
+  o.y = pack_fp8x4<F>(q2.x, q2.y, q3.x, q3.y);
   return o;
 }
 
