@@ -94,6 +94,12 @@ def lib() -> ctypes.CDLL:
                 "orc_concat_key": (None, [vp, i64, i64, vp, i64, i32, i32, i32, i32, vp]),
                 "orc_context_kv_pack": (None, [vp, i64, i64, vp, i64, i64, vp, i64, i32, i32,
                                               i32, i32, i32, i32, vp, vp, i32, f32]),
+                "orc_bf16_from_fp8_scaled": (ctypes.c_uint16, [ctypes.c_uint8, ctypes.c_int, f32]),
+                "orc_context_gather_scaled": (u32, [vp, i32, i64, i32, i64, i64, i32, vp, i64, vp,
+                                                    vp, i32, i32, vp, i64, f32]),
+                "orc_context_kv_pack_paged": (u32, [vp, i64, i64, vp, i64, i64, vp, i32, i64, i32,
+                                                    i64, i64, i32, vp, i64, vp, vp, i32, i32, i32,
+                                                    i32, i32, i32, vp, vp, i32, f32]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -280,3 +286,40 @@ def context_kv_pack(k_nope_buf, kn_token_stride, kn_head_stride, v_buf, v_token_
                               kpe_dtype, T, H, nope, rope, v_dim, _p(key), _p(vout),
                               out_dtype, float(out_scale))
     return key, vout
+
+
+# -------------------------------------------------------------- next steps
+def bf16_from_fp8_scaled(c: int, fmt: int, scale: float) -> int:
+    return lib().orc_bf16_from_fp8_scaled(int(c), fmt, float(scale))
+
+
+def context_gather_scaled(cache, cache_dtype, num_blocks, block_size, block_stride, entry_stride,
+                          entry_dim, block_table, cu_chunk_lens, chunk_starts, out, dequant_scale):
+    """Gather with the scaled fp8 -> bf16 widening into ``out`` (uint16 2-D, in place)."""
+    _chk(block_table, np.int32), _chk(cu_chunk_lens, np.int32), _chk(chunk_starts, np.int32)
+    _chk(out, np.uint16)
+    return lib().orc_context_gather_scaled(
+        _p(cache), cache_dtype, num_blocks, block_size, block_stride, entry_stride, entry_dim,
+        _p(block_table), block_table.shape[1], _p(cu_chunk_lens), _p(chunk_starts),
+        chunk_starts.shape[0], out.shape[0], _p(out), out.shape[1], float(dequant_scale))
+
+
+def context_kv_pack_paged(k_nope_buf, kn_token_stride, kn_head_stride, v_buf, v_token_stride,
+                          v_head_stride, cache, cache_dtype, num_blocks, block_size, block_stride,
+                          entry_stride, rope_offset, block_table, cu_chunk_lens, chunk_starts, T,
+                          H, nope, rope, v_dim, out_dtype, out_scale=1.0, with_v=True,
+                          key_init=None, v_init=None):
+    """Pack with k_pe from the paged cache.  Returns (key, v, error bits); key
+    starts as ``key_init`` (rope slices of tokens without a row stay as given)."""
+    odt = np.uint16 if out_dtype == BF16 else np.uint8
+    key = (np.array(key_init, dtype=odt, copy=True) if key_init is not None
+           else np.zeros((T, H, nope + rope), odt))
+    vout = (np.array(v_init, dtype=odt, copy=True) if v_init is not None
+            else np.zeros((T, H, v_dim), odt)) if with_v else None
+    err = lib().orc_context_kv_pack_paged(
+        _p(k_nope_buf), kn_token_stride, kn_head_stride, _p(v_buf), v_token_stride, v_head_stride,
+        _p(cache), cache_dtype, num_blocks, block_size, block_stride, entry_stride, rope_offset,
+        _p(block_table), block_table.shape[1], _p(cu_chunk_lens), _p(chunk_starts),
+        chunk_starts.shape[0], T, H, nope, rope, v_dim, _p(key), _p(vout), out_dtype,
+        float(out_scale))
+    return key, vout, err

@@ -490,3 +490,136 @@ void orc_context_kv_pack(const uint16_t* k_nope, int64_t kn_token_stride,
     }
   }
 }
+
+/* ======================================================================== */
+/* Next steps of the chunked-context path (the gather fused into the pack,  */
+/* and a scaled dequantising gather).                                        */
+/* ======================================================================== */
+
+/*
+ * fp8 -> bf16 with a dequantisation scale: the exact value of the fp8 code
+ * times the scale as ONE fp32 multiplication (round to nearest even), then
+ * rounded once to bf16.  A NaN code gives the quiet NaN with the code's sign
+ * (as the unscaled widening does); any other NaN product (an infinity times a
+ * zero scale, a NaN scale) gives the positive quiet NaN 0x7FC0.
+ *
+ * The pages cast the gathered fp8 latent to the kv_b_proj input dtype with a
+ * plain, unscaled ".to()" ("PR #51772", Implementation items 2 and 5); a cache
+ * written with k_scale != 1 ("PR #55356", Source snippets: scaled_convert
+ * divides by the layer's k_scale) holds value / k_scale, and multiplying by the
+ * same k_scale is the dequantisation a bf16 kv_b_proj then needs.  This is
+ * that scaled form of the cast.
+ */
+uint16_t orc_bf16_from_fp8_scaled(uint8_t c, int fmt, float scale) {
+  double v = orc_fp8_to_f64(c, fmt);
+  if (isnan(v)) return (uint16_t)(((c & 0x80u) ? 0x8000u : 0u) | 0x7FC0u);
+  float p = (float)v * scale; /* (float)v is exact; the product rounds once */
+  if (isnan(p)) return 0x7FC0u;
+  return orc_bf16_from_f32(p);
+}
+
+/* The gather of orc_context_gather with every element widened by
+ * orc_bf16_from_fp8_scaled (fp8 cache, bf16 output). */
+uint32_t orc_context_gather_scaled(const void* cache, int32_t cache_dtype, int64_t num_blocks,
+                                   int32_t block_size, int64_t block_stride, int64_t entry_stride,
+                                   int32_t entry_dim, const int32_t* block_table,
+                                   int64_t block_table_stride, const int32_t* cu_chunk_lens,
+                                   const int32_t* chunk_starts, int32_t num_seqs,
+                                   int32_t num_tokens, uint16_t* out, int64_t out_row_stride,
+                                   float dequant_scale) {
+  uint32_t err = 0;
+  for (int32_t s = 0; s < num_seqs; ++s) {
+    for (int64_t i = cu_chunk_lens[s]; i < cu_chunk_lens[s + 1]; ++i) {
+      if (i < 0 || i >= num_tokens) continue;
+      int64_t p = (int64_t)chunk_starts[s] + (i - cu_chunk_lens[s]);
+      int64_t k = p >= 0 ? p / block_size : -1;
+      if (k < 0 || k >= block_table_stride) {
+        err |= ORC_ERR_BLOCK_OOB;
+        continue;
+      }
+      int32_t blk = block_table[(int64_t)s * block_table_stride + k];
+      if (blk < 0 || (int64_t)blk >= num_blocks) {
+        err |= ORC_ERR_BLOCK_OOB;
+        continue;
+      }
+      const uint8_t* row =
+          (const uint8_t*)cache + (int64_t)blk * block_stride + (p % block_size) * entry_stride;
+      for (int32_t e = 0; e < entry_dim; ++e)
+        out[i * out_row_stride + e] = orc_bf16_from_fp8_scaled(row[e], cache_dtype, dequant_scale);
+    }
+  }
+  return err;
+}
+
+/*
+ * The pack with k_pe read straight from the paged cache: token i of the chunk
+ * takes its k_pe from the cache row the gather would fetch for it (sequence
+ * by cu_chunk_lens, position chunk_starts[s] + i - cu_chunk_lens[s], block by
+ * the table), elements rope_offset .. rope_offset + rope_dim.  Everything else
+ * -- k_nope, V and every element rule -- is orc_context_kv_pack with that row
+ * as k_pe (of the cache's element type).  A token whose row cannot be found
+ * still gets its k_nope and V, and the rope slice of its key is left
+ * untouched: silently when no sequence owns it, with ORC_ERR_BLOCK_OOB when its
+ * block index or block id is out of range.  ("PR #51772" Implementation item
+ * 1 reads k_pe from the gathered workspace, still in the cache layout; reading
+ * the same bytes from the cache itself drops the workspace's k_pe columns.)
+ */
+uint32_t orc_context_kv_pack_paged(
+    const uint16_t* k_nope, int64_t kn_token_stride, int64_t kn_head_stride, const uint16_t* v,
+    int64_t v_token_stride, int64_t v_head_stride, const void* cache, int32_t cache_dtype,
+    int64_t num_blocks, int32_t block_size, int64_t block_stride, int64_t entry_stride,
+    int32_t rope_offset, const int32_t* block_table, int64_t block_table_stride,
+    const int32_t* cu_chunk_lens, const int32_t* chunk_starts, int32_t num_seqs,
+    int32_t num_tokens, int32_t num_heads, int32_t nope_dim, int32_t rope_dim, int32_t v_dim,
+    void* key_out, void* v_out, int32_t out_dtype, float out_scale) {
+  uint32_t err = 0;
+  const size_t ce = cache_dtype == ORC_BF16 ? 2u : 1u, oe = out_dtype == ORC_BF16 ? 2u : 1u;
+  const int64_t kd = (int64_t)nope_dim + rope_dim;
+  uint8_t* key_tmp = (uint8_t*)malloc((size_t)num_heads * kd * oe);
+  uint8_t* v_tmp = (uint8_t*)malloc((size_t)num_heads * v_dim * oe + 1);
+  if (!key_tmp || !v_tmp) {
+    free(key_tmp);
+    free(v_tmp);
+    return 0xFFFFFFFFu;
+  }
+  for (int32_t t = 0; t < num_tokens; ++t) {
+    /* the cache row of token t, if any */
+    const uint8_t* row = NULL;
+    for (int32_t s = 0; s < num_seqs && !row; ++s) {
+      if (t < cu_chunk_lens[s] || t >= cu_chunk_lens[s + 1]) continue;
+      int64_t p = (int64_t)chunk_starts[s] + (t - cu_chunk_lens[s]);
+      int64_t k = p >= 0 ? p / block_size : -1;
+      if (k < 0 || k >= block_table_stride) {
+        err |= ORC_ERR_BLOCK_OOB;
+        break;
+      }
+      int32_t blk = block_table[(int64_t)s * block_table_stride + k];
+      if (blk < 0 || (int64_t)blk >= num_blocks) {
+        err |= ORC_ERR_BLOCK_OOB;
+        break;
+      }
+      row = (const uint8_t*)cache +
+            ((int64_t)blk * block_stride + (p % block_size) * entry_stride + rope_offset) * ce;
+    }
+    /* pack this one token with its row as k_pe (a dummy row when there is none) */
+    uint16_t zero_pe[256] = {0};
+    orc_context_kv_pack(k_nope + (int64_t)t * kn_token_stride, kn_token_stride, kn_head_stride,
+                        v ? v + (int64_t)t * v_token_stride : NULL, v_token_stride, v_head_stride,
+                        row ? (const void*)row : (const void*)zero_pe, 0, cache_dtype, 1,
+                        num_heads, nope_dim, rope_dim, v_dim, key_tmp, v_out ? v_tmp : NULL,
+                        out_dtype, out_scale);
+    uint8_t* kdst = (uint8_t*)key_out + (int64_t)t * num_heads * kd * oe;
+    for (int32_t h = 0; h < num_heads; ++h) {
+      memcpy(kdst + (int64_t)h * kd * oe, key_tmp + (int64_t)h * kd * oe, (size_t)nope_dim * oe);
+      if (row)
+        memcpy(kdst + ((int64_t)h * kd + nope_dim) * oe, key_tmp + ((int64_t)h * kd + nope_dim) * oe,
+               (size_t)rope_dim * oe);
+    }
+    if (v_out)
+      memcpy((uint8_t*)v_out + (int64_t)t * num_heads * v_dim * oe, v_tmp,
+             (size_t)num_heads * v_dim * oe);
+  }
+  free(key_tmp);
+  free(v_tmp);
+  return err;
+}

@@ -103,6 +103,16 @@ uint32_t orc_context_gather(const void* cache, int32_t cache_dtype, int64_t num_
 void orc_cast_rows(const void* src, int32_t src_dtype, int64_t src_row_stride, int64_t rows,
                    int64_t cols, void* dst, int32_t dst_dtype, int64_t dst_row_stride);
 
+uint16_t orc_bf16_from_fp8_scaled(uint8_t c, int fmt, float scale);
+
+uint32_t orc_context_gather_scaled(const void* cache, int32_t cache_dtype, int64_t num_blocks,
+                                   int32_t block_size, int64_t block_stride, int64_t entry_stride,
+                                   int32_t entry_dim, const int32_t* block_table,
+                                   int64_t block_table_stride, const int32_t* cu_chunk_lens,
+                                   const int32_t* chunk_starts, int32_t num_seqs,
+                                   int32_t num_tokens, uint16_t* out, int64_t out_row_stride,
+                                   float dequant_scale);
+
 /* ---- chunked-context K/V pack ------------------------------------------- */
 void orc_concat_key(const uint16_t* k_nope, int64_t kn_token_stride, int64_t kn_head_stride,
                     const uint16_t* k_pe, int64_t kpe_token_stride, int32_t num_tokens,
@@ -114,6 +124,15 @@ void orc_context_kv_pack(const uint16_t* k_nope, int64_t kn_token_stride,
                          int32_t kpe_dtype, int32_t num_tokens, int32_t num_heads,
                          int32_t nope_dim, int32_t rope_dim, int32_t v_dim, void* key_out,
                          void* v_out, int32_t out_dtype, float out_scale);
+
+uint32_t orc_context_kv_pack_paged(
+    const uint16_t* k_nope, int64_t kn_token_stride, int64_t kn_head_stride, const uint16_t* v,
+    int64_t v_token_stride, int64_t v_head_stride, const void* cache, int32_t cache_dtype,
+    int64_t num_blocks, int32_t block_size, int64_t block_stride, int64_t entry_stride,
+    int32_t rope_offset, const int32_t* block_table, int64_t block_table_stride,
+    const int32_t* cu_chunk_lens, const int32_t* chunk_starts, int32_t num_seqs,
+    int32_t num_tokens, int32_t num_heads, int32_t nope_dim, int32_t rope_dim, int32_t v_dim,
+    void* key_out, void* v_out, int32_t out_dtype, float out_scale);
 
 #ifdef __cplusplus
 }
