@@ -526,8 +526,11 @@ def run_profile_case(name: str, launches: int, tokens: int | None = None,
       insert_raw the same without RMSNorm / RoPE
       insert_plain the insert with the bulk-copy pipeline shape disabled
       gather  262144 context rows from a 4096-block fp8 cache, raw
+      gather_scaled  the gather widened to bf16 times a k_scale
+      gather_kv_c    the raw gather of the 512 kv_c columns only
       pack    32768 tokens, 16 heads, fp8 e4m3 out, fp8 k_pe
-      pack_bf16  the same with bf16 output and a bf16 k_pe"""
+      pack_bf16  the same with bf16 output and a bf16 k_pe
+      pack_paged the fp8 pack reading k_pe from a 4096-block fp8 cache"""
     import torch
     from pack_mla_cache_gb300 import ops
     from pack_mla_cache_gb300 import workloads as W
@@ -557,16 +560,24 @@ def run_profile_case(name: str, launches: int, tokens: int | None = None,
                                                   positions=None if raw else pos,
                                                   cos_sin_cache=None if raw else table)
         nbytes = insert_bytes(T, L_LAYERS)
-    elif name == "gather":
+    elif name in ("gather", "gather_scaled", "gather_kv_c"):
         T, nb = tokens or 262144, 4096
         cache = torch.randint(0, 126, (nb * BS * ENTRY,), generator=g, device=dev, dtype=torch.int32).to(torch.uint8)
         table = torch.randperm(nb, generator=g, device=dev).to(torch.int32)[None, :].contiguous()
         cu = torch.tensor([0, T], dtype=torch.int32, device=dev)
         st = torch.tensor([0], dtype=torch.int32, device=dev)
-        out = torch.empty((T, ENTRY), dtype=torch.uint8, device=dev)
-        fn = lambda: ops.mla_context_gather(cache, 1, nb, BS, BS * ENTRY, ENTRY, ENTRY, table,
-                                            cu, st, out, 1)
-        nbytes = T * B_GATHER_TOK + (T // BS) * 4
+        if name == "gather_scaled":
+            out = torch.empty((T, ENTRY), dtype=torch.bfloat16, device=dev)
+            ks = torch.tensor([0.0137], dtype=torch.float32, device=dev)
+            fn = lambda: ops.mla_context_gather_scaled(cache, 1, nb, BS, BS * ENTRY, ENTRY, ENTRY,
+                                                       table, cu, st, out, ks)
+            nbytes = T * (ENTRY + 2 * ENTRY) + (T // BS) * 4
+        else:
+            cols = 512 if name == "gather_kv_c" else ENTRY
+            out = torch.empty((T, cols), dtype=torch.uint8, device=dev)
+            fn = lambda: ops.mla_context_gather(cache, 1, nb, BS, BS * ENTRY, ENTRY, cols, table,
+                                                cu, st, out, 1)
+            nbytes = T * 2 * cols + (T // BS) * 4
     elif name in ("pack", "pack_bf16"):
         T = tokens or 32768
         bf = name == "pack_bf16"
@@ -584,6 +595,22 @@ def run_profile_case(name: str, launches: int, tokens: int | None = None,
                                              key, vo, 0 if bf else 1, kpe_dtype=0 if bf else 1,
                                              out_scale=sc)
         nbytes = T * (HEADS * 512 + (128 if bf else 64) + HEADS * 320 * (2 if bf else 1))
+    elif name == "pack_paged":
+        T, nb = tokens or 32768, 4096
+        assert T <= nb * BS
+        kvb = torch.randn((T, ROW_STRIDE), generator=g, device=dev).to(torch.bfloat16)
+        heads = kvb[:, :HEADS * 256].view(T, HEADS, 256)
+        cache = torch.randint(0, 126, (nb * BS * ENTRY,), generator=g, device=dev, dtype=torch.int32).to(torch.uint8)
+        table = torch.randperm(nb, generator=g, device=dev).to(torch.int32)[None, :].contiguous()
+        cu = torch.tensor([0, T], dtype=torch.int32, device=dev)
+        st = torch.tensor([0], dtype=torch.int32, device=dev)
+        key = torch.empty((T, HEADS, 192), dtype=torch.uint8, device=dev)
+        vo = torch.empty((T, HEADS, 128), dtype=torch.uint8, device=dev)
+        sc = torch.tensor([OUT_SCALE], dtype=torch.float32, device=dev)
+        fn = lambda: ops.mla_context_kv_pack_paged(heads[:, :, :128], heads[:, :, 128:], cache, 1,
+                                                   nb, BS, BS * ENTRY, ENTRY, table, cu, st, key,
+                                                   vo, 1, out_scale=sc)
+        nbytes = T * (HEADS * 512 + 64 + HEADS * 320) + (T // BS) * 4
     else:
         raise SystemExit(f"unknown profile case {name}")
     for _ in range(2):

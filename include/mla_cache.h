@@ -213,6 +213,33 @@ mla_status_t mla_context_gather(
     mla_dtype_t out_dtype, uint32_t* err_word, mla_stream_t stream);
 
 /*
+ * The gather of mla_context_gather from an fp8 cache into bf16, dequantised:
+ *   out[i * out_row_stride + e] = bf16(fp32(value(code) * *k_scale))
+ * the exact value of the fp8 code times the scale as ONE fp32 multiplication
+ * (round to nearest even), then rounded to bf16 (round to nearest even).  A NaN
+ * code gives the quiet NaN with the code's sign (0x7FC0 | sign); any other NaN
+ * product (an infinity times zero, a NaN scale) gives 0x7FC0.
+ *
+ * For caches written with a k_scale other than 1: the insert stores
+ * value / k_scale ("PR #55356", Source snippets: scaled_convert with the
+ * layer's scale), and the chunked-context path casts the gathered latent to a
+ * bf16 kv_b_proj input ("PR #51772", Implementation items 2 and 5, where the
+ * cast is a plain .to()); this is that cast with the scale applied.
+ *
+ *   cache_dtype   MLA_FP8_E4M3 or MLA_FP8_E5M2 (else UNSUPPORTED).
+ *   out           bf16 rows, 16-byte aligned row starts.
+ *   k_scale       device fp32 scalar (required).
+ * Every other argument, the row rules and the error bits are those of
+ * mla_context_gather.
+ */
+mla_status_t mla_context_gather_scaled(
+    const void* kv_cache, mla_dtype_t cache_dtype, int64_t num_blocks, int32_t block_size,
+    int64_t block_stride, int64_t entry_stride, int32_t entry_dim, const int32_t* block_table,
+    int64_t block_table_stride, const int32_t* cu_chunk_lens, const int32_t* chunk_starts,
+    int32_t num_seqs, int32_t num_tokens, void* out, int64_t out_row_stride,
+    const float* k_scale, uint32_t* err_word, mla_stream_t stream);
+
+/*
  * Chunked-context K/V pack: one launch writes the contiguous full key
  * [k_nope | k_pe] and V from the strided kv_b_proj output and a k_pe that may
  * still be in the fp8 cache layout ("PR #51772", Source snippets:
@@ -239,8 +266,9 @@ mla_status_t mla_context_gather(
  *   v_out               contiguous [T, H, v_dim] of out_dtype, or NULL = no V.
  *   out_scale           device fp32 scalar for fp8 output (NULL = 1.0); must be
  *                       NULL for bf16 output.
- *   err_word            NULL, or a device uint32 for MLA_ERRBIT_* (reserved:
- *                       the pack reads no indices, so no condition sets a bit).
+ *   err_word            NULL, or a device uint32 for MLA_ERRBIT_* (this pack
+ *                       reads no indices, so no condition sets a bit; the paged
+ *                       pack below sets MLA_ERRBIT_BLOCK_OOB).
  */
 mla_status_t mla_context_kv_pack(
     const void* k_nope, int64_t kn_token_stride, int64_t kn_head_stride, const void* v,
@@ -248,6 +276,42 @@ mla_status_t mla_context_kv_pack(
     mla_dtype_t kpe_dtype, int32_t num_tokens, int32_t num_heads, int32_t nope_dim,
     int32_t rope_dim, int32_t v_dim, void* key_out, void* v_out, mla_dtype_t out_dtype,
     const float* out_scale, uint32_t* err_word, mla_stream_t stream);
+
+/*
+ * The pack of mla_context_kv_pack with k_pe read straight from the paged cache
+ * instead of a gathered workspace ("PR #51772", Implementation item 1: the
+ * kernel consumes a k_pe still in the fp8 cache layout; here that layout is
+ * the cache itself, so the gather before it only needs the kv_c columns).
+ *
+ * Token t's k_pe is the rope_dim elements at rope_offset of the cache row that
+ * mla_context_gather would copy into output row t (same sequence, position and
+ * block-table rules), of the cache's element type:
+ *   key_out[t, h, nope_dim + j] = kpe(row_t[rope_offset + j])
+ * with kpe as in mla_context_kv_pack for kpe_dtype = cache_dtype (raw bytes for
+ * an fp8 cache into an fp8 key of its format, the exact widening into a bf16
+ * key, the output conversion for a bf16 cache).  k_nope and V are packed as in
+ * mla_context_kv_pack for every token.  A token whose row is not found keeps
+ * the rope slice of its key untouched: silently when no sequence owns it, and
+ * with MLA_ERRBIT_BLOCK_OOB when its block index or block id is out of range.
+ *
+ *   kv_cache ... chunk_starts   the paged cache and the chunk's sequences, as
+ *                               in mla_context_gather; cache rows must start
+ *                               on 16-byte boundaries.
+ *   rope_offset                 element offset of k_pe in a cache row
+ *                               (kv_lora_rank, 512); rope_offset * element size
+ *                               a multiple of 16 (bf16) or 8 (fp8) bytes.
+ *   num_tokens                  the chunk's tokens (kv_b_proj output rows).
+ * Every other argument is that of mla_context_kv_pack.
+ */
+mla_status_t mla_context_kv_pack_paged(
+    const void* k_nope, int64_t kn_token_stride, int64_t kn_head_stride, const void* v,
+    int64_t v_token_stride, int64_t v_head_stride, const void* kv_cache, mla_dtype_t cache_dtype,
+    int64_t num_blocks, int32_t block_size, int64_t block_stride, int64_t entry_stride,
+    int64_t rope_offset, const int32_t* block_table, int64_t block_table_stride,
+    const int32_t* cu_chunk_lens, const int32_t* chunk_starts, int32_t num_seqs,
+    int32_t num_tokens, int32_t num_heads, int32_t nope_dim, int32_t rope_dim, int32_t v_dim,
+    void* key_out, void* v_out, mla_dtype_t out_dtype, const float* out_scale,
+    uint32_t* err_word, mla_stream_t stream);
 
 /*
  * Fill the rotary cos/sin table the insert's RoPE reads ("PR #50585", Source

@@ -89,6 +89,55 @@ mla::LaunchCfg cfg_for(mla_stream_t stream) {
     if (st_ != MLA_OK) return st_;     \
   } while (0)
 
+// Checks of a paged cache and its chunk's sequence description, shared by the
+// gathers and the paged pack; no CUDA call.  Each cache row is read from
+// element row_off for row_len elements of size ce.
+mla_status_t check_paged(const void* kv_cache, int64_t num_blocks, int32_t block_size,
+                         int64_t block_stride, int64_t entry_stride, int64_t row_off,
+                         int64_t row_len, int ce, const int32_t* block_table,
+                         int64_t block_table_stride, const int32_t* cu, const int32_t* starts,
+                         int32_t num_seqs) {
+  if (num_seqs <= 0) return fail(MLA_ERR_INVALID_ARG, "num_seqs must be >= 1");
+  if (block_size <= 0 || num_blocks <= 0 || block_table_stride <= 0)
+    return fail(MLA_ERR_INVALID_ARG, "block_size, num_blocks and block_table_stride must be >= 1");
+  if (row_off < 0 || row_len <= 0 || row_off + row_len > entry_stride)
+    return fail(MLA_ERR_INVALID_ARG, "the row part read must lie in [0, entry_stride)");
+  if (block_stride < (int64_t)(block_size - 1) * entry_stride + row_off + row_len)
+    return fail(MLA_ERR_INVALID_ARG, "block_stride is too small for block_size entries");
+  if (!a16(kv_cache) || !m16(block_stride * ce) || !m16(entry_stride * ce))
+    return fail(MLA_ERR_MISALIGNED, "cache rows must start on 16-byte boundaries");
+  if ((reinterpret_cast<uintptr_t>(block_table) | reinterpret_cast<uintptr_t>(cu) |
+       reinterpret_cast<uintptr_t>(starts)) & 3)
+    return fail(MLA_ERR_MISALIGNED, "int32 index arrays must be 4-byte aligned");
+  return MLA_OK;
+}
+
+mla::PagedSrc paged_src(const void* kv_cache, int64_t num_blocks, int32_t block_size,
+                        int64_t block_stride, int64_t entry_stride, int ce,
+                        const int32_t* block_table, int64_t block_table_stride,
+                        const int32_t* cu, const int32_t* starts, int32_t num_seqs) {
+  mla::PagedSrc p{};
+  p.cache = static_cast<const uint8_t*>(kv_cache);
+  p.block_stride = block_stride * ce;
+  p.entry_stride = entry_stride * ce;
+  p.num_blocks = num_blocks;
+  p.block_size = block_size;
+  p.bs_shift = log2_exact(block_size);
+  p.block_table = block_table;
+  p.bt_stride = block_table_stride;
+  p.cu = cu;
+  p.starts = starts;
+  p.num_seqs = num_seqs;
+  return p;
+}
+
+mla_status_t check_paged_ptrs(const int32_t* block_table, const int32_t* cu,
+                              const int32_t* starts) {
+  MLA_TRY(check_device_ptr(block_table, "block_table"));
+  MLA_TRY(check_device_ptr(cu, "cu_chunk_lens"));
+  return check_device_ptr(starts, "chunk_starts");
+}
+
 }  // namespace
 
 namespace mla {
@@ -255,82 +304,87 @@ mla_status_t mla_cache_insert_grouped(
                   "mla_cache_insert_grouped");
 }
 
-mla_status_t mla_context_gather(const void* kv_cache, mla_dtype_t cache_dtype, int64_t num_blocks,
-                                int32_t block_size, int64_t block_stride, int64_t entry_stride,
-                                int32_t entry_dim, const int32_t* block_table,
-                                int64_t block_table_stride, const int32_t* cu_chunk_lens,
-                                const int32_t* chunk_starts, int32_t num_seqs, int32_t num_tokens,
-                                void* out, int64_t out_row_stride, mla_dtype_t out_dtype,
-                                uint32_t* err_word, mla_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The gathers: out_dtype == cache_dtype (raw) or MLA_BF16 from an fp8 cache
+// (widened exactly, or times *dequant_scale when it is set).
+mla_status_t gather_impl(const void* kv_cache, mla_dtype_t cache_dtype, int64_t num_blocks,
+                         int32_t block_size, int64_t block_stride, int64_t entry_stride,
+                         int32_t entry_dim, const int32_t* block_table,
+                         int64_t block_table_stride, const int32_t* cu_chunk_lens,
+                         const int32_t* chunk_starts, int32_t num_seqs, int32_t num_tokens,
+                         void* out, int64_t out_row_stride, mla_dtype_t out_dtype,
+                         const float* dequant_scale, uint32_t* err_word, mla_stream_t stream,
+                         const char* what) {
   if (num_tokens < 0) return fail(MLA_ERR_INVALID_ARG, "num_tokens must be >= 0");
-  if (num_seqs <= 0) return fail(MLA_ERR_INVALID_ARG, "num_seqs must be >= 1");
   if (!valid_dtype(cache_dtype) || !valid_dtype(out_dtype))
     return fail(MLA_ERR_INVALID_ARG, "cache_dtype / out_dtype must be an mla_dtype_t value");
   if (out_dtype != cache_dtype && !(cache_dtype != MLA_BF16 && out_dtype == MLA_BF16))
     return fail(MLA_ERR_UNSUPPORTED,
                 "out_dtype must equal cache_dtype (raw) or be MLA_BF16 from an fp8 cache");
-  if (block_size <= 0 || num_blocks <= 0 || block_table_stride <= 0)
-    return fail(MLA_ERR_INVALID_ARG, "block_size, num_blocks and block_table_stride must be >= 1");
-  if (entry_dim <= 0 || entry_dim > entry_stride)
-    return fail(MLA_ERR_INVALID_ARG, "entry_dim must be in [1, entry_stride]");
-  if (block_stride < (int64_t)(block_size - 1) * entry_stride + entry_dim)
-    return fail(MLA_ERR_INVALID_ARG, "block_stride is too small for block_size entries");
   const int ce = elt_size(cache_dtype), oe = elt_size(out_dtype);
+  MLA_TRY(check_paged(kv_cache, num_blocks, block_size, block_stride, entry_stride, 0, entry_dim,
+                      ce, block_table, block_table_stride, cu_chunk_lens, chunk_starts,
+                      num_seqs));
   if (out_row_stride < entry_dim) return fail(MLA_ERR_INVALID_ARG, "out_row_stride must be >= entry_dim");
   if (!m16((int64_t)entry_dim * ce))
     return fail(MLA_ERR_MISALIGNED, "entry_dim must span a multiple of 16 bytes");
   if ((int64_t)entry_dim * ce > 1536)
     return fail(MLA_ERR_UNSUPPORTED, "rows longer than 1536 bytes are not built");
-  if (!a16(kv_cache) || !m16(block_stride * ce) || !m16(entry_stride * ce))
-    return fail(MLA_ERR_MISALIGNED, "cache rows must start on 16-byte boundaries");
   if (!a16(out) || !m16(out_row_stride * oe))
     return fail(MLA_ERR_MISALIGNED, "out rows must start on 16-byte boundaries");
-  if ((reinterpret_cast<uintptr_t>(block_table) | reinterpret_cast<uintptr_t>(cu_chunk_lens) |
-       reinterpret_cast<uintptr_t>(chunk_starts)) & 3)
-    return fail(MLA_ERR_MISALIGNED, "int32 index arrays must be 4-byte aligned");
+  if (dequant_scale && (reinterpret_cast<uintptr_t>(dequant_scale) & 3))
+    return fail(MLA_ERR_MISALIGNED, "k_scale must be 4-byte aligned");
   if (err_word && (reinterpret_cast<uintptr_t>(err_word) & 3))
     return fail(MLA_ERR_MISALIGNED, "err_word must be 4-byte aligned");
   if (num_tokens == 0) return MLA_OK;  // empty inputs may have null data pointers
   if (!kv_cache || !block_table || !cu_chunk_lens || !chunk_starts || !out)
     return fail(MLA_ERR_INVALID_ARG, "kv_cache, block_table, cu_chunk_lens, chunk_starts and out must be non-null");
 
-  MLA_TRY(check_device_ptr(block_table, "block_table"));
-  MLA_TRY(check_device_ptr(cu_chunk_lens, "cu_chunk_lens"));
-  MLA_TRY(check_device_ptr(chunk_starts, "chunk_starts"));
+  MLA_TRY(check_paged_ptrs(block_table, cu_chunk_lens, chunk_starts));
+  if (dequant_scale) MLA_TRY(check_device_ptr(dequant_scale, "k_scale"));
 
   mla::GatherArgs a{};
-  a.cache = static_cast<const uint8_t*>(kv_cache);
-  a.block_stride = block_stride * ce;
-  a.entry_stride = entry_stride * ce;
-  a.num_blocks = num_blocks;
-  a.block_size = block_size;
-  a.bs_shift = log2_exact(block_size);
+  a.src = paged_src(kv_cache, num_blocks, block_size, block_stride, entry_stride, ce, block_table,
+                    block_table_stride, cu_chunk_lens, chunk_starts, num_seqs);
   a.row_chunks = (int32_t)((int64_t)entry_dim * ce / 16);
-  a.block_table = block_table;
-  a.bt_stride = block_table_stride;
-  a.cu = cu_chunk_lens;
-  a.starts = chunk_starts;
-  a.num_seqs = num_seqs;
   a.num_tokens = num_tokens;
   a.out = static_cast<uint8_t*>(out);
   a.out_rs = out_row_stride * oe;
+  a.dequant_scale = dequant_scale;
   a.err = err_word;
   const int mode = (out_dtype == cache_dtype) ? 0 : (int)cache_dtype;
-  return launched(mla::launch_gather(a, mode, cfg_for(stream)), "mla_context_gather");
+  return launched(mla::launch_gather(a, mode, cfg_for(stream)), what);
 }
 
-mla_status_t mla_context_kv_pack(const void* k_nope, int64_t kn_token_stride,
-                                 int64_t kn_head_stride, const void* v, int64_t v_token_stride,
-                                 int64_t v_head_stride, const void* k_pe,
-                                 int64_t kpe_token_stride, mla_dtype_t kpe_dtype,
-                                 int32_t num_tokens, int32_t num_heads, int32_t nope_dim,
-                                 int32_t rope_dim, int32_t v_dim, void* key_out, void* v_out,
-                                 mla_dtype_t out_dtype, const float* out_scale,
-                                 uint32_t* err_word, mla_stream_t stream) {
+// The packs: k_pe given as rows (paged == nullptr) or read from the paged
+// cache at element rope_offset of each token's row (kpe_dtype = the cache's).
+struct PagedKpe {
+  const void* kv_cache;
+  int64_t num_blocks;
+  int32_t block_size;
+  int64_t block_stride, entry_stride, rope_offset;
+  const int32_t* block_table;
+  int64_t block_table_stride;
+  const int32_t* cu;
+  const int32_t* starts;
+  int32_t num_seqs;
+};
+
+mla_status_t pack_impl(const void* k_nope, int64_t kn_token_stride, int64_t kn_head_stride,
+                       const void* v, int64_t v_token_stride, int64_t v_head_stride,
+                       const void* k_pe, int64_t kpe_token_stride, mla_dtype_t kpe_dtype,
+                       const PagedKpe* paged, int32_t num_tokens, int32_t num_heads,
+                       int32_t nope_dim, int32_t rope_dim, int32_t v_dim, void* key_out,
+                       void* v_out, mla_dtype_t out_dtype, const float* out_scale,
+                       uint32_t* err_word, mla_stream_t stream, const char* what) {
   if (num_tokens < 0) return fail(MLA_ERR_INVALID_ARG, "num_tokens must be >= 0");
   if (num_heads <= 0) return fail(MLA_ERR_INVALID_ARG, "num_heads must be >= 1");
   if (!valid_dtype(out_dtype) || !valid_dtype(kpe_dtype))
-    return fail(MLA_ERR_INVALID_ARG, "out_dtype / kpe_dtype must be an mla_dtype_t value");
+    return fail(MLA_ERR_INVALID_ARG, "out_dtype / %s must be an mla_dtype_t value",
+                paged ? "cache_dtype" : "kpe_dtype");
   if (nope_dim != 128 || rope_dim != 64 || v_dim != 128)
     return fail(MLA_ERR_UNSUPPORTED, "only nope 128, rope 64, v 128 are built (got %d, %d, %d)",
                 nope_dim, rope_dim, v_dim);
@@ -344,9 +398,19 @@ mla_status_t mla_context_kv_pack(const void* k_nope, int64_t kn_token_stride,
   if (v_out && (!a16(v) || !m16(v_token_stride * 2) || !m16(v_head_stride * 2)))
     return fail(MLA_ERR_MISALIGNED, "v rows must start on 16-byte boundaries");
   const int ke = elt_size(kpe_dtype);
-  if ((reinterpret_cast<uintptr_t>(k_pe) & (ke == 2 ? 15 : 7)) ||
-      ((kpe_token_stride * ke) & (ke == 2 ? 15 : 7)))
-    return fail(MLA_ERR_MISALIGNED, "k_pe rows must start on %d-byte boundaries", ke == 2 ? 16 : 8);
+  const int kpe_align = ke == 2 ? 15 : 7;
+  if (paged) {
+    MLA_TRY(check_paged(paged->kv_cache, paged->num_blocks, paged->block_size,
+                        paged->block_stride, paged->entry_stride, paged->rope_offset, rope_dim,
+                        ke, paged->block_table, paged->block_table_stride, paged->cu,
+                        paged->starts, paged->num_seqs));
+    if ((paged->rope_offset * ke) & kpe_align)
+      return fail(MLA_ERR_MISALIGNED, "rope_offset must start k_pe on a %d-byte boundary",
+                  kpe_align + 1);
+  } else if ((reinterpret_cast<uintptr_t>(k_pe) & kpe_align) ||
+             ((kpe_token_stride * ke) & kpe_align)) {
+    return fail(MLA_ERR_MISALIGNED, "k_pe rows must start on %d-byte boundaries", kpe_align + 1);
+  }
   if (!a16(key_out) || (v_out && !a16(v_out)))
     return fail(MLA_ERR_MISALIGNED, "key_out and v_out must be 16-byte aligned");
   if (out_scale && (reinterpret_cast<uintptr_t>(out_scale) & 3))
@@ -354,10 +418,15 @@ mla_status_t mla_context_kv_pack(const void* k_nope, int64_t kn_token_stride,
   if (err_word && (reinterpret_cast<uintptr_t>(err_word) & 3))
     return fail(MLA_ERR_MISALIGNED, "err_word must be 4-byte aligned");
   if (num_tokens == 0) return MLA_OK;  // empty inputs may have null data pointers
-  if (!k_nope || !k_pe || !key_out || (v_out && !v))
-    return fail(MLA_ERR_INVALID_ARG, "k_nope, k_pe, key_out (and v when v_out is set) must be non-null");
+  if (!k_nope || !key_out || (v_out && !v))
+    return fail(MLA_ERR_INVALID_ARG, "k_nope, key_out (and v when v_out is set) must be non-null");
+  if (paged ? (!paged->kv_cache || !paged->block_table || !paged->cu || !paged->starts) : !k_pe)
+    return fail(MLA_ERR_INVALID_ARG,
+                paged ? "kv_cache, block_table, cu_chunk_lens and chunk_starts must be non-null"
+                      : "k_pe must be non-null");
 
   if (out_scale) MLA_TRY(check_device_ptr(out_scale, "out_scale"));
+  if (paged) MLA_TRY(check_paged_ptrs(paged->block_table, paged->cu, paged->starts));
 
   mla::PackArgs a{};
   a.k_nope = static_cast<const uint8_t*>(k_nope);
@@ -374,8 +443,83 @@ mla_status_t mla_context_kv_pack(const void* k_nope, int64_t kn_token_stride,
   a.vout = static_cast<uint8_t*>(v_out);
   a.out_scale = out_scale;
   a.err = err_word;
-  return launched(mla::launch_pack(a, (int)out_dtype, (int)kpe_dtype, cfg_for(stream)),
-                  "mla_context_kv_pack");
+  if (paged) {
+    a.paged = paged_src(paged->kv_cache, paged->num_blocks, paged->block_size,
+                        paged->block_stride, paged->entry_stride, ke, paged->block_table,
+                        paged->block_table_stride, paged->cu, paged->starts, paged->num_seqs);
+    a.pe_off = paged->rope_offset * ke;
+  }
+  return launched(mla::launch_pack(a, (int)out_dtype, (int)kpe_dtype, paged != nullptr,
+                                   cfg_for(stream)),
+                  what);
+}
+
+}  // namespace
+
+extern "C" {
+
+mla_status_t mla_context_gather(const void* kv_cache, mla_dtype_t cache_dtype, int64_t num_blocks,
+                                int32_t block_size, int64_t block_stride, int64_t entry_stride,
+                                int32_t entry_dim, const int32_t* block_table,
+                                int64_t block_table_stride, const int32_t* cu_chunk_lens,
+                                const int32_t* chunk_starts, int32_t num_seqs, int32_t num_tokens,
+                                void* out, int64_t out_row_stride, mla_dtype_t out_dtype,
+                                uint32_t* err_word, mla_stream_t stream) {
+  return gather_impl(kv_cache, cache_dtype, num_blocks, block_size, block_stride, entry_stride,
+                     entry_dim, block_table, block_table_stride, cu_chunk_lens, chunk_starts,
+                     num_seqs, num_tokens, out, out_row_stride, out_dtype, nullptr, err_word,
+                     stream, "mla_context_gather");
+}
+
+mla_status_t mla_context_gather_scaled(const void* kv_cache, mla_dtype_t cache_dtype,
+                                       int64_t num_blocks, int32_t block_size,
+                                       int64_t block_stride, int64_t entry_stride,
+                                       int32_t entry_dim, const int32_t* block_table,
+                                       int64_t block_table_stride, const int32_t* cu_chunk_lens,
+                                       const int32_t* chunk_starts, int32_t num_seqs,
+                                       int32_t num_tokens, void* out, int64_t out_row_stride,
+                                       const float* k_scale, uint32_t* err_word,
+                                       mla_stream_t stream) {
+  if (cache_dtype != MLA_FP8_E4M3 && cache_dtype != MLA_FP8_E5M2)
+    return fail(valid_dtype(cache_dtype) ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG,
+                "the scaled gather dequantises an fp8 cache (cache_dtype must be fp8)");
+  if (!k_scale) return fail(MLA_ERR_INVALID_ARG, "k_scale must be non-null");
+  return gather_impl(kv_cache, cache_dtype, num_blocks, block_size, block_stride, entry_stride,
+                     entry_dim, block_table, block_table_stride, cu_chunk_lens, chunk_starts,
+                     num_seqs, num_tokens, out, out_row_stride, MLA_BF16, k_scale, err_word,
+                     stream, "mla_context_gather_scaled");
+}
+
+mla_status_t mla_context_kv_pack(const void* k_nope, int64_t kn_token_stride,
+                                 int64_t kn_head_stride, const void* v, int64_t v_token_stride,
+                                 int64_t v_head_stride, const void* k_pe,
+                                 int64_t kpe_token_stride, mla_dtype_t kpe_dtype,
+                                 int32_t num_tokens, int32_t num_heads, int32_t nope_dim,
+                                 int32_t rope_dim, int32_t v_dim, void* key_out, void* v_out,
+                                 mla_dtype_t out_dtype, const float* out_scale,
+                                 uint32_t* err_word, mla_stream_t stream) {
+  return pack_impl(k_nope, kn_token_stride, kn_head_stride, v, v_token_stride, v_head_stride,
+                   k_pe, kpe_token_stride, kpe_dtype, nullptr, num_tokens, num_heads, nope_dim,
+                   rope_dim, v_dim, key_out, v_out, out_dtype, out_scale, err_word, stream,
+                   "mla_context_kv_pack");
+}
+
+mla_status_t mla_context_kv_pack_paged(
+    const void* k_nope, int64_t kn_token_stride, int64_t kn_head_stride, const void* v,
+    int64_t v_token_stride, int64_t v_head_stride, const void* kv_cache, mla_dtype_t cache_dtype,
+    int64_t num_blocks, int32_t block_size, int64_t block_stride, int64_t entry_stride,
+    int64_t rope_offset, const int32_t* block_table, int64_t block_table_stride,
+    const int32_t* cu_chunk_lens, const int32_t* chunk_starts, int32_t num_seqs,
+    int32_t num_tokens, int32_t num_heads, int32_t nope_dim, int32_t rope_dim, int32_t v_dim,
+    void* key_out, void* v_out, mla_dtype_t out_dtype, const float* out_scale,
+    uint32_t* err_word, mla_stream_t stream) {
+  const PagedKpe pk{kv_cache,      num_blocks,   block_size,  block_stride,
+                    entry_stride,  rope_offset,  block_table, block_table_stride,
+                    cu_chunk_lens, chunk_starts, num_seqs};
+  return pack_impl(k_nope, kn_token_stride, kn_head_stride, v, v_token_stride, v_head_stride,
+                   nullptr, 0, cache_dtype, &pk, num_tokens, num_heads, nope_dim, rope_dim,
+                   v_dim, key_out, v_out, out_dtype, out_scale, err_word, stream,
+                   "mla_context_kv_pack_paged");
 }
 
 mla_status_t mla_rope_cos_sin_cache(float* out, int64_t max_position, int32_t rot_dim,

@@ -99,7 +99,7 @@ __device__ __forceinline__ uint32_t pack_fp8x4(float a0, float a1, float a2, flo
 // finite f16 obtained this way is a bf16 value, so truncating the fp32 is
 // exact.  A NaN becomes the quiet NaN 0x7FC0 with the fp8 code's sign.
 template <int F>
-__device__ __forceinline__ uint32_t fp8x2_to_bf16x2(uint32_t w) {
+__device__ __forceinline__ void fp8x2_to_f32x2(uint32_t w, float& f0, float& f1) {
   uint32_t h2;
   const uint16_t in = static_cast<uint16_t>(w);
   if constexpr (F == kE4M3) {
@@ -107,9 +107,15 @@ __device__ __forceinline__ uint32_t fp8x2_to_bf16x2(uint32_t w) {
   } else {
     asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(h2) : "h"(in));
   }
-  float f0, f1;
   asm("{ .reg .b16 a, b; mov.b32 {a, b}, %2; cvt.f32.f16 %0, a; cvt.f32.f16 %1, b; }"
       : "=f"(f0), "=f"(f1) : "r"(h2));
+}
+
+template <int F>
+__device__ __forceinline__ uint32_t fp8x2_to_bf16x2(uint32_t w) {
+  const uint16_t in = static_cast<uint16_t>(w);
+  float f0, f1;
+  fp8x2_to_f32x2<F>(w, f0, f1);
   uint32_t b0 = __float_as_uint(f0) >> 16, b1 = __float_as_uint(f1) >> 16;
   // the widening does not keep a NaN's sign: take it from the fp8 byte
   if (f0 != f0) b0 = ((in & 0x80u) << 8) | 0x7FC0u;
@@ -288,6 +294,55 @@ __device__ __forceinline__ uint4 fp8x8_to_bf16x8(uint2 v) {
   o.z = fp8x2_to_bf16x2<F>(v.y);
   o.w = fp8x2_to_bf16x2<F>(v.y >> 16);
   return o;
+}
+
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+template <int F>
+__device__ __forceinline__ bool fp8_is_nan(uint32_t c) {
+  return F == kE4M3 ? (c & 0x7Fu) == 0x7Fu : (c & 0x7Fu) > 0x7Cu;
+}
+
+// Eight fp8 -> bf16 dequantised by a scale (s2 = the scale in both halves):
+// each element is the fp8 value (exact in f16 and in fp32) times the scale as
+// one fp32 multiplication, rounded to bf16 with round to nearest even.  A NaN
+// code gives the quiet NaN with the code's sign, any other NaN product the
+// positive quiet NaN.  One NaN test of the sum of the eight products sends
+// the rare group holding a NaN (or an inf - inf) through the per-element rule.
+template <int F>
+__device__ __forceinline__ uint4 fp8x8_to_bf16x8_scaled(uint2 v, uint64_t s2) {
+  const uint32_t w[4] = {v.x, v.x >> 16, v.y, v.y >> 16};
+  uint64_t p[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float a, b;
+    fp8x2_to_f32x2<F>(w[i], a, b);
+    p[i] = mul2(f2(a, b), s2);
+  }
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 q = unf2(p[i]);
+    o[i] = pack_bf16x2(q.x, q.y);
+  }
+  const float2 t = unf2(add2(add2(p[0], p[1]), add2(p[2], p[3])));
+  const float u = t.x + t.y;
+  if (__builtin_expect(u != u, 0)) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 q = unf2(p[i]);
+      const uint32_t c0 = w[i] & 0xFFu, c1 = (w[i] >> 8) & 0xFFu;
+      if (q.x != q.x)
+        o[i] = (o[i] & 0xFFFF0000u) | (fp8_is_nan<F>(c0) ? (c0 & 0x80u) << 8 : 0u) | 0x7FC0u;
+      if (q.y != q.y)
+        o[i] = (o[i] & 0xFFFFu) | (((fp8_is_nan<F>(c1) ? (c1 & 0x80u) << 8 : 0u) | 0x7FC0u) << 16);
+    }
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 // a*b - c*d accurate to two ulps even when the products cancel: the rounding

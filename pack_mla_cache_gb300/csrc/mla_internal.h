@@ -33,19 +33,28 @@ struct InsertArgs {
   bool use_tma;  // allow the bulk-copy pipeline shape
 };
 
-struct GatherArgs {
+// A paged cache and the chunk's sequences: chunk token i of sequence s
+// (cu[s] <= i < cu[s+1]) is context position starts[s] + i - cu[s], held in
+// block block_table[s * bt_stride + position / block_size].
+struct PagedSrc {
   const uint8_t* cache;
   int64_t block_stride, entry_stride;
   int64_t num_blocks;
-  int32_t block_size, bs_shift;
-  int32_t row_chunks;  // 16-byte chunks of the copied part of a cache row
+  int32_t block_size, bs_shift;  // bs_shift = log2(block_size) or -1
   const int32_t* block_table;
   int64_t bt_stride;  // elements
   const int32_t* cu;
   const int32_t* starts;
-  int32_t num_seqs, num_tokens;
+  int32_t num_seqs;
+};
+
+struct GatherArgs {
+  PagedSrc src;
+  int32_t row_chunks;  // 16-byte chunks of the copied part of a cache row
+  int32_t num_tokens;
   uint8_t* out;
   int64_t out_rs;
+  const float* dequant_scale;  // scaled widening only
   uint32_t* err;
 };
 
@@ -60,7 +69,9 @@ struct PackArgs {
   uint8_t* key;
   uint8_t* vout;  // may be null
   const float* out_scale;  // may be null (1.0)
-  uint32_t* err;  // may be null (no pack condition sets a bit today)
+  uint32_t* err;  // may be null; only the paged pack sets bits
+  PagedSrc paged;  // paged pack: k_pe = the cache row of each token, at pe_off
+  int64_t pe_off;  // bytes
 };
 
 struct LaunchCfg {
@@ -72,8 +83,12 @@ struct LaunchCfg {
 // take the values of mla::Fmt.
 cudaError_t launch_insert(const InsertArgs& a, int cache_fmt, bool norm, bool rope,
                           const LaunchCfg& cfg);
+// mode: 0 raw copy, else the fp8 format widened to bf16 (scaled when
+// a.dequant_scale is set).
 cudaError_t launch_gather(const GatherArgs& a, int mode, const LaunchCfg& cfg);
-cudaError_t launch_pack(const PackArgs& a, int out_fmt, int kpe_fmt, const LaunchCfg& cfg);
+// paged: k_pe from a.paged (kpe_fmt = the cache's format) instead of a.k_pe.
+cudaError_t launch_pack(const PackArgs& a, int out_fmt, int kpe_fmt, bool paged,
+                        const LaunchCfg& cfg);
 cudaError_t launch_rope_table(float* out, int64_t max_position, int32_t rot_dim, double base,
                               const LaunchCfg& cfg);
 

@@ -20,8 +20,14 @@
 // once per launch) and the hardware .satfinite converters; an fp8 k_pe is
 // copied byte for byte; an fp8 k_pe into a bf16 key goes through the exact
 // widening.  Any strides, no-V packs and any head count take the same kernel.
+//
+// The paged form reads each token's k_pe straight from the paged cache (the
+// row the context gather would fetch, paged.cuh), so the gather workspace only
+// needs the kv_c columns; a token whose row is not found keeps its key's rope
+// slice and, for a bad block index or id, sets MLA_ERRBIT_BLOCK_OOB.
 #include "mla_device.cuh"
 #include "mla_internal.h"
+#include "paged.cuh"
 
 namespace mla {
 namespace {
@@ -76,7 +82,7 @@ __device__ __forceinline__ void put_pe(uint8_t* dst, const uint4& o16, const uin
 // ---- plain vectorised variant -------------------------------------------------
 constexpr int kThreads = 256;
 
-template <int OF, int KF, bool FAST>
+template <int OF, int KF, bool FAST, bool PAGED>
 __device__ __forceinline__ void pack_plain_items(const PackArgs& a, const DivConst& k) {
   constexpr int OE = (OF == kBF16) ? 2 : 1;
   const int lane = threadIdx.x & 31, H = a.num_heads;
@@ -86,8 +92,18 @@ __device__ __forceinline__ void pack_plain_items(const PackArgs& a, const DivCon
   const bool has_v = a.vout != nullptr;
   const int part_pe = lane & 7;
   const int half = lane >> 4, part = lane & 15;  // v half (lanes 16-31) / unit in the half
+  SeqLanes sl{};
+  if constexpr (PAGED) sl = load_seq_lanes(a.paged, lane);
+  uint32_t errbits = 0;
   for (int64_t j = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5; j < n_items; j += nwarps) {
     const Item it = item_of(j, groups, H);
+    const uint8_t* pe;
+    if constexpr (PAGED) {
+      pe = paged_row(a.paged, sl, lane, it.t, errbits);
+      if (pe) pe += a.pe_off;
+    } else {
+      pe = a.k_pe + it.t * a.kpe_ts;
+    }
     const uint8_t* src = (half ? a.v + it.t * a.v_ts : a.k_nope + it.t * a.kn_ts) + part * 16;
     const int64_t hs = half ? a.v_hs : a.kn_hs;
     uint4 x[kGroup];
@@ -98,8 +114,7 @@ __device__ __forceinline__ void pack_plain_items(const PackArgs& a, const DivCon
     }
     uint4 p16 = make_uint4(0, 0, 0, 0);
     uint2 p8 = make_uint2(0, 0);
-    {
-      const uint8_t* pe = a.k_pe + it.t * a.kpe_ts;
+    if (!PAGED || pe) {
       uint4 x16 = make_uint4(0, 0, 0, 0);
       uint2 x8 = make_uint2(0, 0);
       if constexpr (KF == kBF16) x16 = ld_stream16(pe + part_pe * 16);
@@ -113,12 +128,17 @@ __device__ __forceinline__ void pack_plain_items(const PackArgs& a, const DivCon
 #pragma unroll
     for (int i = 0; i < kGroup; ++i)
       if (i < it.nh && (!half || has_v)) put_unit<OF, FAST>(dst + i * dstride, x[i], k);
-    for (int u = lane; u < it.nh * 8; u += 32)
-      put_pe<OF>(key + ((u >> 3) * kKey + kNope + part_pe * 8) * OE, p16, p8);
+    if (!PAGED || pe)
+      for (int u = lane; u < it.nh * 8; u += 32)
+        put_pe<OF>(key + ((u >> 3) * kKey + kNope + part_pe * 8) * OE, p16, p8);
+  }
+  if constexpr (PAGED) {
+    errbits = __reduce_or_sync(0xFFFFFFFFu, errbits);
+    if (errbits && lane == 0 && a.err) atomicOr(a.err, errbits);
   }
 }
 
-template <int OF, int KF>
+template <int OF, int KF, bool PAGED>
 __global__ void __launch_bounds__(kThreads) pack_kernel(const PackArgs a) {
   pdl_trigger();
   pdl_wait();
@@ -128,10 +148,10 @@ __global__ void __launch_bounds__(kThreads) pack_kernel(const PackArgs a) {
   }
   const DivConst k = div_const(scale);
   if constexpr (OF == kBF16) {
-    pack_plain_items<OF, KF, true>(a, k);
+    pack_plain_items<OF, KF, true, PAGED>(a, k);
   } else {
-    if (k.fast) pack_plain_items<OF, KF, true>(a, k);
-    else pack_plain_items<OF, KF, false>(a, k);
+    if (k.fast) pack_plain_items<OF, KF, true, PAGED>(a, k);
+    else pack_plain_items<OF, KF, false, PAGED>(a, k);
   }
 }
 
@@ -145,9 +165,9 @@ cudaLaunchConfig_t base_cfg(const LaunchCfg& cfg, cudaLaunchAttribute* attr) {
   return lc;
 }
 
-template <int OF, int KF>
+template <int OF, int KF, bool PAGED>
 cudaError_t launch_plain_t(const PackArgs& a, const LaunchCfg& cfg) {
-  auto kern = pack_kernel<OF, KF>;
+  auto kern = pack_kernel<OF, KF, PAGED>;
   const int64_t items = (int64_t)a.num_tokens * ((a.num_heads + kGroup - 1) / kGroup);
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t lc = base_cfg(cfg, attr);
@@ -158,29 +178,30 @@ cudaError_t launch_plain_t(const PackArgs& a, const LaunchCfg& cfg) {
 }
 
 template <int OF, int KF>
-cudaError_t launch_variant(const PackArgs& a, const LaunchCfg& cfg) {
-  return launch_plain_t<OF, KF>(a, cfg);
+cudaError_t launch_variant(const PackArgs& a, bool paged, const LaunchCfg& cfg) {
+  return paged ? launch_plain_t<OF, KF, true>(a, cfg) : launch_plain_t<OF, KF, false>(a, cfg);
 }
 
 template <int OF>
-cudaError_t launch_kpe(const PackArgs& a, int kpe_fmt, const LaunchCfg& cfg) {
-  if (kpe_fmt == kBF16) return launch_variant<OF, kBF16>(a, cfg);
+cudaError_t launch_kpe(const PackArgs& a, int kpe_fmt, bool paged, const LaunchCfg& cfg) {
+  if (kpe_fmt == kBF16) return launch_variant<OF, kBF16>(a, paged, cfg);
   if constexpr (OF == kBF16 || OF == kE4M3) {
-    if (kpe_fmt == kE4M3) return launch_variant<OF, kE4M3>(a, cfg);
+    if (kpe_fmt == kE4M3) return launch_variant<OF, kE4M3>(a, paged, cfg);
   }
   if constexpr (OF == kBF16 || OF == kE5M2) {
-    if (kpe_fmt == kE5M2) return launch_variant<OF, kE5M2>(a, cfg);
+    if (kpe_fmt == kE5M2) return launch_variant<OF, kE5M2>(a, paged, cfg);
   }
   return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-cudaError_t launch_pack(const PackArgs& a, int out_fmt, int kpe_fmt, const LaunchCfg& cfg) {
+cudaError_t launch_pack(const PackArgs& a, int out_fmt, int kpe_fmt, bool paged,
+                        const LaunchCfg& cfg) {
   switch (out_fmt) {
-    case kBF16: return launch_kpe<kBF16>(a, kpe_fmt, cfg);
-    case kE4M3: return launch_kpe<kE4M3>(a, kpe_fmt, cfg);
-    case kE5M2: return launch_kpe<kE5M2>(a, kpe_fmt, cfg);
+    case kBF16: return launch_kpe<kBF16>(a, kpe_fmt, paged, cfg);
+    case kE4M3: return launch_kpe<kE4M3>(a, kpe_fmt, paged, cfg);
+    case kE5M2: return launch_kpe<kE5M2>(a, kpe_fmt, paged, cfg);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -56,6 +56,13 @@ SIGNATURES = {
     "mla_context_kv_pack": (ctypes.c_int, [
         _vp, _i64, _i64, _vp, _i64, _i64, _vp, _i64, ctypes.c_int, _i32, _i32, _i32, _i32, _i32,
         _vp, _vp, ctypes.c_int, _vp, _vp, _vp]),
+    "mla_context_gather_scaled": (ctypes.c_int, [
+        _vp, ctypes.c_int, _i64, _i32, _i64, _i64, _i32, _vp, _i64, _vp, _vp, _i32, _i32, _vp,
+        _i64, _vp, _vp, _vp]),
+    "mla_context_kv_pack_paged": (ctypes.c_int, [
+        _vp, _i64, _i64, _vp, _i64, _i64, _vp, ctypes.c_int, _i64, _i32, _i64, _i64, _i64, _vp,
+        _i64, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp, ctypes.c_int, _vp, _vp,
+        _vp]),
     "mla_rope_cos_sin_cache": (ctypes.c_int, [_vp, _i64, _i32, ctypes.c_double, _vp]),
 }
 
@@ -156,13 +163,46 @@ def mla_context_gather(kv_cache, cache_dtype, num_blocks, block_size, block_stri
     [S, W]; out [num_tokens, >= entry_dim] with unit last stride."""
     S = chunk_starts.shape[0]
     n = out.shape[0] if num_tokens is None else num_tokens
-    # row width of the table: its row stride (a one-row table's stride is not
-    # meaningful, so its width is used)
-    bt_stride = block_table.stride(0) if block_table.size(0) > 1 else block_table.size(1)
     _check(lib().mla_context_gather(
         _ptr(kv_cache), dtype_code(cache_dtype), num_blocks, block_size, block_stride,
-        entry_stride, entry_dim, _ptr(block_table), bt_stride, _ptr(cu_chunk_lens),
+        entry_stride, entry_dim, _ptr(block_table), _bt_stride(block_table), _ptr(cu_chunk_lens),
         _ptr(chunk_starts), S, n, _ptr(out), out.stride(0), dtype_code(out_dtype),
+        _ptr(err_word), _stream(stream)))
+
+
+def _bt_stride(block_table):
+    # row width of the table: its row stride (a one-row table's stride is not
+    # meaningful, so its width is used)
+    return block_table.stride(0) if block_table.size(0) > 1 else block_table.size(1)
+
+
+def mla_context_gather_scaled(kv_cache, cache_dtype, num_blocks, block_size, block_stride,
+                              entry_stride, entry_dim, block_table, cu_chunk_lens, chunk_starts,
+                              out, k_scale, *, num_tokens=None, err_word=None, stream=None):
+    """The gather with the fp8 -> bf16 widening times ``k_scale`` (device fp32
+    scalar tensor); out is bf16 [num_tokens, >= entry_dim]."""
+    S = chunk_starts.shape[0]
+    n = out.shape[0] if num_tokens is None else num_tokens
+    _check(lib().mla_context_gather_scaled(
+        _ptr(kv_cache), dtype_code(cache_dtype), num_blocks, block_size, block_stride,
+        entry_stride, entry_dim, _ptr(block_table), _bt_stride(block_table),
+        _ptr(cu_chunk_lens), _ptr(chunk_starts), S, n, _ptr(out), out.stride(0), _ptr(k_scale),
+        _ptr(err_word), _stream(stream)))
+
+
+def mla_context_kv_pack_paged(k_nope, v, kv_cache, cache_dtype, num_blocks, block_size,
+                              block_stride, entry_stride, block_table, cu_chunk_lens,
+                              chunk_starts, key_out, v_out, out_dtype, *, rope_offset=512,
+                              rope_dim=64, out_scale=None, err_word=None, stream=None):
+    """The pack with each token's k_pe read from its paged cache row at
+    ``rope_offset``; k_nope / v [T, H, 128] bf16 views (strided)."""
+    T, H, N = k_nope.shape
+    _check(lib().mla_context_kv_pack_paged(
+        _ptr(k_nope), k_nope.stride(0), k_nope.stride(1), _ptr(v), v.stride(0), v.stride(1),
+        _ptr(kv_cache), dtype_code(cache_dtype), num_blocks, block_size, block_stride,
+        entry_stride, rope_offset, _ptr(block_table), _bt_stride(block_table),
+        _ptr(cu_chunk_lens), _ptr(chunk_starts), chunk_starts.shape[0], T, H, N, rope_dim,
+        v.shape[2], _ptr(key_out), _ptr(v_out), dtype_code(out_dtype), _ptr(out_scale),
         _ptr(err_word), _stream(stream)))
 
 

@@ -163,6 +163,93 @@ def test_gather_argument_checks(L, kw, status):
     assert gather(L, **kw) == status
 
 
+def gather_scaled(L, **kw):
+    a = dict(cache=A, cdt=1, nb=1024, bs=64, bstride=64 * 576, estride=576, edim=576, bt=A,
+             bts=512, cu=A + 4096, st=A + 8192, S=1, T=8192, out=A + 65536, ors=576,
+             scale=A + 128, err=None)
+    a.update(kw)
+    return L.mla_context_gather_scaled(a["cache"], a["cdt"], a["nb"], a["bs"], a["bstride"],
+                                       a["estride"], a["edim"], a["bt"], a["bts"], a["cu"],
+                                       a["st"], a["S"], a["T"], a["out"], a["ors"], a["scale"],
+                                       a["err"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(T=-1), ops.MLA_ERR_INVALID_ARG),
+    (dict(cdt=0), ops.MLA_ERR_UNSUPPORTED),      # a bf16 cache has nothing to dequantise
+    (dict(cdt=7), ops.MLA_ERR_INVALID_ARG),
+    (dict(scale=None), ops.MLA_ERR_INVALID_ARG),
+    (dict(scale=A + 2), ops.MLA_ERR_MISALIGNED),
+    (dict(S=0), ops.MLA_ERR_INVALID_ARG),
+    (dict(out=A + 8), ops.MLA_ERR_MISALIGNED),
+    (dict(ors=572), ops.MLA_ERR_INVALID_ARG),
+    (dict(ors=580), ops.MLA_ERR_MISALIGNED),     # 1160-byte bf16 rows
+    (dict(bstride=63 * 576), ops.MLA_ERR_INVALID_ARG),
+    (dict(edim=2048, estride=2048, bstride=64 * 2048, ors=2048), ops.MLA_ERR_UNSUPPORTED),
+    (dict(cu=A + 2), ops.MLA_ERR_MISALIGNED),
+])
+def test_gather_scaled_argument_checks(L, kw, status):
+    assert gather_scaled(L, **kw) == status
+
+
+def test_gather_scaled_zero_tokens_is_ok_without_pointers(L):
+    assert gather_scaled(L, T=0, cache=None, bt=None, cu=None, st=None, out=None) == ops.MLA_OK
+
+
+def pack_paged(L, **kw):
+    a = dict(kn=A, kts=4160, khs=256, v=A + 256, vts=4160, vhs=256, cache=A + (3 << 30), cdt=1,
+             nb=1024, bs=64, bstride=64 * 576, estride=576, roff=512, bt=A + 4096, bts=512,
+             cu=A + 8192, st=A + 12288, S=1, T=8192, H=16, N=128, R=64, V=128,
+             key=A + (1 << 30), vout=A + (2 << 30), odt=1, scale=None, err=None)
+    a.update(kw)
+    return L.mla_context_kv_pack_paged(
+        a["kn"], a["kts"], a["khs"], a["v"], a["vts"], a["vhs"], a["cache"], a["cdt"], a["nb"],
+        a["bs"], a["bstride"], a["estride"], a["roff"], a["bt"], a["bts"], a["cu"], a["st"],
+        a["S"], a["T"], a["H"], a["N"], a["R"], a["V"], a["key"], a["vout"], a["odt"],
+        a["scale"], a["err"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(T=-1), ops.MLA_ERR_INVALID_ARG),
+    (dict(H=0), ops.MLA_ERR_INVALID_ARG),
+    (dict(S=0), ops.MLA_ERR_INVALID_ARG),
+    (dict(R=32), ops.MLA_ERR_UNSUPPORTED),
+    (dict(cdt=2, odt=1), ops.MLA_ERR_UNSUPPORTED),  # fp8 k_pe bytes of another format
+    (dict(cdt=5), ops.MLA_ERR_INVALID_ARG),
+    (dict(odt=0, scale=A), ops.MLA_ERR_INVALID_ARG),
+    (dict(roff=520), ops.MLA_ERR_INVALID_ARG),      # 520 + 64 > entry_stride
+    (dict(roff=-8), ops.MLA_ERR_INVALID_ARG),
+    (dict(roff=508), ops.MLA_ERR_MISALIGNED),       # fp8 k_pe must start on 8 bytes
+    (dict(cdt=0, odt=0, roff=508, bstride=64 * 576), ops.MLA_ERR_MISALIGNED),
+    (dict(cache=A + 8), ops.MLA_ERR_MISALIGNED),
+    (dict(estride=580, bstride=64 * 580), ops.MLA_ERR_MISALIGNED),
+    (dict(bstride=63 * 576 + 575), ops.MLA_ERR_INVALID_ARG),
+    (dict(bts=0), ops.MLA_ERR_INVALID_ARG),
+    (dict(nb=0), ops.MLA_ERR_INVALID_ARG),
+    (dict(bt=A + 2), ops.MLA_ERR_MISALIGNED),
+    (dict(kn=A + 2), ops.MLA_ERR_MISALIGNED),
+    (dict(key=A + 8), ops.MLA_ERR_MISALIGNED),
+    (dict(err=A + 1), ops.MLA_ERR_MISALIGNED),
+    (dict(cache=None), ops.MLA_ERR_INVALID_ARG),
+    (dict(bt=None), ops.MLA_ERR_INVALID_ARG),
+    (dict(kn=None), ops.MLA_ERR_INVALID_ARG),
+])
+def test_pack_paged_argument_checks(L, kw, status):
+    assert pack_paged(L, **kw) == status
+
+
+def test_pack_paged_zero_tokens_is_ok_without_pointers(L):
+    assert pack_paged(L, T=0, kn=None, v=None, cache=None, bt=None, cu=None, st=None, key=None,
+                      vout=None) == ops.MLA_OK
+
+
+def test_paged_calls_that_pass_validation_need_a_gpu(L):
+    if torch.cuda.is_available():
+        pytest.skip("this check is for machines without a GPU")
+    assert pack_paged(L) == ops.MLA_ERR_CUDA
+    assert gather_scaled(L) == ops.MLA_ERR_CUDA
+
+
 def pack(L, **kw):
     a = dict(kn=A, kts=4160, khs=256, v=A + 256, vts=4160, vhs=256, kpe=A + 1024, kpets=576,
              kdt=1, T=8192, H=16, N=128, R=64, V=128, key=A + (1 << 30), vout=A + (2 << 30), odt=1,
