@@ -94,6 +94,9 @@ def lib() -> ctypes.CDLL:
                 "orc_concat_key": (None, [vp, i64, i64, vp, i64, i32, i32, i32, i32, vp]),
                 "orc_context_kv_pack": (None, [vp, i64, i64, vp, i64, i64, vp, i64, i32, i32,
                                               i32, i32, i32, i32, vp, vp, i32, f32]),
+                "orc_norm_rope_grouped": (u32, [vp, i64, i64, vp, i64, i64, i32, i32, i32, i32,
+                                                vp, i64, f32, vp, vp, i64, vp, i64, i64, vp, i64,
+                                                i64]),
                 "orc_bf16_from_fp8_scaled": (ctypes.c_uint16, [ctypes.c_uint8, ctypes.c_int, f32]),
                 "orc_context_gather_scaled": (u32, [vp, i32, i64, i32, i64, i64, i32, vp, i64, vp,
                                                     vp, i32, i32, vp, i64, f32]),
@@ -323,3 +326,25 @@ def context_kv_pack_paged(k_nope_buf, kn_token_stride, kn_head_stride, v_buf, v_
         chunk_starts.shape[0], T, H, nope, rope, v_dim, _p(key), _p(vout), out_dtype,
         float(out_scale))
     return key, vout, err
+
+
+def norm_rope_grouped(kv_c_buf, kvc_ts, kvc_ls, k_pe_buf, kpe_ts, kpe_ls, T, L, R=512, P=64,
+                      gamma=None, gamma_ls=512, eps=1e-6, positions=None, cos_sin_cache=None,
+                      out_c=None, oc_ts=None, oc_ls=None, out_p=None, op_ts=None, op_ls=None):
+    """Grouped RMSNorm + RoPE into layer-major outputs (default [L, T, R] and
+    [L, T, P]; pass ``out_c`` / ``out_p`` with strides for other layouts).
+    Returns (kv_c_out, k_pe_out, error bits)."""
+    if out_c is None:
+        out_c, oc_ts, oc_ls = np.zeros((L, T, R), np.uint16), R, T * R
+    if out_p is None:
+        out_p, op_ts, op_ls = np.zeros((L, T, P), np.uint16), P, T * P
+    if gamma is not None:
+        _chk(gamma, np.uint16)
+    if positions is not None:
+        _chk(positions, np.int64), _chk(cos_sin_cache, np.float32)
+    err = lib().orc_norm_rope_grouped(
+        _p(kv_c_buf), kvc_ts, kvc_ls, _p(k_pe_buf), kpe_ts, kpe_ls, T, L, R, P, _p(gamma),
+        gamma_ls, float(eps), _p(positions), _p(cos_sin_cache),
+        0 if cos_sin_cache is None else cos_sin_cache.shape[0], _p(out_c), oc_ts, oc_ls,
+        _p(out_p), op_ts, op_ls)
+    return out_c, out_p, err

@@ -342,6 +342,57 @@ uint32_t orc_insert_grouped(const uint16_t* kv_c, int64_t kvc_token_stride,
   return err;
 }
 
+/*
+ * The grouped RMSNorm + RoPE of the DSpark context projection on its own
+ * ("PR #50585", Implementation item 3 and Source snippets,
+ * _precompute_fused_context_kv: the [num_ctx, L, kv_width] projection output
+ * split into kv_c and k_pe, each made layer-major, kv_c RMS-normalised with
+ * layer l's weight row, k_pe rotated with the token's position, the same
+ * positions for every layer).  For every layer l and token t, in order: if a
+ * rotation is asked for and the position lies outside [0, max_position), the
+ * row is skipped (both outputs untouched, ORC_ERR_POS_OOB); otherwise
+ *   kv_c_out[t, l] = rms_norm_row(kv_c[t, l], gamma[l])   (copy when gamma is NULL)
+ *   k_pe_out[t, l] = rope_neox_row(k_pe[t, l], table[pos[t]])  (copy when positions is NULL)
+ * with element (t, l, i) of each buffer at t * token stride + l * layer stride + i.
+ */
+uint32_t orc_norm_rope_grouped(const uint16_t* kv_c, int64_t kvc_token_stride,
+                               int64_t kvc_layer_stride, const uint16_t* k_pe,
+                               int64_t kpe_token_stride, int64_t kpe_layer_stride,
+                               int32_t num_tokens, int32_t num_layers, int32_t kv_lora_rank,
+                               int32_t pe_dim, const uint16_t* gamma, int64_t gamma_layer_stride,
+                               float eps, const int64_t* positions, const float* cos_sin_cache,
+                               int64_t max_position, uint16_t* kv_c_out, int64_t oc_token_stride,
+                               int64_t oc_layer_stride, uint16_t* k_pe_out,
+                               int64_t op_token_stride, int64_t op_layer_stride) {
+  uint32_t err = 0;
+  for (int32_t l = 0; l < num_layers; ++l) {
+    for (int32_t t = 0; t < num_tokens; ++t) {
+      const float* cs = NULL;
+      if (positions) {
+        int64_t pos = positions[t];
+        if (pos < 0 || pos >= max_position) {
+          err |= ORC_ERR_POS_OOB;
+          continue;
+        }
+        cs = cos_sin_cache + pos * (int64_t)pe_dim;
+      }
+      const uint16_t* x = kv_c + (int64_t)t * kvc_token_stride + (int64_t)l * kvc_layer_stride;
+      const uint16_t* r = k_pe + (int64_t)t * kpe_token_stride + (int64_t)l * kpe_layer_stride;
+      uint16_t* yc = kv_c_out + (int64_t)t * oc_token_stride + (int64_t)l * oc_layer_stride;
+      uint16_t* yp = k_pe_out + (int64_t)t * op_token_stride + (int64_t)l * op_layer_stride;
+      if (gamma)
+        orc_rms_norm_row(x, gamma + (int64_t)l * gamma_layer_stride, kv_lora_rank, eps, yc);
+      else
+        memcpy(yc, x, (size_t)kv_lora_rank * sizeof(uint16_t));
+      if (positions)
+        orc_rope_neox_row(r, cs, pe_dim, yp);
+      else
+        memcpy(yp, r, (size_t)pe_dim * sizeof(uint16_t));
+    }
+  }
+  return err;
+}
+
 /* ======================================================================== */
 /* Context gather and cast ("PR #51772" Implementation item 2:              */
 /* _gather_context_latent then the conditional cast to the kv_b_proj dtype). */

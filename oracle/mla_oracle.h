@@ -92,6 +92,16 @@ uint32_t orc_insert_grouped(const uint16_t* kv_c, int64_t kvc_token_stride,
                             const int64_t* positions, const float* cos_sin_cache,
                             int64_t max_position);
 
+uint32_t orc_norm_rope_grouped(const uint16_t* kv_c, int64_t kvc_token_stride,
+                               int64_t kvc_layer_stride, const uint16_t* k_pe,
+                               int64_t kpe_token_stride, int64_t kpe_layer_stride,
+                               int32_t num_tokens, int32_t num_layers, int32_t kv_lora_rank,
+                               int32_t pe_dim, const uint16_t* gamma, int64_t gamma_layer_stride,
+                               float eps, const int64_t* positions, const float* cos_sin_cache,
+                               int64_t max_position, uint16_t* kv_c_out, int64_t oc_token_stride,
+                               int64_t oc_layer_stride, uint16_t* k_pe_out,
+                               int64_t op_token_stride, int64_t op_layer_stride);
+
 /* ---- context gather and element cast ------------------------------------ */
 uint32_t orc_context_gather(const void* cache, int32_t cache_dtype, int64_t num_blocks,
                             int32_t block_size, int64_t block_stride, int64_t entry_stride,
