@@ -530,7 +530,9 @@ def run_profile_case(name: str, launches: int, tokens: int | None = None,
       gather_kv_c    the raw gather of the 512 kv_c columns only
       pack    32768 tokens, 16 heads, fp8 e4m3 out, fp8 k_pe
       pack_bf16  the same with bf16 output and a bf16 k_pe
-      pack_paged the fp8 pack reading k_pe from a 4096-block fp8 cache"""
+      pack_paged the fp8 pack reading k_pe from a 4096-block fp8 cache
+      norm_rope  65536 tokens x 5 layers of the [T, L, 576] projection, RMSNorm +
+                 RoPE into layer-major outputs"""
     import torch
     from pack_mla_cache_gb300 import ops
     from pack_mla_cache_gb300 import workloads as W
@@ -595,6 +597,20 @@ def run_profile_case(name: str, launches: int, tokens: int | None = None,
                                              key, vo, 0 if bf else 1, kpe_dtype=0 if bf else 1,
                                              out_scale=sc)
         nbytes = T * (HEADS * 512 + (128 if bf else 64) + HEADS * 320 * (2 if bf else 1))
+    elif name == "norm_rope":
+        T = tokens or 65536
+        kv = torch.randn((T, L_LAYERS, ENTRY), generator=g, device=dev).to(torch.bfloat16)
+        pos = torch.randint(0, W.MAX_POSITION, (T,), generator=g, device=dev)
+        gamma = (1 + 0.1 * torch.randn((L_LAYERS, 512), generator=g, device=dev)).to(torch.bfloat16)
+        table = torch.empty((W.MAX_POSITION, 64), dtype=torch.float32, device=dev)
+        ops.mla_rope_cos_sin_cache(table, W.ROPE_BASE)
+        oc = torch.empty((L_LAYERS, T, 512), dtype=torch.bfloat16, device=dev)
+        op = torch.empty((L_LAYERS, T, 64), dtype=torch.bfloat16, device=dev)
+        fn = lambda: ops.mla_norm_rope_grouped(kv[:, :, :512], kv[:, :, 512:],
+                                               oc.transpose(0, 1), op.transpose(0, 1),
+                                               gamma=gamma, eps=1e-6, positions=pos,
+                                               cos_sin_cache=table)
+        nbytes = T * L_LAYERS * 2 * ENTRY * 2 + T * (8 + 256)
     elif name == "pack_paged":
         T, nb = tokens or 32768, 4096
         assert T <= nb * BS

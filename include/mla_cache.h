@@ -314,6 +314,43 @@ mla_status_t mla_context_kv_pack_paged(
     uint32_t* err_word, mla_stream_t stream);
 
 /*
+ * Grouped RMSNorm + RoPE on its own, for when the grouped insert is not the
+ * consumer ("PR #50585 [K3 Perf] Optimize k3 dspark fused kv", Implementation
+ * item 3 and Source snippets: _precompute_fused_context_kv splits the
+ * [num_ctx, L, 576] context projection into kv_c and k_pe, makes both
+ * layer-major, normalises kv_c with one weight row per layer and rotates k_pe
+ * with the token positions repeated for every layer).  One pass: for every
+ * layer l < num_layers and token t < num_tokens,
+ *   kv_c_out[t, l, :] = rmsnorm(kv_c[t, l, :], gamma[l])   (a copy without gamma)
+ *   k_pe_out[t, l, :] = rope(k_pe[t, l, :], positions[t])  (a copy without positions)
+ * with the arithmetic, rounding and table of mla_norm_rope_t (the same as the
+ * grouped insert's, so its bf16 results are identical).  A position outside
+ * [0, max_position) skips the row in both outputs (MLA_ERRBIT_POS_OOB).
+ *
+ *   kv_c, k_pe          bf16 inputs, element (t, l, i) at t * token_stride +
+ *                       l * layer_stride + i; for the [T, L, 576] projection
+ *                       read in place: kv_c = base, k_pe = base + 512, token
+ *                       stride L * 576, layer stride 576.  Rows start on
+ *                       16-byte boundaries.
+ *   kv_lora_rank, pe_dim  must be 512 and 64 (else UNSUPPORTED).
+ *   norm_rope           as for the grouped insert; NULL = the plain layout
+ *                       change.
+ *   kv_c_out, k_pe_out  bf16 outputs addressed the same way with their own
+ *                       strides (layer-major [L, T, 512] / [L, T, 64]: token
+ *                       stride 512 / 64, layer stride T * 512 / T * 64); they
+ *                       must not overlap the inputs.  Rows start on 16-byte
+ *                       boundaries.
+ *   num_tokens * num_layers < 2^32.
+ */
+mla_status_t mla_norm_rope_grouped(
+    const void* kv_c, int64_t kvc_token_stride, int64_t kvc_layer_stride, const void* k_pe,
+    int64_t kpe_token_stride, int64_t kpe_layer_stride, int32_t num_tokens, int32_t num_layers,
+    int32_t kv_lora_rank, int32_t pe_dim, const mla_norm_rope_t* norm_rope, void* kv_c_out,
+    int64_t out_c_token_stride, int64_t out_c_layer_stride, void* k_pe_out,
+    int64_t out_pe_token_stride, int64_t out_pe_layer_stride, uint32_t* err_word,
+    mla_stream_t stream);
+
+/*
  * Fill the rotary cos/sin table the insert's RoPE reads ("PR #50585", Source
  * snippets: the k_pe rotation; the table is the rotary embedding's cached
  * cos/sin): out[p * rot_dim + i] = cos(p * base^(-2i/rot_dim)) and

@@ -112,6 +112,39 @@ mla_status_t check_paged(const void* kv_cache, int64_t num_blocks, int32_t block
   return MLA_OK;
 }
 
+// The optional RMSNorm / RoPE description (no CUDA call): what it asks for
+// and its layout checks.
+mla_status_t check_norm_rope(const mla_norm_rope_t* nr, bool& norm, bool& rope) {
+  norm = rope = false;
+  if (!nr) return MLA_OK;
+  norm = nr->gamma != nullptr;
+  rope = nr->positions != nullptr;
+  if (norm) {
+    if (!a16(nr->gamma) || !m16(nr->gamma_layer_stride * 2))
+      return fail(MLA_ERR_MISALIGNED, "gamma rows must start on 16-byte boundaries");
+    if (!(nr->eps >= 0.0f) || !(nr->eps < 3.0e38f))
+      return fail(MLA_ERR_INVALID_ARG, "eps must be finite and >= 0");
+  }
+  if (rope) {
+    if (!nr->cos_sin_cache || nr->max_position <= 0)
+      return fail(MLA_ERR_INVALID_ARG, "RoPE needs cos_sin_cache and max_position >= 1");
+    if (!a16(nr->cos_sin_cache))
+      return fail(MLA_ERR_MISALIGNED, "cos_sin_cache must be 16-byte aligned");
+    if (reinterpret_cast<uintptr_t>(nr->positions) & 7)
+      return fail(MLA_ERR_MISALIGNED, "positions must be 8-byte aligned");
+  }
+  return MLA_OK;
+}
+
+mla_status_t check_norm_rope_ptrs(const mla_norm_rope_t* nr, bool norm, bool rope) {
+  if (norm) MLA_TRY(check_device_ptr(nr->gamma, "gamma"));
+  if (rope) {
+    MLA_TRY(check_device_ptr(nr->positions, "positions"));
+    MLA_TRY(check_device_ptr(nr->cos_sin_cache, "cos_sin_cache"));
+  }
+  return MLA_OK;
+}
+
 mla::PagedSrc paged_src(const void* kv_cache, int64_t num_blocks, int32_t block_size,
                         int64_t block_stride, int64_t entry_stride, int ce,
                         const int32_t* block_table, int64_t block_table_stride,
@@ -236,24 +269,7 @@ mla_status_t mla_cache_insert_grouped(
   if (err_word && (reinterpret_cast<uintptr_t>(err_word) & 3))
     return fail(MLA_ERR_MISALIGNED, "err_word must be 4-byte aligned");
   bool norm = false, rope = false;
-  if (norm_rope) {
-    norm = norm_rope->gamma != nullptr;
-    rope = norm_rope->positions != nullptr;
-    if (norm) {
-      if (!a16(norm_rope->gamma) || !m16(norm_rope->gamma_layer_stride * 2))
-        return fail(MLA_ERR_MISALIGNED, "gamma rows must start on 16-byte boundaries");
-      if (!(norm_rope->eps >= 0.0f) || !(norm_rope->eps < 3.0e38f))
-        return fail(MLA_ERR_INVALID_ARG, "eps must be finite and >= 0");
-    }
-    if (rope) {
-      if (!norm_rope->cos_sin_cache || norm_rope->max_position <= 0)
-        return fail(MLA_ERR_INVALID_ARG, "RoPE needs cos_sin_cache and max_position >= 1");
-      if (!a16(norm_rope->cos_sin_cache))
-        return fail(MLA_ERR_MISALIGNED, "cos_sin_cache must be 16-byte aligned");
-      if (reinterpret_cast<uintptr_t>(norm_rope->positions) & 7)
-        return fail(MLA_ERR_MISALIGNED, "positions must be 8-byte aligned");
-    }
-  }
+  MLA_TRY(check_norm_rope(norm_rope, norm, rope));
   if ((int64_t)((num_tokens + 3) / 4) * num_layers >= (int64_t(1) << 32))
     return fail(MLA_ERR_UNSUPPORTED, "num_tokens * num_layers is too large for one call");
   if (num_tokens == 0) return MLA_OK;  // empty inputs may have null data pointers
@@ -263,11 +279,7 @@ mla_status_t mla_cache_insert_grouped(
   MLA_TRY(check_device_ptr(slot_mapping, "slot_mapping"));
   MLA_TRY(check_device_ptr(kv_cache_ptrs, "kv_cache_ptrs"));
   if (fp8) MLA_TRY(check_device_ptr(kv_scales, "kv_scales"));
-  if (norm) MLA_TRY(check_device_ptr(norm_rope->gamma, "gamma"));
-  if (rope) {
-    MLA_TRY(check_device_ptr(norm_rope->positions, "positions"));
-    MLA_TRY(check_device_ptr(norm_rope->cos_sin_cache, "cos_sin_cache"));
-  }
+  MLA_TRY(check_norm_rope_ptrs(norm_rope, norm, rope));
 
   mla::InsertArgs a{};
   a.kv_c = static_cast<const uint8_t*>(kv_c);
@@ -520,6 +532,70 @@ mla_status_t mla_context_kv_pack_paged(
                    nullptr, 0, cache_dtype, &pk, num_tokens, num_heads, nope_dim, rope_dim,
                    v_dim, key_out, v_out, out_dtype, out_scale, err_word, stream,
                    "mla_context_kv_pack_paged");
+}
+
+mla_status_t mla_norm_rope_grouped(const void* kv_c, int64_t kvc_token_stride,
+                                   int64_t kvc_layer_stride, const void* k_pe,
+                                   int64_t kpe_token_stride, int64_t kpe_layer_stride,
+                                   int32_t num_tokens, int32_t num_layers, int32_t kv_lora_rank,
+                                   int32_t pe_dim, const mla_norm_rope_t* norm_rope,
+                                   void* kv_c_out, int64_t out_c_token_stride,
+                                   int64_t out_c_layer_stride, void* k_pe_out,
+                                   int64_t out_pe_token_stride, int64_t out_pe_layer_stride,
+                                   uint32_t* err_word, mla_stream_t stream) {
+  if (num_tokens < 0) return fail(MLA_ERR_INVALID_ARG, "num_tokens must be >= 0");
+  if (num_layers <= 0) return fail(MLA_ERR_INVALID_ARG, "num_layers must be >= 1");
+  if (kv_lora_rank != 512 || pe_dim != 64)
+    return fail(MLA_ERR_UNSUPPORTED,
+                "only kv_lora_rank 512 and pe_dim 64 are built (got %d, %d)", kv_lora_rank,
+                pe_dim);
+  if (!a16(kv_c) || !m16(kvc_token_stride * 2) || !m16(kvc_layer_stride * 2))
+    return fail(MLA_ERR_MISALIGNED, "kv_c rows must start on 16-byte boundaries");
+  if (!a16(k_pe) || !m16(kpe_token_stride * 2) || !m16(kpe_layer_stride * 2))
+    return fail(MLA_ERR_MISALIGNED, "k_pe rows must start on 16-byte boundaries");
+  if (!a16(kv_c_out) || !m16(out_c_token_stride * 2) || !m16(out_c_layer_stride * 2))
+    return fail(MLA_ERR_MISALIGNED, "kv_c_out rows must start on 16-byte boundaries");
+  if (!a16(k_pe_out) || !m16(out_pe_token_stride * 2) || !m16(out_pe_layer_stride * 2))
+    return fail(MLA_ERR_MISALIGNED, "k_pe_out rows must start on 16-byte boundaries");
+  if (err_word && (reinterpret_cast<uintptr_t>(err_word) & 3))
+    return fail(MLA_ERR_MISALIGNED, "err_word must be 4-byte aligned");
+  bool norm = false, rope = false;
+  MLA_TRY(check_norm_rope(norm_rope, norm, rope));
+  if ((int64_t)num_tokens * num_layers + 3 >= (int64_t(1) << 32))
+    return fail(MLA_ERR_UNSUPPORTED, "num_tokens * num_layers is too large for one call");
+  if (num_tokens == 0) return MLA_OK;  // empty inputs may have null data pointers
+  if (!kv_c || !k_pe || !kv_c_out || !k_pe_out)
+    return fail(MLA_ERR_INVALID_ARG, "kv_c, k_pe, kv_c_out and k_pe_out must be non-null");
+  MLA_TRY(check_norm_rope_ptrs(norm_rope, norm, rope));
+
+  mla::NormRopeArgs a{};
+  a.kv_c = static_cast<const uint8_t*>(kv_c);
+  a.kvc_ts = kvc_token_stride * 2;
+  a.kvc_ls = kvc_layer_stride * 2;
+  a.k_pe = static_cast<const uint8_t*>(k_pe);
+  a.kpe_ts = kpe_token_stride * 2;
+  a.kpe_ls = kpe_layer_stride * 2;
+  a.num_rows = (int64_t)num_tokens * num_layers;
+  a.num_tokens = num_tokens;
+  a.num_layers = num_layers;
+  if (norm) {
+    a.gamma = static_cast<const uint8_t*>(norm_rope->gamma);
+    a.gamma_ls = norm_rope->gamma_layer_stride * 2;
+    a.eps = norm_rope->eps;
+  }
+  if (rope) {
+    a.positions = norm_rope->positions;
+    a.cos_sin = norm_rope->cos_sin_cache;
+    a.max_position = norm_rope->max_position;
+  }
+  a.out_c = static_cast<uint8_t*>(kv_c_out);
+  a.oc_ts = out_c_token_stride * 2;
+  a.oc_ls = out_c_layer_stride * 2;
+  a.out_p = static_cast<uint8_t*>(k_pe_out);
+  a.op_ts = out_pe_token_stride * 2;
+  a.op_ls = out_pe_layer_stride * 2;
+  a.err = err_word;
+  return launched(mla::launch_norm_rope(a, norm, rope, cfg_for(stream)), "mla_norm_rope_grouped");
 }
 
 mla_status_t mla_rope_cos_sin_cache(float* out, int64_t max_position, int32_t rot_dim,

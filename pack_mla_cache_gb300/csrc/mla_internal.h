@@ -74,6 +74,28 @@ struct PackArgs {
   int64_t pe_off;  // bytes
 };
 
+// Standalone grouped RMSNorm + RoPE: row (t, l) of kv_c / k_pe to the
+// outputs at t * token stride + l * layer stride (bytes).
+struct NormRopeArgs {
+  const uint8_t* kv_c;
+  int64_t kvc_ts, kvc_ls;
+  const uint8_t* k_pe;
+  int64_t kpe_ts, kpe_ls;
+  int64_t num_rows;  // num_tokens * num_layers, < 2^32
+  int32_t num_tokens, num_layers;
+  const uint8_t* gamma;
+  int64_t gamma_ls;
+  float eps;
+  const int64_t* positions;
+  const float* cos_sin;
+  int64_t max_position;
+  uint8_t* out_c;
+  int64_t oc_ts, oc_ls;
+  uint8_t* out_p;
+  int64_t op_ts, op_ls;
+  uint32_t* err;
+};
+
 struct LaunchCfg {
   cudaStream_t stream;
   bool pdl;
@@ -89,6 +111,7 @@ cudaError_t launch_gather(const GatherArgs& a, int mode, const LaunchCfg& cfg);
 // paged: k_pe from a.paged (kpe_fmt = the cache's format) instead of a.k_pe.
 cudaError_t launch_pack(const PackArgs& a, int out_fmt, int kpe_fmt, bool paged,
                         const LaunchCfg& cfg);
+cudaError_t launch_norm_rope(const NormRopeArgs& a, bool norm, bool rope, const LaunchCfg& cfg);
 cudaError_t launch_rope_table(float* out, int64_t max_position, int32_t rot_dim, double base,
                               const LaunchCfg& cfg);
 

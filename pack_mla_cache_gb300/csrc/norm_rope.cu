@@ -1,0 +1,124 @@
+// norm_rope.cu -- standalone grouped RMSNorm + RoPE for sm_103a.
+//
+// What it computes: for every (token, layer) row of a [kv_c 512 | k_pe 64]
+// bf16 input (any token / layer strides, e.g. the [T, L, 576] DSpark context
+// projection read in place), kv_c RMS-normalised with layer l's weight row and
+// k_pe rotated (neox) with the token's position -- the same position for every
+// layer -- each rounded to bf16 and written to caller-strided outputs (e.g.
+// the layer-major [L, T, 512] and [L, T, 64] the insert consumes) ("PR #50585
+// [K3 Perf] Optimize k3 dspark fused kv", Implementation item 3 and Source
+// snippets: _precompute_fused_context_kv, which makes both parts layer-major
+// with permute().contiguous(), then runs the grouped rms_norm and the
+// rotation as separate passes).  Here the layout change, the norm and the
+// rotation are one pass: each row is read once and written once.
+//
+// Design: rows in token-major order; a warp takes kRows consecutive rows
+// (its loads -- two 512-byte kv_c warp loads and the k_pe pair per row --
+// issued before the first row is processed), normalises and rotates them
+// with the insert's per-lane arithmetic (norm_rope.cuh), and stores two
+// 512-byte kv_c warp stores and the k_pe pair per row.  The grid is capped at
+// the resident CTAs and loops over the rows.
+#include "mla_device.cuh"
+#include "mla_internal.h"
+#include "norm_rope.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kRows = 4;
+constexpr int kP = 64;
+
+__device__ __forceinline__ uint32_t ld_u16(const uint8_t* p) {
+  return __ldcs(reinterpret_cast<const unsigned short*>(p));
+}
+__device__ __forceinline__ void st_u16(uint8_t* p, uint32_t v) {
+  *reinterpret_cast<unsigned short*>(p) = static_cast<unsigned short>(v);
+}
+
+template <bool NORM, bool ROPE>
+__global__ void __launch_bounds__(kThreads) norm_rope_kernel(const NormRopeArgs a) {
+  pdl_trigger();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
+  const uint32_t L = (uint32_t)a.num_layers;
+  uint32_t errbits = 0;
+  for (int64_t r0 = warp * kRows; r0 < a.num_rows; r0 += nwarps * kRows) {
+    uint4 x0[kRows], x1[kRows];
+    uint32_t pe[kRows];
+    int64_t pos[kRows];
+#pragma unroll
+    for (int k = 0; k < kRows; ++k) {
+      x0[k] = x1[k] = make_uint4(0, 0, 0, 0);
+      pe[k] = 0;
+      pos[k] = 0;
+      const int64_t r = r0 + k;
+      if (r >= a.num_rows) continue;
+      const uint32_t t = (uint32_t)r / L, l = (uint32_t)r - t * L;  // rows < 2^32
+      const uint8_t* src = a.kv_c + (int64_t)t * a.kvc_ts + (int64_t)l * a.kvc_ls;
+      x0[k] = ld_stream16(src + lane * 16);
+      x1[k] = ld_stream16(src + 512 + lane * 16);
+      const uint8_t* p = a.k_pe + (int64_t)t * a.kpe_ts + (int64_t)l * a.kpe_ls;
+      pe[k] = ld_u16(p + lane * 2) | (ld_u16(p + kP + lane * 2) << 16);
+      if constexpr (ROPE) pos[k] = __ldg(a.positions + t);
+    }
+#pragma unroll
+    for (int k = 0; k < kRows; ++k) {
+      const int64_t r = r0 + k;
+      if (r >= a.num_rows) continue;
+      const uint32_t t = (uint32_t)r / L, l = (uint32_t)r - t * L;
+      float2 cs = make_float2(1.f, 0.f);
+      if constexpr (ROPE) {
+        if (pos[k] < 0 || pos[k] >= a.max_position) {  // uniform across the warp
+          errbits |= kErrPosOOB;
+          continue;
+        }
+        const float* row = a.cos_sin + pos[k] * kP;
+        cs = make_float2(__ldg(row + lane), __ldg(row + kP / 2 + lane));
+      }
+      uint4 y0 = x0[k], y1 = x1[k];
+      if constexpr (NORM) {
+        const uint8_t* g = a.gamma + (int64_t)l * a.gamma_ls;
+        rms_norm16(x0[k], x1[k], ld_shared_ro16(g + lane * 16),
+                   ld_shared_ro16(g + 512 + lane * 16), a.eps, y0, y1);
+      }
+      uint32_t p = pe[k];
+      if constexpr (ROPE) p = rope_pair(pe[k], cs);
+      uint8_t* dc = a.out_c + (int64_t)t * a.oc_ts + (int64_t)l * a.oc_ls;
+      st16(dc + lane * 16, y0);
+      st16(dc + 512 + lane * 16, y1);
+      uint8_t* dp = a.out_p + (int64_t)t * a.op_ts + (int64_t)l * a.op_ls;
+      st_u16(dp + lane * 2, p);
+      st_u16(dp + kP + lane * 2, p >> 16);
+    }
+  }
+  if (errbits && lane == 0 && a.err) atomicOr(a.err, errbits);
+}
+
+template <bool NORM, bool ROPE>
+cudaError_t launch_t(const NormRopeArgs& a, const LaunchCfg& cfg) {
+  auto kern = norm_rope_kernel<NORM, ROPE>;
+  const int64_t warps = (a.num_rows + kRows - 1) / kRows;
+  const int64_t ctas = (warps + kThreads / 32 - 1) / (kThreads / 32);
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(capped_grid(reinterpret_cast<const void*>(kern), kThreads, ctas));
+  lc.blockDim = dim3(kThreads);
+  lc.stream = cfg.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = cfg.pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&lc, kern, a);
+}
+
+}  // namespace
+
+cudaError_t launch_norm_rope(const NormRopeArgs& a, bool norm, bool rope, const LaunchCfg& cfg) {
+  if (norm) return rope ? launch_t<true, true>(a, cfg) : launch_t<true, false>(a, cfg);
+  return rope ? launch_t<false, true>(a, cfg) : launch_t<false, false>(a, cfg);
+}
+
+}  // namespace mla

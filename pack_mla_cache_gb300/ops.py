@@ -63,6 +63,9 @@ SIGNATURES = {
         _vp, _i64, _i64, _vp, _i64, _i64, _vp, ctypes.c_int, _i64, _i32, _i64, _i64, _i64, _vp,
         _i64, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp, ctypes.c_int, _vp, _vp,
         _vp]),
+    "mla_norm_rope_grouped": (ctypes.c_int, [
+        _vp, _i64, _i64, _vp, _i64, _i64, _i32, _i32, _i32, _i32, ctypes.POINTER(NormRope), _vp,
+        _i64, _i64, _vp, _i64, _i64, _vp, _vp]),
     "mla_rope_cos_sin_cache": (ctypes.c_int, [_vp, _i64, _i32, ctypes.c_double, _vp]),
 }
 
@@ -154,6 +157,25 @@ def mla_cache_insert_grouped(kv_c, k_pe, slot_mapping, kv_cache_ptrs, kv_scales,
         T, L, R, P, _ptr(slot_mapping), slot_layer_stride, _ptr(kv_cache_ptrs), _ptr(kv_scales),
         dtype_code(cache_dtype), num_blocks, block_size, block_stride, entry_stride,
         ctypes.byref(nr) if nr is not None else None, _ptr(err_word), _stream(stream)))
+
+
+def mla_norm_rope_grouped(kv_c, k_pe, kv_c_out, k_pe_out, *, gamma=None, eps=1e-6,
+                          positions=None, cos_sin_cache=None, err_word=None, stream=None):
+    """Every tensor is a bf16 view indexed [token, layer, i] (any strides, unit
+    last stride): kv_c / kv_c_out [T, L, 512], k_pe / k_pe_out [T, L, 64].  For
+    layer-major outputs pass e.g. ``out.transpose(0, 1)`` of an [L, T, .] tensor."""
+    T, L, R = kv_c.shape
+    P = k_pe.shape[2]
+    nr = None
+    if gamma is not None or positions is not None:
+        nr = NormRope(_ptr(gamma), 0 if gamma is None else gamma.stride(0), float(eps),
+                      _ptr(positions), _ptr(cos_sin_cache),
+                      0 if cos_sin_cache is None else cos_sin_cache.shape[0])
+    _check(lib().mla_norm_rope_grouped(
+        _ptr(kv_c), kv_c.stride(0), kv_c.stride(1), _ptr(k_pe), k_pe.stride(0), k_pe.stride(1),
+        T, L, R, P, ctypes.byref(nr) if nr is not None else None, _ptr(kv_c_out),
+        kv_c_out.stride(0), kv_c_out.stride(1), _ptr(k_pe_out), k_pe_out.stride(0),
+        k_pe_out.stride(1), _ptr(err_word), _stream(stream)))
 
 
 def mla_context_gather(kv_cache, cache_dtype, num_blocks, block_size, block_stride,

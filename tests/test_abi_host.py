@@ -250,6 +250,55 @@ def test_paged_calls_that_pass_validation_need_a_gpu(L):
     assert gather_scaled(L) == ops.MLA_ERR_CUDA
 
 
+def norm_rope(L, nr=None, **kw):
+    a = dict(kvc=A, kts=5 * 576, kls=576, kpe=A + 1024, pts=5 * 576, pls=576, T=4096, Ly=5,
+             R=512, P=64, oc=A + (1 << 30), octs=512, ocls=4096 * 512, op=A + (2 << 30),
+             opts=64, opls=4096 * 64, err=None)
+    a.update(kw)
+    return L.mla_norm_rope_grouped(a["kvc"], a["kts"], a["kls"], a["kpe"], a["pts"], a["pls"],
+                                   a["T"], a["Ly"], a["R"], a["P"],
+                                   ctypes.byref(nr) if nr is not None else None, a["oc"],
+                                   a["octs"], a["ocls"], a["op"], a["opts"], a["opls"], a["err"],
+                                   None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(T=-1), ops.MLA_ERR_INVALID_ARG),
+    (dict(Ly=0), ops.MLA_ERR_INVALID_ARG),
+    (dict(R=256), ops.MLA_ERR_UNSUPPORTED),
+    (dict(P=32), ops.MLA_ERR_UNSUPPORTED),
+    (dict(kvc=A + 2), ops.MLA_ERR_MISALIGNED),
+    (dict(kls=580), ops.MLA_ERR_MISALIGNED),
+    (dict(kpe=A + 8), ops.MLA_ERR_MISALIGNED),
+    (dict(oc=A + 4), ops.MLA_ERR_MISALIGNED),
+    (dict(octs=500), ops.MLA_ERR_MISALIGNED),
+    (dict(op=A + 2), ops.MLA_ERR_MISALIGNED),
+    (dict(opls=4), ops.MLA_ERR_MISALIGNED),
+    (dict(err=A + 2), ops.MLA_ERR_MISALIGNED),
+    (dict(T=1 << 30, Ly=8), ops.MLA_ERR_UNSUPPORTED),
+    (dict(kvc=None), ops.MLA_ERR_INVALID_ARG),
+    (dict(op=None), ops.MLA_ERR_INVALID_ARG),
+])
+def test_norm_rope_argument_checks(L, kw, status):
+    assert norm_rope(L, **kw) == status
+
+
+def test_norm_rope_description_checks(L):
+    bad_gamma = ops.NormRope(A + 2, 512, 1e-6, None, None, 0)
+    assert norm_rope(L, bad_gamma) == ops.MLA_ERR_MISALIGNED
+    bad_eps = ops.NormRope(A, 512, -1.0, None, None, 0)
+    assert norm_rope(L, bad_eps) == ops.MLA_ERR_INVALID_ARG
+    no_table = ops.NormRope(None, 0, 0.0, A, None, 32768)
+    assert norm_rope(L, no_table) == ops.MLA_ERR_INVALID_ARG
+    bad_pos = ops.NormRope(None, 0, 0.0, A + 4, A, 32768)
+    assert norm_rope(L, bad_pos) == ops.MLA_ERR_MISALIGNED
+    assert norm_rope(L, T=0, kvc=None, kpe=None, oc=None, op=None) == ops.MLA_OK
+    if not torch.cuda.is_available():
+        assert norm_rope(L) == ops.MLA_ERR_CUDA  # valid; the launch needs a GPU
+        ok = ops.NormRope(A, 512, 1e-6, A + 64, A + 128, 32768)
+        assert norm_rope(L, ok) == ops.MLA_ERR_CUDA
+
+
 def pack(L, **kw):
     a = dict(kn=A, kts=4160, khs=256, v=A + 256, vts=4160, vhs=256, kpe=A + 1024, kpets=576,
              kdt=1, T=8192, H=16, N=128, R=64, V=128, key=A + (1 << 30), vout=A + (2 << 30), odt=1,

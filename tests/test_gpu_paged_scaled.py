@@ -100,8 +100,10 @@ def test_scaled_gather_many_sequences_and_bad_blocks(orc):
     rng = np.random.default_rng(0)
     S = 37
     table = rng.integers(0, 128, size=(S, 8)).astype(np.int32)
-    table[5, 1], table[9, 0] = 128, -3
-    cu = np.concatenate([[0], np.cumsum(rng.integers(0, 200, size=S))]).astype(np.int32)
+    table[5, :], table[9, 0] = 128, -3  # every block id of sequence 5 out of range
+    lens = rng.integers(0, 200, size=S)
+    lens[5] = max(lens[5], 1)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
     starts = rng.integers(0, 300, size=S).astype(np.int32)
     T = int(cu[-1]) + 5
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -135,7 +137,8 @@ class PagedCase:
             self.starts = np.array([37], np.int32)
         else:
             self.table, self.cu, self.starts = seqs
-        self.kvb = W.pack_workload(T, T, num_blocks=8, num_heads=H, seed=seed + 1).kv_b_proj[0] \
+        self.kvb = W.pack_workload(T, T, num_blocks=(T + 63) // 64, num_heads=H,
+                                   seed=seed + 1).kv_b_proj[0] \
             if T > 0 else np.zeros((0, H * 256 + 64), np.uint16)
         self.cache_t = dev_cache(self.pw)
 
