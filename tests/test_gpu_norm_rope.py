@@ -50,8 +50,10 @@ def gpu_norm_rope(wl, kv, cos_sin, *, norm=True, rope=True, positions=None, err=
     k_pe [L,T,64]) as uint16 and whether the guard bands held."""
     T, L = wl.num_tokens, wl.num_layers
     kv_t = D.dev_bf16(kv)
-    oc = D.Guarded(L * T * 512 * 2, fill=0x11)
-    op = D.Guarded(L * T * 64 * 2, fill=0x22)
+    oc = D.Guarded(L * T * 512 * 2)
+    op = D.Guarded(L * T * 64 * 2)
+    oc.t.fill_(0x11)  # payloads only: the guard bands keep their canary
+    op.t.fill_(0x22)
     oc_v = oc.t.view(torch.bfloat16).view(L, T, 512)
     op_v = op.t.view(torch.bfloat16).view(L, T, 64)
     pos = positions if positions is not None else wl.positions
