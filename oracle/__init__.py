@@ -22,7 +22,8 @@ Passages followed (page title, section):
     fused_mla_kv_concat_quant_fp8): ``context_gather``, ``cast_rows``,
     ``concat_key``, ``context_kv_pack``.
   * OCP 8-bit Floating Point Specification (OFP8) rev. 1.0: the e4m3fn and
-    e5m2 encodings behind ``fp8_from_f32`` / ``fp8_to_f64``.
+    e5m2 encodings behind ``fp8_from_f32`` / ``fp8_to_f64``; IEEE 754 binary16
+    behind ``f16_from_f64`` / ``f16_to_f64`` (the pack's fp16 inputs).
 """
 from __future__ import annotations
 
@@ -33,7 +34,7 @@ import threading
 
 import numpy as np
 
-BF16, FP8_E4M3, FP8_E5M2 = 0, 1, 2
+BF16, FP8_E4M3, FP8_E5M2, F16 = 0, 1, 2, 3
 ERR_SLOT_OOB, ERR_BLOCK_OOB, ERR_POS_OOB = 1, 2, 4
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -76,6 +77,9 @@ def lib() -> ctypes.CDLL:
                 "orc_fp8_from_f32": (ctypes.c_uint8, [f32, ctypes.c_int]),
                 "orc_fp8_to_f64": (f64, [ctypes.c_uint8, ctypes.c_int]),
                 "orc_bf16_from_fp8": (ctypes.c_uint16, [ctypes.c_uint8, ctypes.c_int]),
+                "orc_f16_from_f64": (ctypes.c_uint16, [f64]),
+                "orc_f16_to_f64": (f64, [ctypes.c_uint16]),
+                "orc_f16_from_fp8": (ctypes.c_uint16, [ctypes.c_uint8, ctypes.c_int]),
                 "orc_fp8_encode_f32_array": (None, [vp, i64, ctypes.c_int, vp]),
                 "orc_fp8_decode_array": (None, [vp, i64, ctypes.c_int, vp]),
                 "orc_bf16_from_f64_array": (None, [vp, i64, vp]),
@@ -93,7 +97,7 @@ def lib() -> ctypes.CDLL:
                 "orc_cast_rows": (None, [vp, i32, i64, i64, i64, vp, i32, i64]),
                 "orc_concat_key": (None, [vp, i64, i64, vp, i64, i32, i32, i32, i32, vp]),
                 "orc_context_kv_pack": (None, [vp, i64, i64, vp, i64, i64, vp, i64, i32, i32,
-                                              i32, i32, i32, i32, vp, vp, i32, f32]),
+                                              i32, i32, i32, i32, vp, vp, i32, f32, i32]),
                 "orc_norm_rope_grouped": (u32, [vp, i64, i64, vp, i64, i64, i32, i32, i32, i32,
                                                 vp, i64, f32, vp, vp, i64, vp, i64, i64, vp, i64,
                                                 i64]),
@@ -102,7 +106,7 @@ def lib() -> ctypes.CDLL:
                                                     vp, i32, i32, vp, i64, f32]),
                 "orc_context_kv_pack_paged": (u32, [vp, i64, i64, vp, i64, i64, vp, i32, i64, i32,
                                                     i64, i64, i32, vp, i64, vp, vp, i32, i32, i32,
-                                                    i32, i32, i32, vp, vp, i32, f32]),
+                                                    i32, i32, i32, vp, vp, i32, f32, i32]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -137,6 +141,18 @@ def fp8_to_f64(c: int, fmt: int) -> float:
 
 def bf16_from_fp8(c: int, fmt: int) -> int:
     return lib().orc_bf16_from_fp8(int(c), fmt)
+
+
+def f16_from_f64(x: float) -> int:
+    return lib().orc_f16_from_f64(float(x))
+
+
+def f16_to_f64(h: int) -> float:
+    return lib().orc_f16_to_f64(int(h))
+
+
+def f16_from_fp8(c: int, fmt: int) -> int:
+    return lib().orc_f16_from_fp8(int(c), fmt)
 
 
 # ----------------------------------------------------------------- array codecs
@@ -257,7 +273,7 @@ def context_gather(cache, cache_dtype, num_blocks, block_size, block_stride, ent
 
 def cast_rows(src, src_dtype, dst_dtype):
     rows, cols = src.shape
-    out = np.empty((rows, cols), np.uint16 if dst_dtype == BF16 else np.uint8)
+    out = np.empty((rows, cols), np.uint16 if dst_dtype in (BF16, F16) else np.uint8)
     lib().orc_cast_rows(_p(np.ascontiguousarray(src)), src_dtype, cols, rows, cols, _p(out),
                         dst_dtype, cols)
     return out
@@ -275,19 +291,19 @@ def concat_key(k_nope_rows, kn_token_stride, kn_head_stride, k_pe_rows, kpe_toke
 
 def context_kv_pack(k_nope_buf, kn_token_stride, kn_head_stride, v_buf, v_token_stride,
                     v_head_stride, k_pe_buf, kpe_token_stride, kpe_dtype, T, H, nope, rope,
-                    v_dim, out_dtype, out_scale=1.0, with_v=True):
+                    v_dim, out_dtype, out_scale=1.0, with_v=True, in_dtype=BF16):
     """Fused pack over flat buffers addressed by element strides.
 
     ``k_nope_buf`` / ``v_buf`` are flat uint16 arrays positioned at the first
     element (numpy views are fine: their data pointer is used).  Returns
     (key [T, H, nope+rope], v [T, H, v_dim] or None) in the output format."""
-    odt = np.uint16 if out_dtype == BF16 else np.uint8
+    odt = np.uint16 if out_dtype in (BF16, F16) else np.uint8
     key = np.empty((T, H, nope + rope), odt)
     vout = np.empty((T, H, v_dim), odt) if with_v else None
     lib().orc_context_kv_pack(_p(k_nope_buf), kn_token_stride, kn_head_stride, _p(v_buf),
                               v_token_stride, v_head_stride, _p(k_pe_buf), kpe_token_stride,
                               kpe_dtype, T, H, nope, rope, v_dim, _p(key), _p(vout),
-                              out_dtype, float(out_scale))
+                              out_dtype, float(out_scale), in_dtype)
     return key, vout
 
 
@@ -311,10 +327,10 @@ def context_kv_pack_paged(k_nope_buf, kn_token_stride, kn_head_stride, v_buf, v_
                           v_head_stride, cache, cache_dtype, num_blocks, block_size, block_stride,
                           entry_stride, rope_offset, block_table, cu_chunk_lens, chunk_starts, T,
                           H, nope, rope, v_dim, out_dtype, out_scale=1.0, with_v=True,
-                          key_init=None, v_init=None):
+                          key_init=None, v_init=None, in_dtype=BF16):
     """Pack with k_pe from the paged cache.  Returns (key, v, error bits); key
     starts as ``key_init`` (rope slices of tokens without a row stay as given)."""
-    odt = np.uint16 if out_dtype == BF16 else np.uint8
+    odt = np.uint16 if out_dtype in (BF16, F16) else np.uint8
     key = (np.array(key_init, dtype=odt, copy=True) if key_init is not None
            else np.zeros((T, H, nope + rope), odt))
     vout = (np.array(v_init, dtype=odt, copy=True) if v_init is not None
@@ -324,7 +340,7 @@ def context_kv_pack_paged(k_nope_buf, kn_token_stride, kn_head_stride, v_buf, v_
         _p(cache), cache_dtype, num_blocks, block_size, block_stride, entry_stride, rope_offset,
         _p(block_table), block_table.shape[1], _p(cu_chunk_lens), _p(chunk_starts),
         chunk_starts.shape[0], T, H, nope, rope, v_dim, _p(key), _p(vout), out_dtype,
-        float(out_scale))
+        float(out_scale), in_dtype)
     return key, vout, err
 
 

@@ -65,6 +65,35 @@ double orc_bf16_to_f64(uint16_t b) {
   return (double)f;
 }
 
+/* ---- IEEE binary16: 1 sign, 5 exponent (bias 15), 10 mantissa bits ------ */
+
+/* Round to nearest even with 11 significant bits, smallest normal 2^-14
+ * (subnormal quantum 2^-24); a rounded magnitude above the largest finite
+ * value 65504 is an infinity (IEEE overflow under round to nearest). */
+uint16_t orc_f16_from_f64(double x) {
+  uint16_t sign = signbit(x) ? 0x8000u : 0u;
+  if (isnan(x)) return (uint16_t)(sign | 0x7E00u);
+  double r = round_to_precision(x, 11, -14);
+  double a = fabs(r);
+  if (a > 65504.0) return (uint16_t)(sign | 0x7C00u);
+  if (a == 0.0) return sign;
+  int e;
+  (void)frexp(a, &e); /* a = m * 2^e, 0.5 <= m < 1: unbiased exponent e - 1 */
+  if (e - 1 < -14) /* subnormal: a = n * 2^-24 exactly */
+    return (uint16_t)(sign | (uint16_t)ldexp(a, 24));
+  uint16_t exp_field = (uint16_t)(e - 1 + 15);
+  uint16_t mant = (uint16_t)(ldexp(a, 10 - (e - 1)) - 1024.0); /* a / 2^(e-1) * 2^10 - 2^10 */
+  return (uint16_t)(sign | (exp_field << 10) | mant);
+}
+
+double orc_f16_to_f64(uint16_t h) {
+  double sign = (h & 0x8000u) ? -1.0 : 1.0;
+  int ef = (h >> 10) & 0x1F, m = h & 0x3FF;
+  if (ef == 0x1F) return m ? NAN : sign * INFINITY;
+  if (ef == 0) return sign * ldexp((double)m, -24);
+  return sign * ldexp(1024.0 + m, ef - 15 - 10);
+}
+
 /* ---- OCP OFP8 formats --------------------------------------------------- */
 
 typedef struct {
@@ -154,6 +183,14 @@ uint16_t orc_bf16_from_fp8(uint8_t c, int fmt) {
   if (isnan(v)) return (uint16_t)(sign | 0x7FC0u);
   if (isinf(v)) return (uint16_t)(sign | 0x7F80u);
   return orc_bf16_from_f64(v);
+}
+
+/* fp8 -> fp16, exact (every e4m3 and e5m2 value is an fp16 value); a NaN code
+ * gives the quiet NaN with the code's sign. */
+uint16_t orc_f16_from_fp8(uint8_t c, int fmt) {
+  double v = orc_fp8_to_f64(c, fmt);
+  if (isnan(v)) return (uint16_t)(((c & 0x80u) ? 0x8000u : 0u) | 0x7E00u);
+  return orc_f16_from_f64(v);
 }
 
 void orc_fp8_encode_f32_array(const float* x, int64_t n, int fmt, uint8_t* out) {
@@ -399,15 +436,20 @@ uint32_t orc_norm_rope_grouped(const uint16_t* kv_c, int64_t kvc_token_stride,
 /* ======================================================================== */
 
 /* Copy one element, widening fp8 -> bf16 exactly when the formats differ. */
+static int is16(int32_t d) { return d == ORC_BF16 || d == ORC_F16; }
+
+/* Copy one element, widening fp8 -> bf16 / fp16 exactly when the formats differ. */
 static void copy_elt(const void* src, int32_t sd, int64_t si, void* dst, int32_t dd,
                      int64_t di) {
   if (sd == dd) {
-    if (sd == ORC_BF16)
+    if (is16(sd))
       ((uint16_t*)dst)[di] = ((const uint16_t*)src)[si];
     else
       ((uint8_t*)dst)[di] = ((const uint8_t*)src)[si];
-  } else { /* fp8 -> bf16 */
+  } else if (dd == ORC_BF16) {
     ((uint16_t*)dst)[di] = orc_bf16_from_fp8(((const uint8_t*)src)[si], sd);
+  } else { /* fp8 -> fp16 */
+    ((uint16_t*)dst)[di] = orc_f16_from_fp8(((const uint8_t*)src)[si], sd);
   }
 }
 
@@ -485,12 +527,14 @@ void orc_concat_key(const uint16_t* k_nope, int64_t kn_token_stride, int64_t kn_
 
 /* One bf16 element into the output format: the bits themselves for bf16, else
  * fp8(float(e) / out_scale). */
-static void put_from_bf16(uint16_t e, void* out, int32_t out_dtype, int64_t i,
-                          float out_scale) {
-  if (out_dtype == ORC_BF16) {
+/* One 16-bit input element (bf16 or fp16, in_dtype) to the output: its bits
+ * for a 16-bit output (of the same type), else fp8(float(e) / out_scale). */
+static void put_from_16(uint16_t e, int32_t in_dtype, void* out, int32_t out_dtype, int64_t i,
+                        float out_scale) {
+  if (is16(out_dtype)) {
     ((uint16_t*)out)[i] = e;
   } else {
-    float v = (float)orc_bf16_to_f64(e);
+    float v = (float)(in_dtype == ORC_F16 ? orc_f16_to_f64(e) : orc_bf16_to_f64(e));
     ((uint8_t*)out)[i] = orc_fp8_from_f32(v / out_scale, out_dtype);
   }
 }
@@ -501,32 +545,34 @@ static void put_from_bf16(uint16_t e, void* out, int32_t out_dtype, int64_t i,
  *   key[t,h,i]        = conv(k_nope[t,h,i])            i < nope
  *   key[t,h,nope + j] = k_pe term                      j < rope
  *   V[t,h,i]          = conv(v[t,h,i])                 i < v_dim
- * where conv is the identity for bf16 output and fp8(float(e)/out_scale) for fp8
- * output.  The k_pe term: a bf16 k_pe goes through conv; an fp8 k_pe is copied
- * byte for byte into an fp8 key of the same format (the KPE_FP8 branch: no
- * rescale) and widened exactly, with no scale, into a bf16 key.
+ * where conv is the identity for a 16-bit output and fp8(float(e)/out_scale) for
+ * fp8 output.  k_nope and v are 16-bit of in_dtype (bf16 or fp16; "PR #51772"
+ * Review: bf16 and fp16 inputs), and a 16-bit output has the input's type.
+ * The k_pe term: a 16-bit k_pe (of in_dtype) goes through conv; an fp8 k_pe is
+ * copied byte for byte into an fp8 key of the same format (the KPE_FP8 branch:
+ * no rescale) and widened exactly, with no scale, into a 16-bit key.
  */
 void orc_context_kv_pack(const uint16_t* k_nope, int64_t kn_token_stride,
                          int64_t kn_head_stride, const uint16_t* v, int64_t v_token_stride,
                          int64_t v_head_stride, const void* k_pe, int64_t kpe_token_stride,
                          int32_t kpe_dtype, int32_t num_tokens, int32_t num_heads,
                          int32_t nope_dim, int32_t rope_dim, int32_t v_dim, void* key_out,
-                         void* v_out, int32_t out_dtype, float out_scale) {
+                         void* v_out, int32_t out_dtype, float out_scale, int32_t in_dtype) {
   int64_t kd = (int64_t)nope_dim + rope_dim;
   for (int32_t t = 0; t < num_tokens; ++t) {
     for (int32_t h = 0; h < num_heads; ++h) {
       int64_t krow = ((int64_t)t * num_heads + h) * kd;
       for (int32_t i = 0; i < nope_dim; ++i) {
         uint16_t e = k_nope[(int64_t)t * kn_token_stride + (int64_t)h * kn_head_stride + i];
-        put_from_bf16(e, key_out, out_dtype, krow + i, out_scale);
+        put_from_16(e, in_dtype, key_out, out_dtype, krow + i, out_scale);
       }
       for (int32_t j = 0; j < rope_dim; ++j) {
         int64_t si = (int64_t)t * kpe_token_stride + j;
         int64_t di = krow + nope_dim + j;
-        if (kpe_dtype == ORC_BF16) {
-          put_from_bf16(((const uint16_t*)k_pe)[si], key_out, out_dtype, di, out_scale);
-        } else if (out_dtype == ORC_BF16) {
-          ((uint16_t*)key_out)[di] = orc_bf16_from_fp8(((const uint8_t*)k_pe)[si], kpe_dtype);
+        if (is16(kpe_dtype)) {
+          put_from_16(((const uint16_t*)k_pe)[si], in_dtype, key_out, out_dtype, di, out_scale);
+        } else if (is16(out_dtype)) {
+          copy_elt(k_pe, kpe_dtype, si, key_out, out_dtype, di);
         } else {
           ((uint8_t*)key_out)[di] = ((const uint8_t*)k_pe)[si];
         }
@@ -535,7 +581,7 @@ void orc_context_kv_pack(const uint16_t* k_nope, int64_t kn_token_stride,
         int64_t vrow = ((int64_t)t * num_heads + h) * v_dim;
         for (int32_t i = 0; i < v_dim; ++i) {
           uint16_t e = v[(int64_t)t * v_token_stride + (int64_t)h * v_head_stride + i];
-          put_from_bf16(e, v_out, out_dtype, vrow + i, out_scale);
+          put_from_16(e, in_dtype, v_out, out_dtype, vrow + i, out_scale);
         }
       }
     }
@@ -622,9 +668,9 @@ uint32_t orc_context_kv_pack_paged(
     int32_t rope_offset, const int32_t* block_table, int64_t block_table_stride,
     const int32_t* cu_chunk_lens, const int32_t* chunk_starts, int32_t num_seqs,
     int32_t num_tokens, int32_t num_heads, int32_t nope_dim, int32_t rope_dim, int32_t v_dim,
-    void* key_out, void* v_out, int32_t out_dtype, float out_scale) {
+    void* key_out, void* v_out, int32_t out_dtype, float out_scale, int32_t in_dtype) {
   uint32_t err = 0;
-  const size_t ce = cache_dtype == ORC_BF16 ? 2u : 1u, oe = out_dtype == ORC_BF16 ? 2u : 1u;
+  const size_t ce = is16(cache_dtype) ? 2u : 1u, oe = is16(out_dtype) ? 2u : 1u;
   const int64_t kd = (int64_t)nope_dim + rope_dim;
   uint8_t* key_tmp = (uint8_t*)malloc((size_t)num_heads * kd * oe);
   uint8_t* v_tmp = (uint8_t*)malloc((size_t)num_heads * v_dim * oe + 1);
@@ -658,7 +704,7 @@ uint32_t orc_context_kv_pack_paged(
                         v ? v + (int64_t)t * v_token_stride : NULL, v_token_stride, v_head_stride,
                         row ? (const void*)row : (const void*)zero_pe, 0, cache_dtype, 1,
                         num_heads, nope_dim, rope_dim, v_dim, key_tmp, v_out ? v_tmp : NULL,
-                        out_dtype, out_scale);
+                        out_dtype, out_scale, in_dtype);
     uint8_t* kdst = (uint8_t*)key_out + (int64_t)t * num_heads * kd * oe;
     for (int32_t h = 0; h < num_heads; ++h) {
       memcpy(kdst + (int64_t)h * kd * oe, key_tmp + (int64_t)h * kd * oe, (size_t)nope_dim * oe);

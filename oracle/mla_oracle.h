@@ -21,6 +21,8 @@
  *   [OFP8] OCP 8-bit Floating Point Specification (OFP8), rev. 1.0: the E4M3
  *        (no infinities, single NaN mantissa pattern) and E5M2 (IEEE-like)
  *        encodings.
+ *   [IEEE] IEEE 754-2008 binary16 (fp16): 1 sign, 5 exponent (bias 15), 10
+ *        mantissa bits, subnormals, infinities and NaNs.
  *
  * All floating point arithmetic that produces a rounded result is done in
  * double precision and rounded ONCE to the target format with round-to-nearest,
@@ -44,7 +46,7 @@ extern "C" {
 
 /* Cache / tensor element formats.  Numbering matches the product's public
  * enum by convention only; the oracle defines its own. */
-enum { ORC_BF16 = 0, ORC_FP8_E4M3 = 1, ORC_FP8_E5M2 = 2 };
+enum { ORC_BF16 = 0, ORC_FP8_E4M3 = 1, ORC_FP8_E5M2 = 2, ORC_F16 = 3 };
 
 /* Error bits returned by the row-skipping functions. */
 enum { ORC_ERR_SLOT_OOB = 1u, ORC_ERR_BLOCK_OOB = 2u, ORC_ERR_POS_OOB = 4u };
@@ -56,6 +58,9 @@ double orc_bf16_to_f64(uint16_t b);
 uint8_t orc_fp8_from_f32(float x, int fmt);
 double orc_fp8_to_f64(uint8_t c, int fmt);
 uint16_t orc_bf16_from_fp8(uint8_t c, int fmt);
+uint16_t orc_f16_from_f64(double x);
+double orc_f16_to_f64(uint16_t h);
+uint16_t orc_f16_from_fp8(uint8_t c, int fmt);
 
 /* ---- array forms of the codecs (for exhaustive tests) ------------------- */
 void orc_fp8_encode_f32_array(const float* x, int64_t n, int fmt, uint8_t* out);
@@ -133,7 +138,7 @@ void orc_context_kv_pack(const uint16_t* k_nope, int64_t kn_token_stride,
                          int64_t v_head_stride, const void* k_pe, int64_t kpe_token_stride,
                          int32_t kpe_dtype, int32_t num_tokens, int32_t num_heads,
                          int32_t nope_dim, int32_t rope_dim, int32_t v_dim, void* key_out,
-                         void* v_out, int32_t out_dtype, float out_scale);
+                         void* v_out, int32_t out_dtype, float out_scale, int32_t in_dtype);
 
 uint32_t orc_context_kv_pack_paged(
     const uint16_t* k_nope, int64_t kn_token_stride, int64_t kn_head_stride, const uint16_t* v,
@@ -142,7 +147,7 @@ uint32_t orc_context_kv_pack_paged(
     int32_t rope_offset, const int32_t* block_table, int64_t block_table_stride,
     const int32_t* cu_chunk_lens, const int32_t* chunk_starts, int32_t num_seqs,
     int32_t num_tokens, int32_t num_heads, int32_t nope_dim, int32_t rope_dim, int32_t v_dim,
-    void* key_out, void* v_out, int32_t out_dtype, float out_scale);
+    void* key_out, void* v_out, int32_t out_dtype, float out_scale, int32_t in_dtype);
 
 #ifdef __cplusplus
 }
