@@ -55,11 +55,15 @@ struct CUstream_st;
 /* Same type as cudaStream_t. */
 typedef struct CUstream_st* mla_stream_t;
 
-/* Element formats of caches and outputs.  The vLLM cache-dtype strings map as
- * "auto"/"bfloat16" -> MLA_BF16, "fp8"/"fp8_e4m3" -> MLA_FP8_E4M3,
+/* Element formats of caches, inputs and outputs.  The vLLM cache-dtype strings
+ * map as "auto"/"bfloat16" -> MLA_BF16, "fp8"/"fp8_e4m3" -> MLA_FP8_E4M3,
  * "fp8_e5m2" -> MLA_FP8_E5M2 ("PR #55356", Source snippets: the host dtype
- * whitelist and the three template instances). */
-typedef enum { MLA_BF16 = 0, MLA_FP8_E4M3 = 1, MLA_FP8_E5M2 = 2 } mla_dtype_t;
+ * whitelist and the three template instances).  MLA_FP16 (IEEE binary16) is
+ * an input / output format of the chunked-context path only: an fp16
+ * kv_b_proj output into the pack, and the gather's widening for an fp16
+ * kv_b_proj input ("PR #51772", Review: bf16 and fp16 inputs); the grouped
+ * insert takes bf16 input and bf16 / fp8 caches only. */
+typedef enum { MLA_BF16 = 0, MLA_FP8_E4M3 = 1, MLA_FP8_E5M2 = 2, MLA_FP16 = 3 } mla_dtype_t;
 
 typedef enum {
   MLA_OK = 0,
@@ -183,7 +187,7 @@ mla_status_t mla_cache_insert_grouped(
 
 /*
  * Gather latent rows of context chunks from a paged cache, with the optional
- * exact widening fp8 -> bf16 ("PR #51772", Implementation item 2:
+ * exact widening fp8 -> bf16 or fp16 ("PR #51772", Implementation item 2:
  * _gather_context_latent, then the conditional .to() of item 5; no scale is
  * applied, a plain fp8 gather returns fp8).
  *
@@ -195,7 +199,8 @@ mla_status_t mla_cache_insert_grouped(
  *   out[i * out_row_stride + e] = cache[blk * block_stride +
  *                                       (p % block_size) * entry_stride + e],
  * for e < entry_dim, copied raw (out_dtype == cache_dtype) or widened exactly
- * to bf16 (cache fp8, out_dtype MLA_BF16).
+ * (cache fp8, out_dtype MLA_BF16 or MLA_FP16: the kv_b_proj input's type; a
+ * NaN code gives that format's quiet NaN with the code's sign).
  *
  *   block_table         int32 device [num_seqs, block_table_stride]; the row
  *                       width is block_table_stride.  A table index outside
@@ -250,29 +255,33 @@ mla_status_t mla_context_gather_scaled(
  *   key_out[t, h, i]          = conv(k_nope[t, h, i])        i < nope_dim
  *   key_out[t, h, nope_dim+j] = kpe(k_pe[t, j])               j < rope_dim
  *   v_out[t, h, i]            = conv(v[t, h, i])              i < v_dim
- * with conv = identity for MLA_BF16 output and
+ * with conv = identity for a 16-bit output (of the input's type) and
  * fp8(float(e) / *out_scale) (round to nearest even, saturating) for fp8
- * output; kpe = conv for a bf16 k_pe, the raw byte for an fp8 k_pe into an fp8
- * key of the same format (no rescale), and the exact unscaled widening for an
- * fp8 k_pe into a bf16 key.
+ * output; kpe = conv for a 16-bit k_pe, the raw byte for an fp8 k_pe into an
+ * fp8 key of the same format (no rescale), and the exact unscaled widening for
+ * an fp8 k_pe into a 16-bit key.
  *
- *   k_nope, v           bf16, element (t, h, i) at t * token_stride +
+ *   k_nope, v           element (t, h, i) at t * token_stride +
  *                       h * head_stride + i (e.g. the two halves of a
  *                       [T, H, nope + v] kv_b_proj output, row stride 4160).
+ *   in_dtype            their type: MLA_BF16 or MLA_FP16 ("PR #51772",
+ *                       Review: bf16 and fp16 inputs).
  *   k_pe                [T, rope_dim] with row stride kpe_token_stride, of type
- *                       kpe_dtype (bf16 or the cache's fp8).
+ *                       kpe_dtype (in_dtype, or the cache's fp8).
  *   nope_dim, rope_dim, v_dim  must be 128, 64, 128 (else UNSUPPORTED).
+ *   out_dtype           in_dtype, MLA_FP8_E4M3 or MLA_FP8_E5M2.
  *   key_out             contiguous [T, H, nope_dim + rope_dim] of out_dtype.
  *   v_out               contiguous [T, H, v_dim] of out_dtype, or NULL = no V.
  *   out_scale           device fp32 scalar for fp8 output (NULL = 1.0); must be
- *                       NULL for bf16 output.
+ *                       NULL for a 16-bit output.
  *   err_word            NULL, or a device uint32 for MLA_ERRBIT_* (this pack
  *                       reads no indices, so no condition sets a bit; the paged
  *                       pack below sets MLA_ERRBIT_BLOCK_OOB).
  */
 mla_status_t mla_context_kv_pack(
     const void* k_nope, int64_t kn_token_stride, int64_t kn_head_stride, const void* v,
-    int64_t v_token_stride, int64_t v_head_stride, const void* k_pe, int64_t kpe_token_stride,
+    int64_t v_token_stride, int64_t v_head_stride, mla_dtype_t in_dtype, const void* k_pe,
+    int64_t kpe_token_stride,
     mla_dtype_t kpe_dtype, int32_t num_tokens, int32_t num_heads, int32_t nope_dim,
     int32_t rope_dim, int32_t v_dim, void* key_out, void* v_out, mla_dtype_t out_dtype,
     const float* out_scale, uint32_t* err_word, mla_stream_t stream);
@@ -288,8 +297,8 @@ mla_status_t mla_context_kv_pack(
  * block-table rules), of the cache's element type:
  *   key_out[t, h, nope_dim + j] = kpe(row_t[rope_offset + j])
  * with kpe as in mla_context_kv_pack for kpe_dtype = cache_dtype (raw bytes for
- * an fp8 cache into an fp8 key of its format, the exact widening into a bf16
- * key, the output conversion for a bf16 cache).  k_nope and V are packed as in
+ * an fp8 cache into an fp8 key of its format, the exact widening into a 16-bit
+ * key, the output conversion for a 16-bit cache of in_dtype's type).  k_nope and V are packed as in
  * mla_context_kv_pack for every token.  A token whose row is not found keeps
  * the rope slice of its key untouched: silently when no sequence owns it, and
  * with MLA_ERRBIT_BLOCK_OOB when its block index or block id is out of range.
@@ -305,7 +314,8 @@ mla_status_t mla_context_kv_pack(
  */
 mla_status_t mla_context_kv_pack_paged(
     const void* k_nope, int64_t kn_token_stride, int64_t kn_head_stride, const void* v,
-    int64_t v_token_stride, int64_t v_head_stride, const void* kv_cache, mla_dtype_t cache_dtype,
+    int64_t v_token_stride, int64_t v_head_stride, mla_dtype_t in_dtype, const void* kv_cache,
+    mla_dtype_t cache_dtype,
     int64_t num_blocks, int32_t block_size, int64_t block_stride, int64_t entry_stride,
     int64_t rope_offset, const int32_t* block_table, int64_t block_table_stride,
     const int32_t* cu_chunk_lens, const int32_t* chunk_starts, int32_t num_seqs,

@@ -38,8 +38,11 @@ mla_status_t fail(mla_status_t st, const char* fmt, ...) {
 
 inline bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool m16(int64_t bytes) { return (bytes & 15) == 0; }
-inline bool valid_dtype(int d) { return d == MLA_BF16 || d == MLA_FP8_E4M3 || d == MLA_FP8_E5M2; }
-inline int elt_size(int d) { return d == MLA_BF16 ? 2 : 1; }
+inline bool valid_dtype(int d) {
+  return d == MLA_BF16 || d == MLA_FP8_E4M3 || d == MLA_FP8_E5M2 || d == MLA_FP16;
+}
+inline bool is16(int d) { return d == MLA_BF16 || d == MLA_FP16; }
+inline int elt_size(int d) { return is16(d) ? 2 : 1; }
 inline int log2_exact(int64_t v) {
   if (v <= 0 || (v & (v - 1))) return -1;
   int s = 0;
@@ -236,7 +239,7 @@ mla_status_t mla_cache_insert_grouped(
   if (num_tokens < 0) return fail(MLA_ERR_INVALID_ARG, "num_tokens must be >= 0");
   if (num_layers <= 0) return fail(MLA_ERR_INVALID_ARG, "num_layers must be >= 1");
   if (num_layers > 128) return fail(MLA_ERR_UNSUPPORTED, "at most 128 layers per call are built");
-  if (!valid_dtype(cache_dtype))
+  if (cache_dtype != MLA_BF16 && cache_dtype != MLA_FP8_E4M3 && cache_dtype != MLA_FP8_E5M2)
     return fail(MLA_ERR_INVALID_ARG,
                 "cache_dtype must be MLA_BF16, MLA_FP8_E4M3 or MLA_FP8_E5M2; got %d",
                 (int)cache_dtype);
@@ -333,9 +336,10 @@ mla_status_t gather_impl(const void* kv_cache, mla_dtype_t cache_dtype, int64_t 
   if (num_tokens < 0) return fail(MLA_ERR_INVALID_ARG, "num_tokens must be >= 0");
   if (!valid_dtype(cache_dtype) || !valid_dtype(out_dtype))
     return fail(MLA_ERR_INVALID_ARG, "cache_dtype / out_dtype must be an mla_dtype_t value");
-  if (out_dtype != cache_dtype && !(cache_dtype != MLA_BF16 && out_dtype == MLA_BF16))
+  if (out_dtype != cache_dtype && !(!is16(cache_dtype) && is16(out_dtype)))
     return fail(MLA_ERR_UNSUPPORTED,
-                "out_dtype must equal cache_dtype (raw) or be MLA_BF16 from an fp8 cache");
+                "out_dtype must equal cache_dtype (raw) or be MLA_BF16 / MLA_FP16 from an fp8 "
+                "cache");
   const int ce = elt_size(cache_dtype), oe = elt_size(out_dtype);
   MLA_TRY(check_paged(kv_cache, num_blocks, block_size, block_stride, entry_stride, 0, entry_dim,
                       ce, block_table, block_table_stride, cu_chunk_lens, chunk_starts,
@@ -368,7 +372,7 @@ mla_status_t gather_impl(const void* kv_cache, mla_dtype_t cache_dtype, int64_t 
   a.dequant_scale = dequant_scale;
   a.err = err_word;
   const int mode = (out_dtype == cache_dtype) ? 0 : (int)cache_dtype;
-  return launched(mla::launch_gather(a, mode, cfg_for(stream)), what);
+  return launched(mla::launch_gather(a, mode, (int)out_dtype, cfg_for(stream)), what);
 }
 
 // The packs: k_pe given as rows (paged == nullptr) or read from the paged
@@ -387,24 +391,30 @@ struct PagedKpe {
 
 mla_status_t pack_impl(const void* k_nope, int64_t kn_token_stride, int64_t kn_head_stride,
                        const void* v, int64_t v_token_stride, int64_t v_head_stride,
-                       const void* k_pe, int64_t kpe_token_stride, mla_dtype_t kpe_dtype,
+                       mla_dtype_t in_dtype, const void* k_pe, int64_t kpe_token_stride, mla_dtype_t kpe_dtype,
                        const PagedKpe* paged, int32_t num_tokens, int32_t num_heads,
                        int32_t nope_dim, int32_t rope_dim, int32_t v_dim, void* key_out,
                        void* v_out, mla_dtype_t out_dtype, const float* out_scale,
                        uint32_t* err_word, mla_stream_t stream, const char* what) {
   if (num_tokens < 0) return fail(MLA_ERR_INVALID_ARG, "num_tokens must be >= 0");
   if (num_heads <= 0) return fail(MLA_ERR_INVALID_ARG, "num_heads must be >= 1");
-  if (!valid_dtype(out_dtype) || !valid_dtype(kpe_dtype))
-    return fail(MLA_ERR_INVALID_ARG, "out_dtype / %s must be an mla_dtype_t value",
+  if (!valid_dtype(out_dtype) || !valid_dtype(kpe_dtype) || !valid_dtype(in_dtype))
+    return fail(MLA_ERR_INVALID_ARG, "in_dtype / out_dtype / %s must be an mla_dtype_t value",
                 paged ? "cache_dtype" : "kpe_dtype");
+  if (!is16(in_dtype))
+    return fail(MLA_ERR_UNSUPPORTED, "k_nope and v must be MLA_BF16 or MLA_FP16 (in_dtype)");
   if (nope_dim != 128 || rope_dim != 64 || v_dim != 128)
     return fail(MLA_ERR_UNSUPPORTED, "only nope 128, rope 64, v 128 are built (got %d, %d, %d)",
                 nope_dim, rope_dim, v_dim);
-  if (out_dtype != MLA_BF16 && kpe_dtype != MLA_BF16 && kpe_dtype != out_dtype)
+  if (is16(out_dtype) && out_dtype != in_dtype)
+    return fail(MLA_ERR_UNSUPPORTED, "a 16-bit output has the input's type (in_dtype)");
+  if (is16(kpe_dtype) && kpe_dtype != in_dtype)
+    return fail(MLA_ERR_UNSUPPORTED, "a 16-bit k_pe must have k_nope's type (in_dtype)");
+  if (!is16(out_dtype) && !is16(kpe_dtype) && kpe_dtype != out_dtype)
     return fail(MLA_ERR_UNSUPPORTED,
                 "an fp8 k_pe is copied raw, so it must have the fp8 output's format");
-  if (out_dtype == MLA_BF16 && out_scale)
-    return fail(MLA_ERR_INVALID_ARG, "a bf16 pack does not use out_scale");
+  if (is16(out_dtype) && out_scale)
+    return fail(MLA_ERR_INVALID_ARG, "a 16-bit pack does not use out_scale");
   if (!a16(k_nope) || !m16(kn_token_stride * 2) || !m16(kn_head_stride * 2))
     return fail(MLA_ERR_MISALIGNED, "k_nope rows must start on 16-byte boundaries");
   if (v_out && (!a16(v) || !m16(v_token_stride * 2) || !m16(v_head_stride * 2)))
@@ -461,8 +471,8 @@ mla_status_t pack_impl(const void* k_nope, int64_t kn_token_stride, int64_t kn_h
                         paged->block_table_stride, paged->cu, paged->starts, paged->num_seqs);
     a.pe_off = paged->rope_offset * ke;
   }
-  return launched(mla::launch_pack(a, (int)out_dtype, (int)kpe_dtype, paged != nullptr,
-                                   cfg_for(stream)),
+  return launched(mla::launch_pack(a, (int)in_dtype, (int)out_dtype, (int)kpe_dtype,
+                                   paged != nullptr, cfg_for(stream)),
                   what);
 }
 
@@ -504,32 +514,32 @@ mla_status_t mla_context_gather_scaled(const void* kv_cache, mla_dtype_t cache_d
 
 mla_status_t mla_context_kv_pack(const void* k_nope, int64_t kn_token_stride,
                                  int64_t kn_head_stride, const void* v, int64_t v_token_stride,
-                                 int64_t v_head_stride, const void* k_pe,
+                                 int64_t v_head_stride, mla_dtype_t in_dtype, const void* k_pe,
                                  int64_t kpe_token_stride, mla_dtype_t kpe_dtype,
                                  int32_t num_tokens, int32_t num_heads, int32_t nope_dim,
                                  int32_t rope_dim, int32_t v_dim, void* key_out, void* v_out,
                                  mla_dtype_t out_dtype, const float* out_scale,
                                  uint32_t* err_word, mla_stream_t stream) {
   return pack_impl(k_nope, kn_token_stride, kn_head_stride, v, v_token_stride, v_head_stride,
-                   k_pe, kpe_token_stride, kpe_dtype, nullptr, num_tokens, num_heads, nope_dim,
+                   in_dtype, k_pe, kpe_token_stride, kpe_dtype, nullptr, num_tokens, num_heads, nope_dim,
                    rope_dim, v_dim, key_out, v_out, out_dtype, out_scale, err_word, stream,
                    "mla_context_kv_pack");
 }
 
 mla_status_t mla_context_kv_pack_paged(
     const void* k_nope, int64_t kn_token_stride, int64_t kn_head_stride, const void* v,
-    int64_t v_token_stride, int64_t v_head_stride, const void* kv_cache, mla_dtype_t cache_dtype,
-    int64_t num_blocks, int32_t block_size, int64_t block_stride, int64_t entry_stride,
-    int64_t rope_offset, const int32_t* block_table, int64_t block_table_stride,
-    const int32_t* cu_chunk_lens, const int32_t* chunk_starts, int32_t num_seqs,
-    int32_t num_tokens, int32_t num_heads, int32_t nope_dim, int32_t rope_dim, int32_t v_dim,
-    void* key_out, void* v_out, mla_dtype_t out_dtype, const float* out_scale,
+    int64_t v_token_stride, int64_t v_head_stride, mla_dtype_t in_dtype, const void* kv_cache,
+    mla_dtype_t cache_dtype, int64_t num_blocks, int32_t block_size, int64_t block_stride,
+    int64_t entry_stride, int64_t rope_offset, const int32_t* block_table,
+    int64_t block_table_stride, const int32_t* cu_chunk_lens, const int32_t* chunk_starts,
+    int32_t num_seqs, int32_t num_tokens, int32_t num_heads, int32_t nope_dim, int32_t rope_dim,
+    int32_t v_dim, void* key_out, void* v_out, mla_dtype_t out_dtype, const float* out_scale,
     uint32_t* err_word, mla_stream_t stream) {
   const PagedKpe pk{kv_cache,      num_blocks,   block_size,  block_stride,
                     entry_stride,  rope_offset,  block_table, block_table_stride,
                     cu_chunk_lens, chunk_starts, num_seqs};
   return pack_impl(k_nope, kn_token_stride, kn_head_stride, v, v_token_stride, v_head_stride,
-                   nullptr, 0, cache_dtype, &pk, num_tokens, num_heads, nope_dim, rope_dim,
+                   in_dtype, nullptr, 0, cache_dtype, &pk, num_tokens, num_heads, nope_dim, rope_dim,
                    v_dim, key_out, v_out, out_dtype, out_scale, err_word, stream,
                    "mla_context_kv_pack_paged");
 }

@@ -2,7 +2,7 @@
 //
 // What it computes: output row i of sequence s is the cache row of context
 // position chunk_starts[s] + (i - cu_chunk_lens[s]), found through the block
-// table, copied raw or widened fp8 -> bf16 ("PR #51772 [Attention][MLA] Fuse
+// table, copied raw or widened fp8 -> bf16 / fp16 ("PR #51772 [Attention][MLA] Fuse
 // Kimi-K3 chunked-context K/V packing", Implementation item 2:
 // _gather_context_latent, and item 5: the conditional cast to the kv_b_proj
 // input dtype, fused here into the gather).  The widening is exact, or
@@ -24,9 +24,9 @@ constexpr int kThreads = 256;
 constexpr int kRows = 4;
 constexpr int kMaxChunks = 3;        // up to 96 x 16 B = 1536-byte rows
 
-// MODE 0: raw copy; kE4M3 / kE5M2: widen that fp8 format to bf16 (times the
-// dequantisation scale when SCALED).
-template <int MODE, bool SCALED>
+// MODE 0: raw copy; kE4M3 / kE5M2: widen that fp8 format to OUT (bf16 or
+// fp16; bf16 times the dequantisation scale when SCALED).
+template <int MODE, int OUT, bool SCALED>
 __global__ void __launch_bounds__(kThreads) gather_kernel(const GatherArgs a) {
   pdl_trigger();
   pdl_wait();
@@ -74,8 +74,8 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const GatherArgs a) {
           st16(dst + ch * 32 + 16,
                fp8x8_to_bf16x8_scaled<MODE>(make_uint2(v[k][c].z, v[k][c].w), s2));
         } else {
-          st16(dst + ch * 32, fp8x8_to_bf16x8<MODE>(make_uint2(v[k][c].x, v[k][c].y)));
-          st16(dst + ch * 32 + 16, fp8x8_to_bf16x8<MODE>(make_uint2(v[k][c].z, v[k][c].w)));
+          st16(dst + ch * 32, fp8x8_to_x16x8<MODE, OUT>(make_uint2(v[k][c].x, v[k][c].y)));
+          st16(dst + ch * 32 + 16, fp8x8_to_x16x8<MODE, OUT>(make_uint2(v[k][c].z, v[k][c].w)));
         }
       }
     }
@@ -84,9 +84,9 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const GatherArgs a) {
   if (errbits && lane == 0 && a.err) atomicOr(a.err, errbits);
 }
 
-template <int MODE, bool SCALED>
+template <int MODE, int OUT, bool SCALED>
 cudaError_t launch_t(const GatherArgs& a, const LaunchCfg& cfg) {
-  auto kern = gather_kernel<MODE, SCALED>;
+  auto kern = gather_kernel<MODE, OUT, SCALED>;
   const int64_t warps = ((int64_t)a.num_tokens + kRows - 1) / kRows;
   const int64_t ctas = (warps + kThreads / 32 - 1) / (kThreads / 32);
   cudaLaunchConfig_t lc = {};
@@ -101,14 +101,22 @@ cudaError_t launch_t(const GatherArgs& a, const LaunchCfg& cfg) {
   return cudaLaunchKernelEx(&lc, kern, a);
 }
 
+template <int MODE>
+cudaError_t launch_widen(const GatherArgs& a, int out_fmt, const LaunchCfg& cfg) {
+  if (a.dequant_scale)
+    return out_fmt == kBF16 ? launch_t<MODE, kBF16, true>(a, cfg) : cudaErrorInvalidValue;
+  if (out_fmt == kBF16) return launch_t<MODE, kBF16, false>(a, cfg);
+  if (out_fmt == kF16) return launch_t<MODE, kF16, false>(a, cfg);
+  return cudaErrorInvalidValue;
+}
+
 }  // namespace
 
-cudaError_t launch_gather(const GatherArgs& a, int mode, const LaunchCfg& cfg) {
-  const bool scaled = a.dequant_scale != nullptr;
+cudaError_t launch_gather(const GatherArgs& a, int mode, int out_fmt, const LaunchCfg& cfg) {
   switch (mode) {
-    case 0: return launch_t<0, false>(a, cfg);
-    case kE4M3: return scaled ? launch_t<kE4M3, true>(a, cfg) : launch_t<kE4M3, false>(a, cfg);
-    case kE5M2: return scaled ? launch_t<kE5M2, true>(a, cfg) : launch_t<kE5M2, false>(a, cfg);
+    case 0: return launch_t<0, kBF16, false>(a, cfg);
+    case kE4M3: return launch_widen<kE4M3>(a, out_fmt, cfg);
+    case kE5M2: return launch_widen<kE5M2>(a, out_fmt, cfg);
     default: return cudaErrorInvalidValue;
   }
 }

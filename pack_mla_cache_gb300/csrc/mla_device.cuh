@@ -12,7 +12,10 @@
 
 namespace mla {
 
-enum Fmt : int { kBF16 = 0, kE4M3 = 1, kE5M2 = 2 };
+enum Fmt : int { kBF16 = 0, kE4M3 = 1, kE5M2 = 2, kF16 = 3 };
+
+// Whether a format is a 16-bit float (bf16 or fp16).
+constexpr bool is16(int f) { return f == kBF16 || f == kF16; }
 
 constexpr uint32_t kErrSlotOOB = 1u;
 constexpr uint32_t kErrBlockOOB = 2u;
@@ -51,6 +54,29 @@ __device__ __forceinline__ void st8(void* p, uint2 v) { *reinterpret_cast<uint2*
 // ---- bf16 ------------------------------------------------------------------
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// ---- fp16 ------------------------------------------------------------------
+__device__ __forceinline__ float f16lo(uint32_t w) {
+  float f;
+  asm("{ .reg .b16 a, b; mov.b32 {a, b}, %1; cvt.f32.f16 %0, a; }" : "=f"(f) : "r"(w));
+  return f;
+}
+__device__ __forceinline__ float f16hi(uint32_t w) {
+  float f;
+  asm("{ .reg .b16 a, b; mov.b32 {a, b}, %1; cvt.f32.f16 %0, b; }" : "=f"(f) : "r"(w));
+  return f;
+}
+// The two 16-bit floats of a word (format IF) as exact fp32 values.
+template <int IF>
+__device__ __forceinline__ float x16lo(uint32_t w) {
+  if constexpr (IF == kF16) return f16lo(w);
+  else return __uint_as_float(w << 16);
+}
+template <int IF>
+__device__ __forceinline__ float x16hi(uint32_t w) {
+  if constexpr (IF == kF16) return f16hi(w);
+  else return __uint_as_float(w & 0xFFFF0000u);
+}
 
 // Two fp32 -> bf16x2, round to nearest even; `lo` lands in the low half.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -179,7 +205,10 @@ struct DivConst {
   float b, y;
   uint64_t y2, nb2;  // ( y,  y), (-b, -b): guarded path
   uint64_t ny2, b2;  // (-y, -y), ( b,  b): fast path
-  uint32_t thr2;
+  uint32_t thr2;   // bf16 inputs
+  uint32_t thr2h;  // fp16 inputs: 0x8000 - 0x7C00 (only inf / NaN are special)
+                   // while |y| < 2^111 (|a| <= 65504 < 2^16 keeps a*y finite),
+                   // else 0x7FFF (every nonzero value takes the guarded path)
   bool fast;
 };
 __device__ __forceinline__ DivConst div_const(float scale) {
@@ -196,6 +225,8 @@ __device__ __forceinline__ DivConst div_const(float scale) {
   const int t = min(381 - e_y, 255);
   const uint32_t h = 0x8000u - ((uint32_t)max(t, 1) << 7);
   k.thr2 = h | (h << 16);
+  const uint32_t hh = ay < 2.5961484e33f ? 0x0400u : 0x7FFFu;  // 2^111
+  k.thr2h = hh | (hh << 16);
   return k;
 }
 
@@ -227,9 +258,10 @@ __device__ __forceinline__ float2 div2(float a0, float a1, const DivConst& k) {
 // -a, q = (-a)(-y), r' = q*b - a (exact), q' = q - r'*y is the correctly rounded
 // a/b, and the sign of a zero input survives every step (-0 -> q = -0,
 // r' = +0, q' = -0), so no per-element fix-up is needed.
+template <int IF = kBF16>
 __device__ __forceinline__ float2 div2_fast(uint32_t w, const DivConst& k) {
   const uint32_t nw = w ^ 0x80008000u;
-  const uint64_t na = f2(bf16lo(nw), bf16hi(nw));
+  const uint64_t na = f2(x16lo<IF>(nw), x16hi<IF>(nw));
   const uint64_t q = mul2(na, k.ny2);
   const uint64_t r = fma2(q, k.b2, na);
   return unf2(fma2(r, k.ny2, q));
@@ -247,6 +279,31 @@ __device__ __forceinline__ bool special_pairs(uint32_t m, uint32_t thr2) {
   return ((m + thr2) & 0x80008000u) != 0u;
 }
 
+// 8 16-bit floats of format IF (one uint4) -> 8 fp8 (one uint2), each value
+// divided by the scale; the special-value check is done once for the 8.
+template <int F, int IF, bool FAST>
+__device__ __forceinline__ uint2 x16x8_to_fp8x8(uint4 v, const DivConst& k) {
+  uint2 o;
+  if constexpr (FAST) {
+    const uint32_t m = umax16x2(umax16x2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                                umax16x2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+    if (!special_pairs(m, IF == kF16 ? k.thr2h : k.thr2)) {
+      const float2 q0 = div2_fast<IF>(v.x, k), q1 = div2_fast<IF>(v.y, k);
+      const float2 q2 = div2_fast<IF>(v.z, k), q3 = div2_fast<IF>(v.w, k);
+      o.x = pack_fp8x4<F>(q0.x, q0.y, q1.x, q1.y);
+      o.y = pack_fp8x4<F>(q2.x, q2.y, q3.x, q3.y);
+      return o;
+    }
+  }
+  const float2 q0 = div2<FAST>(x16lo<IF>(v.x), x16hi<IF>(v.x), k);
+  const float2 q1 = div2<FAST>(x16lo<IF>(v.y), x16hi<IF>(v.y), k);
+  const float2 q2 = div2<FAST>(x16lo<IF>(v.z), x16hi<IF>(v.z), k);
+  const float2 q3 = div2<FAST>(x16lo<IF>(v.w), x16hi<IF>(v.w), k);
+  o.x = pack_fp8x4<F>(q0.x, q0.y, q1.x, q1.y);
+  o.y = pack_fp8x4<F>(q2.x, q2.y, q3.x, q3.y);
+  return o;
+}
+
 // Two bf16 in a 32-bit word -> two fp8 (low 16 bits), divided by the scale.
 template <int F, bool FAST>
 __device__ __forceinline__ uint32_t bf16x2_to_fp8x2(uint32_t w, const DivConst& k) {
@@ -261,28 +318,9 @@ __device__ __forceinline__ uint32_t bf16x2_to_fp8x2(uint32_t w, const DivConst& 
 }
 
 // 8 bf16 (one uint4) -> 8 fp8 (one uint2), each value divided by the scale.
-// The special-value check is done once for the 8 values.
 template <int F, bool FAST>
 __device__ __forceinline__ uint2 bf16x8_to_fp8x8(uint4 v, const DivConst& k) {
-  uint2 o;
-  if constexpr (FAST) {
-    const uint32_t m = umax16x2(umax16x2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
-                                umax16x2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
-    if (!special_pairs(m, k.thr2)) {
-      const float2 q0 = div2_fast(v.x, k), q1 = div2_fast(v.y, k);
-      const float2 q2 = div2_fast(v.z, k), q3 = div2_fast(v.w, k);
-      o.x = pack_fp8x4<F>(q0.x, q0.y, q1.x, q1.y);
-      o.y = pack_fp8x4<F>(q2.x, q2.y, q3.x, q3.y);
-      return o;
-    }
-  }
-  const float2 q0 = div2<FAST>(bf16lo(v.x), bf16hi(v.x), k);
-  const float2 q1 = div2<FAST>(bf16lo(v.y), bf16hi(v.y), k);
-  const float2 q2 = div2<FAST>(bf16lo(v.z), bf16hi(v.z), k);
-  const float2 q3 = div2<FAST>(bf16lo(v.w), bf16hi(v.w), k);
-  o.x = pack_fp8x4<F>(q0.x, q0.y, q1.x, q1.y);
-  o.y = pack_fp8x4<F>(q2.x, q2.y, q3.x, q3.y);
-  return o;
+  return x16x8_to_fp8x8<F, kBF16, FAST>(v, k);
 }
 
 // 8 fp8 (one uint2) -> 8 bf16 (one uint4), exact.
@@ -294,6 +332,34 @@ __device__ __forceinline__ uint4 fp8x8_to_bf16x8(uint2 v) {
   o.z = fp8x2_to_bf16x2<F>(v.y);
   o.w = fp8x2_to_bf16x2<F>(v.y >> 16);
   return o;
+}
+
+// fp8x2 (low 16 bits of `w`) -> two exact fp16 values (the hardware widening
+// is exact for both formats); a NaN becomes the quiet NaN 0x7E00 with the fp8
+// code's sign.
+template <int F>
+__device__ __forceinline__ uint32_t fp8x2_to_f16x2(uint32_t w) {
+  uint32_t h2;
+  const uint16_t in = static_cast<uint16_t>(w);
+  if constexpr (F == kE4M3) {
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+  } else {
+    asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(h2) : "h"(in));
+  }
+  if ((h2 & 0x7FFFu) > 0x7C00u) h2 = (h2 & 0xFFFF0000u) | ((in & 0x80u) << 8) | 0x7E00u;
+  if ((h2 & 0x7FFF0000u) > 0x7C000000u) h2 = (h2 & 0xFFFFu) | ((in & 0x8000u) << 16) | 0x7E000000u;
+  return h2;
+}
+
+// 8 fp8 (one uint2) -> 8 exact 16-bit floats of format OF (bf16 or fp16).
+template <int F, int OF>
+__device__ __forceinline__ uint4 fp8x8_to_x16x8(uint2 v) {
+  if constexpr (OF == kBF16) {
+    return fp8x8_to_bf16x8<F>(v);
+  } else {
+    return make_uint4(fp8x2_to_f16x2<F>(v.x), fp8x2_to_f16x2<F>(v.x >> 16),
+                      fp8x2_to_f16x2<F>(v.y), fp8x2_to_f16x2<F>(v.y >> 16));
+  }
 }
 
 __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {

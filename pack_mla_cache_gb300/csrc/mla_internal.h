@@ -105,11 +105,12 @@ struct LaunchCfg {
 // take the values of mla::Fmt.
 cudaError_t launch_insert(const InsertArgs& a, int cache_fmt, bool norm, bool rope,
                           const LaunchCfg& cfg);
-// mode: 0 raw copy, else the fp8 format widened to bf16 (scaled when
-// a.dequant_scale is set).
-cudaError_t launch_gather(const GatherArgs& a, int mode, const LaunchCfg& cfg);
-// paged: k_pe from a.paged (kpe_fmt = the cache's format) instead of a.k_pe.
-cudaError_t launch_pack(const PackArgs& a, int out_fmt, int kpe_fmt, bool paged,
+// mode: 0 raw copy, else the fp8 format widened to out_fmt (bf16 or fp16;
+// bf16 times the scale when a.dequant_scale is set).
+cudaError_t launch_gather(const GatherArgs& a, int mode, int out_fmt, const LaunchCfg& cfg);
+// in_fmt: kBF16 or kF16 (k_nope / v); paged: k_pe from a.paged (kpe_fmt = the
+// cache's format) instead of a.k_pe.
+cudaError_t launch_pack(const PackArgs& a, int in_fmt, int out_fmt, int kpe_fmt, bool paged,
                         const LaunchCfg& cfg);
 cudaError_t launch_norm_rope(const NormRopeArgs& a, bool norm, bool rope, const LaunchCfg& cfg);
 cudaError_t launch_rope_table(float* out, int64_t max_position, int32_t rot_dim, double base,

@@ -1,209 +1,17 @@
-// pack.cu -- chunked-context K/V pack for sm_103a.
-//
-// What it computes: the contiguous full key [k_nope | k_pe] (k_pe broadcast to
-// every head) and the contiguous V from the strided kv_b_proj output and a
-// k_pe that may still be fp8 from the cache, in bf16 or fp8 ("PR #51772
-// [Attention][MLA] Fuse Kimi-K3 chunked-context K/V packing", Implementation
-// item 1 and Source snippets: fused_mla_kv_concat /
-// fused_mla_kv_concat_quant_fp8).
-//
-// Design: a work item is one token's group of up to 8 heads (4 KB of k_nope +
-// v), so a 16-head token is two items; one warp per item, its 8 16-byte loads
-// per lane issued before the first store (74 registers, 3 CTAs and 24 warps --
-// 96 KB of loads -- in flight per SM, enough to keep HBM busy; staging the
-// items through shared memory with bulk copies measured slower, 19.8 vs 17.6 us
-// per 8192-token chunk).  The grid is capped at the resident CTAs and loops
-// over items (long contexts never grow the grid); lanes 0-15 write a head's
-// k_nope slice and lanes 16-31 its V slice, 8 elements each, so every warp
-// store is whole sectors; k_pe part (lane % 8) is loaded and converted once
-// per item; fp8 output uses the exact division by the scale (fast path chosen
-// once per launch) and the hardware .satfinite converters; an fp8 k_pe is
-// copied byte for byte; an fp8 k_pe into a bf16 key goes through the exact
-// widening.  Any strides, no-V packs and any head count take the same kernel.
-//
-// The paged form reads each token's k_pe straight from the paged cache (the
-// row the context gather would fetch, paged.cuh), so the gather workspace only
-// needs the kv_c columns; a token whose row is not found keeps its key's rope
-// slice and, for a bad block index or id, sets MLA_ERRBIT_BLOCK_OOB.
-#include "mla_device.cuh"
-#include "mla_internal.h"
-#include "paged.cuh"
+// pack.cu -- chunked-context K/V pack for sm_103a: the bf16-input instances
+// and the dispatch on the input format (kernel design: pack_kernel.cuh).
+#include "pack_kernel.cuh"
 
 namespace mla {
-namespace {
 
-constexpr int kNope = 128, kRope = 64, kV = 128, kKey = kNope + kRope;
-constexpr int kGroup = 8;  // heads per work item
+cudaError_t launch_pack_f16(const PackArgs& a, int out_fmt, int kpe_fmt, bool paged,
+                            const LaunchCfg& cfg);
 
-struct Item {
-  int64_t t;
-  int h0, nh;  // first head and head count of the item
-};
-
-// Item j -> (token, head group).  Item counts stay below 2^32 (tokens are
-// int32 and at most a few groups per token), so 32-bit division suffices; the
-// usual 16-head case (2 groups) is a shift.
-__device__ __forceinline__ Item item_of(int64_t j, int groups, int H) {
-  Item it;
-  const uint32_t ju = (uint32_t)j;
-  it.t = groups == 2 ? (int64_t)(ju >> 1) : (int64_t)(ju / (uint32_t)groups);
-  const int g = (int)(ju - (uint32_t)it.t * (uint32_t)groups);
-  it.h0 = g * kGroup;
-  it.nh = min(kGroup, H - it.h0);
-  return it;
-}
-
-// The k_pe part of this lane (elements 8*(lane%8) .. +8) in the output format.
-template <int OF, int KF, bool FAST>
-__device__ __forceinline__ void pe_part(const uint4& x16, const uint2& x8, const DivConst& k,
-                                        uint4& o16, uint2& o8) {
-  if constexpr (KF == kBF16) {
-    if constexpr (OF == kBF16) o16 = x16;
-    else o8 = bf16x8_to_fp8x8<OF, FAST>(x16, k);
-  } else {
-    if constexpr (OF == kBF16) o16 = fp8x8_to_bf16x8<KF>(x8);
-    else o8 = x8;  // same fp8 format: raw bytes
-  }
-}
-
-// One head row (lane < 16: k_nope part `lane`; lane >= 16: v part lane-16).
-template <int OF, bool FAST>
-__device__ __forceinline__ void put_unit(uint8_t* dst, const uint4& x, const DivConst& k) {
-  if constexpr (OF == kBF16) st16(dst, x);
-  else st8(dst, bf16x8_to_fp8x8<OF, FAST>(x, k));
-}
-
-template <int OF>
-__device__ __forceinline__ void put_pe(uint8_t* dst, const uint4& o16, const uint2& o8) {
-  if constexpr (OF == kBF16) st16(dst, o16);
-  else st8(dst, o8);
-}
-
-// ---- plain vectorised variant -------------------------------------------------
-constexpr int kThreads = 256;
-
-template <int OF, int KF, bool FAST, bool PAGED>
-__device__ __forceinline__ void pack_plain_items(const PackArgs& a, const DivConst& k) {
-  constexpr int OE = (OF == kBF16) ? 2 : 1;
-  const int lane = threadIdx.x & 31, H = a.num_heads;
-  const int groups = (H + kGroup - 1) / kGroup;
-  const int64_t n_items = (int64_t)a.num_tokens * groups;
-  const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
-  const bool has_v = a.vout != nullptr;
-  const int part_pe = lane & 7;
-  const int half = lane >> 4, part = lane & 15;  // v half (lanes 16-31) / unit in the half
-  SeqLanes sl{};
-  if constexpr (PAGED) sl = load_seq_lanes(a.paged, lane);
-  uint32_t errbits = 0;
-  for (int64_t j = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5; j < n_items; j += nwarps) {
-    const Item it = item_of(j, groups, H);
-    const uint8_t* pe;
-    if constexpr (PAGED) {
-      pe = paged_row(a.paged, sl, lane, it.t, errbits);
-      if (pe) pe += a.pe_off;
-    } else {
-      pe = a.k_pe + it.t * a.kpe_ts;
-    }
-    const uint8_t* src = (half ? a.v + it.t * a.v_ts : a.k_nope + it.t * a.kn_ts) + part * 16;
-    const int64_t hs = half ? a.v_hs : a.kn_hs;
-    uint4 x[kGroup];
-#pragma unroll
-    for (int i = 0; i < kGroup; ++i) {
-      x[i] = make_uint4(0, 0, 0, 0);
-      if (i < it.nh && (!half || has_v)) x[i] = ld_stream16(src + (int64_t)(it.h0 + i) * hs);
-    }
-    uint4 p16 = make_uint4(0, 0, 0, 0);
-    uint2 p8 = make_uint2(0, 0);
-    if (!PAGED || pe) {
-      uint4 x16 = make_uint4(0, 0, 0, 0);
-      uint2 x8 = make_uint2(0, 0);
-      if constexpr (KF == kBF16) x16 = ld_stream16(pe + part_pe * 16);
-      else x8 = ld_stream8(pe + part_pe * 8);
-      pe_part<OF, KF, FAST>(x16, x8, k, p16, p8);
-    }
-    uint8_t* key = a.key + (it.t * H + it.h0) * (int64_t)kKey * OE;
-    uint8_t* dst = half ? a.vout + (it.t * H + it.h0) * (int64_t)kV * OE + part * 8 * OE
-                        : key + part * 8 * OE;
-    const int dstride = (half ? kV : kKey) * OE;
-#pragma unroll
-    for (int i = 0; i < kGroup; ++i)
-      if (i < it.nh && (!half || has_v)) put_unit<OF, FAST>(dst + i * dstride, x[i], k);
-    if (!PAGED || pe)
-      for (int u = lane; u < it.nh * 8; u += 32)
-        put_pe<OF>(key + ((u >> 3) * kKey + kNope + part_pe * 8) * OE, p16, p8);
-  }
-  if constexpr (PAGED) {
-    errbits = __reduce_or_sync(0xFFFFFFFFu, errbits);
-    if (errbits && lane == 0 && a.err) atomicOr(a.err, errbits);
-  }
-}
-
-template <int OF, int KF, bool PAGED>
-__global__ void __launch_bounds__(kThreads) pack_kernel(const PackArgs a) {
-  pdl_trigger();
-  pdl_wait();
-  float scale = 1.0f;
-  if constexpr (OF != kBF16) {
-    if (a.out_scale) scale = *a.out_scale;
-  }
-  const DivConst k = div_const(scale);
-  if constexpr (OF == kBF16) {
-    pack_plain_items<OF, KF, true, PAGED>(a, k);
-  } else {
-    if (k.fast) pack_plain_items<OF, KF, true, PAGED>(a, k);
-    else pack_plain_items<OF, KF, false, PAGED>(a, k);
-  }
-}
-
-cudaLaunchConfig_t base_cfg(const LaunchCfg& cfg, cudaLaunchAttribute* attr) {
-  cudaLaunchConfig_t lc = {};
-  lc.stream = cfg.stream;
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  lc.attrs = attr;
-  lc.numAttrs = cfg.pdl ? 1 : 0;
-  return lc;
-}
-
-template <int OF, int KF, bool PAGED>
-cudaError_t launch_plain_t(const PackArgs& a, const LaunchCfg& cfg) {
-  auto kern = pack_kernel<OF, KF, PAGED>;
-  const int64_t items = (int64_t)a.num_tokens * ((a.num_heads + kGroup - 1) / kGroup);
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t lc = base_cfg(cfg, attr);
-  lc.gridDim = dim3(capped_grid(reinterpret_cast<const void*>(kern), kThreads,
-                                (items + kThreads / 32 - 1) / (kThreads / 32)));
-  lc.blockDim = dim3(kThreads);
-  return cudaLaunchKernelEx(&lc, kern, a);
-}
-
-template <int OF, int KF>
-cudaError_t launch_variant(const PackArgs& a, bool paged, const LaunchCfg& cfg) {
-  return paged ? launch_plain_t<OF, KF, true>(a, cfg) : launch_plain_t<OF, KF, false>(a, cfg);
-}
-
-template <int OF>
-cudaError_t launch_kpe(const PackArgs& a, int kpe_fmt, bool paged, const LaunchCfg& cfg) {
-  if (kpe_fmt == kBF16) return launch_variant<OF, kBF16>(a, paged, cfg);
-  if constexpr (OF == kBF16 || OF == kE4M3) {
-    if (kpe_fmt == kE4M3) return launch_variant<OF, kE4M3>(a, paged, cfg);
-  }
-  if constexpr (OF == kBF16 || OF == kE5M2) {
-    if (kpe_fmt == kE5M2) return launch_variant<OF, kE5M2>(a, paged, cfg);
-  }
-  return cudaErrorInvalidValue;
-}
-
-}  // namespace
-
-cudaError_t launch_pack(const PackArgs& a, int out_fmt, int kpe_fmt, bool paged,
+cudaError_t launch_pack(const PackArgs& a, int in_fmt, int out_fmt, int kpe_fmt, bool paged,
                         const LaunchCfg& cfg) {
-  switch (out_fmt) {
-    case kBF16: return launch_kpe<kBF16>(a, kpe_fmt, paged, cfg);
-    case kE4M3: return launch_kpe<kE4M3>(a, kpe_fmt, paged, cfg);
-    case kE5M2: return launch_kpe<kE5M2>(a, kpe_fmt, paged, cfg);
-    default: return cudaErrorInvalidValue;
-  }
+  if (in_fmt == kF16) return launch_pack_f16(a, out_fmt, kpe_fmt, paged, cfg);
+  if (in_fmt == kBF16) return launch_pack_in<kBF16>(a, out_fmt, kpe_fmt, paged, cfg);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace mla

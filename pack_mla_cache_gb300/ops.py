@@ -16,13 +16,13 @@ import torch
 
 from .build import LIB_PATH
 
-MLA_BF16, MLA_FP8_E4M3, MLA_FP8_E5M2 = 0, 1, 2
+MLA_BF16, MLA_FP8_E4M3, MLA_FP8_E5M2, MLA_FP16 = 0, 1, 2, 3
 MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_MISALIGNED, MLA_ERR_CUDA = range(5)
 MLA_ERRBIT_SLOT_OOB, MLA_ERRBIT_BLOCK_OOB, MLA_ERRBIT_POS_OOB, MLA_ERRBIT_MISALIGNED = 1, 2, 4, 8
 MLA_ERRBIT_TIMEOUT = 16
 
 _TORCH_DTYPE = {MLA_BF16: torch.bfloat16, MLA_FP8_E4M3: torch.float8_e4m3fn,
-                MLA_FP8_E5M2: torch.float8_e5m2}
+                MLA_FP8_E5M2: torch.float8_e5m2, MLA_FP16: torch.float16}
 
 
 class MlaError(RuntimeError):
@@ -54,13 +54,14 @@ SIGNATURES = {
         _vp, ctypes.c_int, _i64, _i32, _i64, _i64, _i32, _vp, _i64, _vp, _vp, _i32, _i32, _vp,
         _i64, ctypes.c_int, _vp, _vp]),
     "mla_context_kv_pack": (ctypes.c_int, [
-        _vp, _i64, _i64, _vp, _i64, _i64, _vp, _i64, ctypes.c_int, _i32, _i32, _i32, _i32, _i32,
-        _vp, _vp, ctypes.c_int, _vp, _vp, _vp]),
+        _vp, _i64, _i64, _vp, _i64, _i64, ctypes.c_int, _vp, _i64, ctypes.c_int, _i32, _i32, _i32,
+        _i32, _i32, _vp, _vp, ctypes.c_int, _vp, _vp, _vp]),
     "mla_context_gather_scaled": (ctypes.c_int, [
         _vp, ctypes.c_int, _i64, _i32, _i64, _i64, _i32, _vp, _i64, _vp, _vp, _i32, _i32, _vp,
         _i64, _vp, _vp, _vp]),
     "mla_context_kv_pack_paged": (ctypes.c_int, [
-        _vp, _i64, _i64, _vp, _i64, _i64, _vp, ctypes.c_int, _i64, _i32, _i64, _i64, _i64, _vp,
+        _vp, _i64, _i64, _vp, _i64, _i64, ctypes.c_int, _vp, ctypes.c_int, _i64, _i32, _i64, _i64,
+        _i64, _vp,
         _i64, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp, ctypes.c_int, _vp, _vp,
         _vp]),
     "mla_norm_rope_grouped": (ctypes.c_int, [
@@ -215,13 +216,15 @@ def mla_context_gather_scaled(kv_cache, cache_dtype, num_blocks, block_size, blo
 def mla_context_kv_pack_paged(k_nope, v, kv_cache, cache_dtype, num_blocks, block_size,
                               block_stride, entry_stride, block_table, cu_chunk_lens,
                               chunk_starts, key_out, v_out, out_dtype, *, rope_offset=512,
-                              rope_dim=64, out_scale=None, err_word=None, stream=None):
+                              rope_dim=64, out_scale=None, in_dtype=None, err_word=None,
+                              stream=None):
     """The pack with each token's k_pe read from its paged cache row at
     ``rope_offset``; k_nope / v [T, H, 128] bf16 views (strided)."""
     T, H, N = k_nope.shape
     _check(lib().mla_context_kv_pack_paged(
         _ptr(k_nope), k_nope.stride(0), k_nope.stride(1), _ptr(v), v.stride(0), v.stride(1),
-        _ptr(kv_cache), dtype_code(cache_dtype), num_blocks, block_size, block_stride,
+        dtype_code(in_dtype if in_dtype is not None else k_nope.dtype), _ptr(kv_cache),
+        dtype_code(cache_dtype), num_blocks, block_size, block_stride,
         entry_stride, rope_offset, _ptr(block_table), _bt_stride(block_table),
         _ptr(cu_chunk_lens), _ptr(chunk_starts), chunk_starts.shape[0], T, H, N, rope_dim,
         v.shape[2], _ptr(key_out), _ptr(v_out), dtype_code(out_dtype), _ptr(out_scale),
@@ -229,14 +232,16 @@ def mla_context_kv_pack_paged(k_nope, v, kv_cache, cache_dtype, num_blocks, bloc
 
 
 def mla_context_kv_pack(k_nope, v, k_pe, key_out, v_out, out_dtype, *, kpe_dtype=None,
-                        out_scale=None, err_word=None, stream=None):
-    """k_nope / v: [T, H, 128] bf16 views (strided); k_pe [T, 64] (bf16 or fp8,
-    strided rows); key_out [T, H, 192] and v_out [T, H, 128] (or None)."""
+                        out_scale=None, in_dtype=None, err_word=None, stream=None):
+    """k_nope / v: [T, H, 128] bf16 or fp16 views (strided; their dtype is the
+    input type unless ``in_dtype`` is given); k_pe [T, 64] (the input type or
+    fp8, strided rows); key_out [T, H, 192] and v_out [T, H, 128] (or None)."""
     T, H, N = k_nope.shape
     kd = dtype_code(kpe_dtype if kpe_dtype is not None else k_pe.dtype)
     _check(lib().mla_context_kv_pack(
         _ptr(k_nope), k_nope.stride(0), k_nope.stride(1), _ptr(v), v.stride(0), v.stride(1),
-        _ptr(k_pe), k_pe.stride(0), kd, T, H, N, k_pe.shape[-1], v.shape[2], _ptr(key_out),
+        dtype_code(in_dtype if in_dtype is not None else k_nope.dtype), _ptr(k_pe),
+        k_pe.stride(0), kd, T, H, N, k_pe.shape[-1], v.shape[2], _ptr(key_out),
         _ptr(v_out), dtype_code(out_dtype), _ptr(out_scale), _ptr(err_word), _stream(stream)))
 
 

@@ -86,6 +86,7 @@ def insert(L, **kw):
     (dict(T=-1), ops.MLA_ERR_INVALID_ARG, "num_tokens"),
     (dict(nl=0), ops.MLA_ERR_INVALID_ARG, "num_layers"),
     (dict(dtype=7), ops.MLA_ERR_INVALID_ARG, "cache_dtype"),
+    (dict(dtype=3), ops.MLA_ERR_INVALID_ARG, "cache_dtype"),  # no fp16 caches in the insert
     (dict(R=256), ops.MLA_ERR_UNSUPPORTED, "kv_lora_rank"),
     (dict(P=32), ops.MLA_ERR_UNSUPPORTED, "pe_dim"),
     (dict(scales=None), ops.MLA_ERR_INVALID_ARG, "FP8 grouped cache insert requires kv_scales"),
@@ -124,8 +125,8 @@ def test_insert_norm_rope_checks(L):
 
 def test_zero_tokens_is_a_no_op_without_cuda(L):
     assert insert(L, T=0) == ops.MLA_OK
-    assert L.mla_context_kv_pack(A, 4160, 256, A, 4160, 256, A, 576, 1, 0, 16, 128, 64, 128, A,
-                                 A, 1, None, None, None) == ops.MLA_OK
+    assert L.mla_context_kv_pack(A, 4160, 256, A, 4160, 256, 0, A, 576, 1, 0, 16, 128, 64, 128,
+                                 A, A, 1, None, None, None) == ops.MLA_OK
 
 
 def test_validated_call_without_gpu_reports_cuda_error(L):
@@ -150,6 +151,8 @@ def gather(L, **kw):
     (dict(S=0), ops.MLA_ERR_INVALID_ARG),
     (dict(cdt=0, odt=1), ops.MLA_ERR_UNSUPPORTED),
     (dict(cdt=1, odt=2), ops.MLA_ERR_UNSUPPORTED),
+    (dict(cdt=0, odt=3), ops.MLA_ERR_UNSUPPORTED),     # bf16 rows are not widened to fp16
+    (dict(cdt=3, odt=0), ops.MLA_ERR_UNSUPPORTED),
     (dict(bt=None), ops.MLA_ERR_INVALID_ARG),
     (dict(edim=600), ops.MLA_ERR_INVALID_ARG),
     (dict(edim=570, estride=576), ops.MLA_ERR_MISALIGNED),
@@ -177,6 +180,7 @@ def gather_scaled(L, **kw):
 @pytest.mark.parametrize("kw,status", [
     (dict(T=-1), ops.MLA_ERR_INVALID_ARG),
     (dict(cdt=0), ops.MLA_ERR_UNSUPPORTED),      # a bf16 cache has nothing to dequantise
+    (dict(cdt=3), ops.MLA_ERR_UNSUPPORTED),
     (dict(cdt=7), ops.MLA_ERR_INVALID_ARG),
     (dict(scale=None), ops.MLA_ERR_INVALID_ARG),
     (dict(scale=A + 2), ops.MLA_ERR_MISALIGNED),
@@ -197,13 +201,15 @@ def test_gather_scaled_zero_tokens_is_ok_without_pointers(L):
 
 
 def pack_paged(L, **kw):
-    a = dict(kn=A, kts=4160, khs=256, v=A + 256, vts=4160, vhs=256, cache=A + (3 << 30), cdt=1,
+    a = dict(kn=A, kts=4160, khs=256, v=A + 256, vts=4160, vhs=256, idt=0, cache=A + (3 << 30),
+             cdt=1,
              nb=1024, bs=64, bstride=64 * 576, estride=576, roff=512, bt=A + 4096, bts=512,
              cu=A + 8192, st=A + 12288, S=1, T=8192, H=16, N=128, R=64, V=128,
              key=A + (1 << 30), vout=A + (2 << 30), odt=1, scale=None, err=None)
     a.update(kw)
     return L.mla_context_kv_pack_paged(
-        a["kn"], a["kts"], a["khs"], a["v"], a["vts"], a["vhs"], a["cache"], a["cdt"], a["nb"],
+        a["kn"], a["kts"], a["khs"], a["v"], a["vts"], a["vhs"], a["idt"], a["cache"], a["cdt"],
+        a["nb"],
         a["bs"], a["bstride"], a["estride"], a["roff"], a["bt"], a["bts"], a["cu"], a["st"],
         a["S"], a["T"], a["H"], a["N"], a["R"], a["V"], a["key"], a["vout"], a["odt"],
         a["scale"], a["err"], None)
@@ -233,6 +239,7 @@ def pack_paged(L, **kw):
     (dict(cache=None), ops.MLA_ERR_INVALID_ARG),
     (dict(bt=None), ops.MLA_ERR_INVALID_ARG),
     (dict(kn=None), ops.MLA_ERR_INVALID_ARG),
+    (dict(idt=3, cdt=0, odt=1), ops.MLA_ERR_UNSUPPORTED),  # bf16 cache rows, fp16 k_nope
 ])
 def test_pack_paged_argument_checks(L, kw, status):
     assert pack_paged(L, **kw) == status
@@ -300,12 +307,13 @@ def test_norm_rope_description_checks(L):
 
 
 def pack(L, **kw):
-    a = dict(kn=A, kts=4160, khs=256, v=A + 256, vts=4160, vhs=256, kpe=A + 1024, kpets=576,
-             kdt=1, T=8192, H=16, N=128, R=64, V=128, key=A + (1 << 30), vout=A + (2 << 30), odt=1,
-             scale=None, err=None)
+    a = dict(kn=A, kts=4160, khs=256, v=A + 256, vts=4160, vhs=256, idt=0, kpe=A + 1024,
+             kpets=576, kdt=1, T=8192, H=16, N=128, R=64, V=128, key=A + (1 << 30),
+             vout=A + (2 << 30), odt=1, scale=None, err=None)
     a.update(kw)
     return L.mla_context_kv_pack(a["kn"], a["kts"], a["khs"], a["v"], a["vts"], a["vhs"],
-                                 a["kpe"], a["kpets"], a["kdt"], a["T"], a["H"], a["N"], a["R"],
+                                 a["idt"], a["kpe"], a["kpets"], a["kdt"], a["T"], a["H"], a["N"],
+                                 a["R"],
                                  a["V"], a["key"], a["vout"], a["odt"], a["scale"], a["err"],
                                  None)
 
@@ -326,6 +334,12 @@ def pack(L, **kw):
     (dict(key=A + 8), ops.MLA_ERR_MISALIGNED),
     (dict(odt=9), ops.MLA_ERR_INVALID_ARG),
     (dict(err=A + 1), ops.MLA_ERR_MISALIGNED),
+    (dict(idt=1), ops.MLA_ERR_UNSUPPORTED),            # k_nope / v must be 16-bit
+    (dict(idt=7), ops.MLA_ERR_INVALID_ARG),
+    (dict(idt=3, odt=0, kdt=0), ops.MLA_ERR_UNSUPPORTED),  # fp16 input, bf16 output
+    (dict(idt=3, odt=1, kdt=0), ops.MLA_ERR_UNSUPPORTED),  # bf16 k_pe with fp16 k_nope
+    (dict(idt=0, odt=3, kdt=1), ops.MLA_ERR_UNSUPPORTED),  # fp16 output of bf16 input
+    (dict(idt=3, odt=3, kdt=3, scale=A), ops.MLA_ERR_INVALID_ARG),
 ])
 def test_pack_argument_checks(L, kw, status):
     assert pack(L, **kw) == status
