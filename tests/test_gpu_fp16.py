@@ -137,7 +137,7 @@ def test_gather_widens_every_code_into_fp16(orc, fmt):
 
 
 def test_gather_fp16_rows_8192(orc):
-    pw = W.pack_workload(16384, 8192, num_blocks=512, seed=6, cache_dtype=2)
+    pw = W.pack_workload(16448, 8192, num_blocks=512, seed=6, cache_dtype=2)
     for c in range(2):
         cu, st = np.array([0, 8192], np.int32), np.array([c * 8192 + 5], np.int32)
         np.testing.assert_array_equal(gpu_gather_f16(pw, pw.block_table, cu, st, 8192),
