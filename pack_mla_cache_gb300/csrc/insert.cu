@@ -14,8 +14,9 @@
 //     stores are two 256-byte warp stores, the bf16 stores two 512-byte ones.
 //     k_pe: lane l holds the neox pair (l, l+32), so the rotation needs no
 //     shuffle and every lane does one pair;
-//   * RMSNorm: 16 squares per lane on packed fp32x2 FMAs, a 5-step xor-shuffle
-//     sum, a correctly rounded reciprocal square root;
+//   * RMSNorm: 16 squares per lane on mixed-precision bf16 x bf16 + fp32 FMAs,
+//     a 5-step xor-shuffle sum, a correctly rounded reciprocal square root
+//     (norm_rope.cuh);
 //   * RoPE: each rotated element is a difference of two products with an FMA
 //     error correction (two-ulp accurate even when the products cancel);
 //   * fp8: a correctly rounded division per element on packed fp32x2 pairs
@@ -213,7 +214,7 @@ constexpr int kRun = 4;
 constexpr int kILP = 2;  // rows of an item processed in lockstep
 constexpr int kIConsumers = 16;
 constexpr int kIStages = kIConsumers * 2;
-static_assert(kIStages == 32, "producer lane s owns stage s");
+static_assert(kIStages <= 32, "producer lane s owns stage s");
 constexpr int kIThreads = (kIConsumers + 1) * 32;
 constexpr int kOffPe = kRun * 2 * kR;              // k_pe rows after the kv_c rows
 constexpr int kOffSlot = kOffPe + kRun * 2 * kP;   // then the slots
@@ -372,7 +373,7 @@ __global__ void __launch_bounds__(kIThreads, 1) insert_tma_kernel(const InsertAr
     // all 32 lanes issue, each for its own stage)
     {
       const int s = lane;
-      for (int64_t i = lane; i < n_local; i += kIStages) {
+      for (int64_t i = lane; lane < kIStages && i < n_local; i += kIStages) {
         const int64_t n = i / kIStages;
         if (n > 0 && !mbar_wait(empty0 + 8 * s, (uint32_t)((n - 1) & 1), kIWaitLimitNs)) {
           *abort_flag = 1;

@@ -6,8 +6,10 @@
 //
 // Row layout in a warp: lane l holds kv_c elements [8l, 8l+8) (x0) and
 // [256+8l, 256+8l+8) (x1) and the rotary pair (l, l+32) of k_pe.
-//   * RMSNorm: 16 squares per lane on packed fp32x2 FMAs, a 5-step xor-shuffle
-//     sum, a correctly rounded reciprocal square root, bf16 rounding;
+//   * RMSNorm: 16 squares per lane on mixed-precision FMAs (bf16 operands,
+//     fp32 accumulator: no unpacking), a 5-step xor-shuffle sum, a correctly
+//     rounded reciprocal square root; y = (x * gamma, exact in fp32) * rstd,
+//     one fp32 rounding, then bf16 rounding;
 //   * RoPE: each rotated element is a difference of two products with an FMA
 //     error correction (two-ulp accurate even when the products cancel).
 #pragma once
@@ -18,20 +20,34 @@ namespace mla {
 
 constexpr int kNormRank = 512;  // kv_lora_rank of the rows
 
+// Exact fp32 value of a*b + c for bf16 a, b (mixed-precision FMA, sm_100+).
+__device__ __forceinline__ float fma_bf16lo(uint32_t a, uint32_t b, float c) {
+  float d;
+  asm("{ .reg .b16 al, ah, bl, bh; mov.b32 {al, ah}, %1; mov.b32 {bl, bh}, %2;\n"
+      "  fma.rn.f32.bf16 %0, al, bl, %3; }" : "=f"(d) : "r"(a), "r"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float fma_bf16hi(uint32_t a, uint32_t b, float c) {
+  float d;
+  asm("{ .reg .b16 al, ah, bl, bh; mov.b32 {al, ah}, %1; mov.b32 {bl, bh}, %2;\n"
+      "  fma.rn.f32.bf16 %0, ah, bh, %3; }" : "=f"(d) : "r"(a), "r"(b), "f"(c));
+  return d;
+}
+
 // This lane's part of a row's sum of squares (16 kv_c elements in x0 / x1).
 __device__ __forceinline__ float sum_sq16(const uint4& x0, const uint4& x1) {
   const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-  uint64_t acc = f2(0.f, 0.f);
+  float a0 = 0.f, a1 = 0.f;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const uint64_t v = f2(bf16lo(w[i]), bf16hi(w[i]));
-    acc = fma2(v, v, acc);
+    a0 = fma_bf16lo(w[i], w[i], a0);
+    a1 = fma_bf16hi(w[i], w[i], a1);
   }
-  const float2 acc2 = unf2(acc);
-  return acc2.x + acc2.y;
+  return a0 + a1;
 }
 
-// y = x * rstd * gamma for this lane's 16 elements, rounded to bf16.
+// y = x * gamma * rstd for this lane's 16 elements (x * gamma is exact in
+// fp32), rounded to bf16.
 __device__ __forceinline__ void scale16(const uint4& x0, const uint4& x1, const uint4& g0,
                                         const uint4& g1, float rstd, uint4& y0, uint4& y1) {
   const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
@@ -40,8 +56,8 @@ __device__ __forceinline__ void scale16(const uint4& x0, const uint4& x1, const 
   uint32_t o[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const uint64_t v = f2(bf16lo(w[i]), bf16hi(w[i]));
-    const float2 y = unf2(mul2(mul2(v, rstd2), f2(bf16lo(gw[i]), bf16hi(gw[i]))));
+    const uint64_t xg = f2(fma_bf16lo(w[i], gw[i], -0.0f), fma_bf16hi(w[i], gw[i], -0.0f));
+    const float2 y = unf2(mul2(xg, rstd2));
     o[i] = pack_bf16x2(y.x, y.y);
   }
   y0 = make_uint4(o[0], o[1], o[2], o[3]);
