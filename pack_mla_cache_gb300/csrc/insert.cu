@@ -234,7 +234,7 @@ constexpr uint64_t kIWaitLimitNs = 2000000000ull;  // 2 s: a wait that long mean
 template <int F, bool NORM, bool ROPE, bool FAST>
 __device__ __forceinline__ uint32_t insert_consume_item(
     const InsertArgs& a, uint32_t src, const uint8_t* stage, int64_t t0, int nt, int l,
-    int lane, int64_t cptr, const DivConst& k) {
+    int lane, int64_t cptr, const DivConst& k, uint32_t empty_bar) {
   uint32_t err = 0;
   // per-row metadata: from the stage for a full run, from global for the tail
   int64_t slot[kRun], pos[kRun];
@@ -305,6 +305,12 @@ __device__ __forceinline__ uint32_t insert_consume_item(
       asm volatile("ld.shared.u16 %0, [%1];" : "=r"(lo) : "r"(pr));
       asm volatile("ld.shared.u16 %0, [%1];" : "=r"(hi) : "r"(pr + kP));
       pe[i] = lo | (hi << 16);
+    }
+    if (h + kILP >= kRun) {
+      // every read of the stage is done: hand it back to the producer before
+      // the last rows are computed
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_bar);
     }
     if constexpr (NORM) {
       float ss[kILP];
@@ -417,11 +423,11 @@ __global__ void __launch_bounds__(kIThreads, 1) insert_tma_kernel(const InsertAr
       const DivConst k = div_const(s_scale[l]);
       const int64_t cptr = s_cptr[l];
       if (F == kBF16 || k.fast)
-        errbits |= insert_consume_item<F, NORM, ROPE, true>(a, src, stage, t0, nt, l, lane, cptr, k);
+        errbits |= insert_consume_item<F, NORM, ROPE, true>(a, src, stage, t0, nt, l, lane, cptr,
+                                                            k, empty0 + 8 * s);
       else
-        errbits |= insert_consume_item<F, NORM, ROPE, false>(a, src, stage, t0, nt, l, lane, cptr, k);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8 * s);
+        errbits |= insert_consume_item<F, NORM, ROPE, false>(a, src, stage, t0, nt, l, lane, cptr,
+                                                             k, empty0 + 8 * s);
     }
   }
   __syncthreads();
