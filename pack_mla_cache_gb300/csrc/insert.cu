@@ -204,8 +204,9 @@ __global__ void __launch_bounds__(kThreads) insert_token_kernel(const InsertArgs
 // 512, k_pe token stride 64 -- the layer-major [L, T, .] buffers), one layer's
 // run of kRun consecutive tokens is contiguous.  A work item is such a run: a
 // producer warp streams its kv_c rows, k_pe rows, slots and positions into a
-// ring of 32 shared-memory stages with cp.async.bulk (byte-counted on a
-// per-stage mbarrier; lane s of the producer fills stage s), and 16 consumer
+// ring of 32 or 48 shared-memory stages (Ring below) with cp.async.bulk
+// (byte-counted on a per-stage mbarrier; lane s of the producer fills stages s
+// and s + 32), and 16 consumer
 // warps process the rows from shared memory (the
 // rotary cos/sin of the item's rows are loaded together, the layer's gamma once
 // per item).  Each consumer owns the stages s == warp (mod kIConsumers) and
@@ -213,17 +214,25 @@ __global__ void __launch_bounds__(kThreads) insert_token_kernel(const InsertArgs
 constexpr int kRun = 4;
 constexpr int kILP = 2;  // rows of an item processed in lockstep
 constexpr int kIConsumers = 16;
-constexpr int kIStages = kIConsumers * 2;
-static_assert(kIStages <= 32, "producer lane s owns stage s");
 constexpr int kIThreads = (kIConsumers + 1) * 32;
 constexpr int kOffPe = kRun * 2 * kR;              // k_pe rows after the kv_c rows
 constexpr int kOffSlot = kOffPe + kRun * 2 * kP;   // then the slots
 constexpr int kOffPos = kOffSlot + kRun * 8;       // then the positions
 constexpr int kIStageBytes = kOffPos + kRun * 8;   // 4672
 constexpr int kMaxLayers = 128;
-constexpr int kOffBars = kIStages * kIStageBytes;
-constexpr int kOffLayers = kOffBars + 2 * kIStages * 8 + 16;
-constexpr int kISmem = kOffLayers + kMaxLayers * (8 + 4);
+// The ring: 2 stages per consumer (32, one per producer lane) with RMSNorm,
+// whose consumers are compute-bound, and 3 (48; producer lanes 0-15 own two)
+// without, where a deeper ring keeps more copies in flight (measured: 102 vs
+// 112 us raw, 143 vs 137 us with RMSNorm + RoPE, 65536 tokens x 5 layers).
+template <bool NORM>
+struct Ring {
+  static constexpr int kStages = kIConsumers * (NORM ? 2 : 3);
+  static constexpr int kOffBars = kStages * kIStageBytes;
+  static constexpr int kOffLayers = kOffBars + 2 * kStages * 8 + 16;
+  static constexpr int kSmem = kOffLayers + kMaxLayers * (8 + 4);
+  static_assert(kStages <= 64, "a producer lane owns at most two stages");
+  static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
+};
 constexpr uint64_t kIWaitLimitNs = 2000000000ull;  // 2 s: a wait that long means a fault
 
 // One item (a layer's run of up to kRun tokens) from its shared-memory stage.
@@ -338,10 +347,11 @@ __device__ __forceinline__ uint32_t insert_consume_item(
 
 template <int F, bool NORM, bool ROPE>
 __global__ void __launch_bounds__(kIThreads, 1) insert_tma_kernel(const InsertArgs a) {
+  constexpr int kIStages = Ring<NORM>::kStages;
   extern __shared__ __align__(128) uint8_t smem[];
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Ring<NORM>::kOffBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kIStages);
-  int64_t* s_cptr = reinterpret_cast<int64_t*>(smem + kOffLayers);
+  int64_t* s_cptr = reinterpret_cast<int64_t*>(smem + Ring<NORM>::kOffLayers);
   float* s_scale = reinterpret_cast<float*>(s_cptr + kMaxLayers);
   const uint32_t stage0 = smem_addr(smem);
   const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + kIStages);
@@ -370,46 +380,50 @@ __global__ void __launch_bounds__(kIThreads, 1) insert_tma_kernel(const InsertAr
   const int64_t n_items = runs * L;
   const int64_t G = gridDim.x, b = blockIdx.x;
   const int64_t n_local = n_items > b ? (n_items - 1 - b) / G + 1 : 0;
-  int64_t fills = 0;  // producer lane: fills issued to its stage
+  int64_t fills0 = 0, fills1 = 0;  // producer lane: fills issued to its stages lane, lane + 32
   uint32_t errbits = 0;
 
   if (warp == kIConsumers) {
-    // ---------------- producer: lane s fills stage s -----------------------------
+    // ---------------- producer: lane s fills stages s and s + 32 -----------------
     // (one issuing lane sustains only about one bulk copy per ~270 cycles, so
-    // all 32 lanes issue, each for its own stage)
-    {
-      const int s = lane;
-      for (int64_t i = lane; lane < kIStages && i < n_local; i += kIStages) {
-        const int64_t n = i / kIStages;
-        if (n > 0 && !mbar_wait(empty0 + 8 * s, (uint32_t)((n - 1) & 1), kIWaitLimitNs)) {
-          *abort_flag = 1;
-          break;
-        }
-        if (*abort_flag) break;
-        const int64_t j = b + G * i;
-        const int64_t run = (int64_t)((uint32_t)j / (uint32_t)L);
-        const int l = (int)((uint32_t)j - (uint32_t)run * (uint32_t)L);
-        const int64_t t0 = run * kRun;
-        const int nt = (int)min((int64_t)kRun, (int64_t)a.num_tokens - t0);
-        const uint32_t dst = stage0 + (uint32_t)(s * kIStageBytes);
-        const uint32_t meta = nt == kRun ? (ROPE ? 2u : 1u) * kRun * 8u : 0u;
-        mbar_arrive_expect_tx(full0 + 8 * s, (uint32_t)nt * (2 * kR + 2 * kP) + meta);
-        bulk_g2s(dst, a.kv_c + t0 * a.kvc_ts + (int64_t)l * a.kvc_ls, (uint32_t)nt * 2 * kR,
-                 full0 + 8 * s);
-        bulk_g2s(dst + kOffPe, a.k_pe + t0 * a.kpe_ts + (int64_t)l * a.kpe_ls,
-                 (uint32_t)nt * 2 * kP, full0 + 8 * s);
-        if (nt == kRun) {
-          bulk_g2s(dst + kOffSlot, a.slots + (int64_t)l * a.slot_ls + t0, kRun * 8, full0 + 8 * s);
-          if (ROPE) bulk_g2s(dst + kOffPos, a.positions + t0, kRun * 8, full0 + 8 * s);
-        }
-        fills = n + 1;
+    // all 32 lanes issue, each for its own stages).  A lane takes its items in
+    // order: item i goes to stage i % kIStages (items per CTA < 2^32).
+    for (int64_t i = lane; lane < kIStages && i < n_local;) {
+      const int s = (int)((uint32_t)i % (uint32_t)kIStages);
+      const int64_t n = (int64_t)((uint32_t)i / (uint32_t)kIStages);
+      if (n > 0 && !mbar_wait(empty0 + 8 * s, (uint32_t)((n - 1) & 1), kIWaitLimitNs)) {
+        *abort_flag = 1;
+        break;
       }
+      if (*abort_flag) break;
+      const int64_t j = b + G * i;
+      const int64_t run = (int64_t)((uint32_t)j / (uint32_t)L);
+      const int l = (int)((uint32_t)j - (uint32_t)run * (uint32_t)L);
+      const int64_t t0 = run * kRun;
+      const int nt = (int)min((int64_t)kRun, (int64_t)a.num_tokens - t0);
+      const uint32_t dst = stage0 + (uint32_t)(s * kIStageBytes);
+      const uint32_t meta = nt == kRun ? (ROPE ? 2u : 1u) * kRun * 8u : 0u;
+      mbar_arrive_expect_tx(full0 + 8 * s, (uint32_t)nt * (2 * kR + 2 * kP) + meta);
+      bulk_g2s(dst, a.kv_c + t0 * a.kvc_ts + (int64_t)l * a.kvc_ls, (uint32_t)nt * 2 * kR,
+               full0 + 8 * s);
+      bulk_g2s(dst + kOffPe, a.k_pe + t0 * a.kpe_ts + (int64_t)l * a.kpe_ls,
+               (uint32_t)nt * 2 * kP, full0 + 8 * s);
+      if (nt == kRun) {
+        bulk_g2s(dst + kOffSlot, a.slots + (int64_t)l * a.slot_ls + t0, kRun * 8, full0 + 8 * s);
+        if (ROPE) bulk_g2s(dst + kOffPos, a.positions + t0, kRun * 8, full0 + 8 * s);
+      }
+      if (kIStages <= 32 || s < 32) fills0 = n + 1;
+      else fills1 = n + 1;
+      // next item of this lane: its second stage in this round, else its first
+      // stage in the next round
+      if constexpr (kIStages <= 32) i += kIStages;
+      else i += (s == lane && lane + 32 < kIStages) ? 32 : kIStages - (s - lane);
     }
   } else {
     // ---------------- consumers --------------------------------------------------
     for (int64_t i = warp; i < n_local; i += kIConsumers) {
-      const int s = (int)(i % kIStages);
-      if (!mbar_wait(full0 + 8 * s, (uint32_t)((i / kIStages) & 1), kIWaitLimitNs)) {
+      const int s = (int)((uint32_t)i % (uint32_t)kIStages);
+      if (!mbar_wait(full0 + 8 * s, ((uint32_t)i / (uint32_t)kIStages) & 1u, kIWaitLimitNs)) {
         *abort_flag = 1;
         break;
       }
@@ -433,8 +447,12 @@ __global__ void __launch_bounds__(kIThreads, 1) insert_tma_kernel(const InsertAr
   __syncthreads();
   if (*abort_flag) {
     // Let every copy this CTA issued land before its shared memory is released.
-    if (warp == kIConsumers && fills > 0)
-      (void)mbar_wait(full0 + 8 * lane, (uint32_t)((fills - 1) & 1), kIWaitLimitNs / 8);
+    if (warp == kIConsumers) {
+      if (fills0 > 0)
+        (void)mbar_wait(full0 + 8 * lane, (uint32_t)((fills0 - 1) & 1), kIWaitLimitNs / 8);
+      if (kIStages > 32 && fills1 > 0)
+        (void)mbar_wait(full0 + 8 * (lane + 32), (uint32_t)((fills1 - 1) & 1), kIWaitLimitNs / 8);
+    }
     errbits |= kErrTimeout;
   }
   if (errbits && lane == 0 && a.err) atomicOr(a.err, errbits);
@@ -456,16 +474,17 @@ cudaError_t launch_tma(const InsertArgs& a, const LaunchCfg& cfg) {
   auto kern = insert_tma_kernel<F, NORM, ROPE>;
   static bool configured = false;  // per instance
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kISmem);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Ring<NORM>::kSmem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   const int64_t items = ((int64_t)a.num_tokens + kRun - 1) / kRun * a.num_layers;
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(capped_grid(reinterpret_cast<const void*>(kern), kIThreads,
-                                (items + kIConsumers - 1) / kIConsumers, kISmem));
+                                (items + kIConsumers - 1) / kIConsumers, Ring<NORM>::kSmem));
   lc.blockDim = dim3(kIThreads);
-  lc.dynamicSmemBytes = kISmem;
+  lc.dynamicSmemBytes = Ring<NORM>::kSmem;
   lc.stream = cfg.stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
