@@ -204,29 +204,31 @@ __global__ void __launch_bounds__(kThreads) insert_token_kernel(const InsertArgs
 // 512, k_pe token stride 64 -- the layer-major [L, T, .] buffers), one layer's
 // run of kRun consecutive tokens is contiguous.  A work item is such a run: a
 // producer warp streams its kv_c rows, k_pe rows, slots and positions into a
-// ring of 32 or 48 shared-memory stages (Ring below) with cp.async.bulk
+// ring of 46 shared-memory stages (Ring below) with cp.async.bulk
 // (byte-counted on a per-stage mbarrier; lane s of the producer fills stages s
-// and s + 32), and 16 consumer
-// warps process the rows from shared memory (the
+// and s + 32), and 23 consumer warps process the rows from shared memory (the
 // rotary cos/sin of the item's rows are loaded together, the layer's gamma once
 // per item).  Each consumer owns the stages s == warp (mod kIConsumers) and
 // takes their fills in order, so no parity wait can alias an older phase.
+// A consumer loads its item's rows into registers and hands the stage back
+// before computing them, so the producer refills it meanwhile.
 constexpr int kRun = 4;
-constexpr int kILP = 2;  // rows of an item processed in lockstep
-constexpr int kIConsumers = 16;
+constexpr int kILP = 1;  // rows of an item processed in lockstep
+constexpr int kIConsumers = 23;
 constexpr int kIThreads = (kIConsumers + 1) * 32;
 constexpr int kOffPe = kRun * 2 * kR;              // k_pe rows after the kv_c rows
 constexpr int kOffSlot = kOffPe + kRun * 2 * kP;   // then the slots
 constexpr int kOffPos = kOffSlot + kRun * 8;       // then the positions
 constexpr int kIStageBytes = kOffPos + kRun * 8;   // 4672
 constexpr int kMaxLayers = 128;
-// The ring: 2 stages per consumer (32, one per producer lane) with RMSNorm,
-// whose consumers are compute-bound, and 3 (48; producer lanes 0-15 own two)
-// without, where a deeper ring keeps more copies in flight (measured: 102 vs
-// 112 us raw, 143 vs 137 us with RMSNorm + RoPE, 65536 tokens x 5 layers).
+// The ring: 2 stages per consumer, 46 in all (producer lanes 0-13 own two).
+// 23 consumers of one row at a time (77 registers: 6 warps per SM
+// sub-partition) beat 16 consumers of two rows in lockstep (91 registers):
+// 130.5 vs 137 us with RMSNorm + RoPE and 99.5 vs 101 us raw (65536 tokens x
+// 5 layers); one stage per consumer starves them (174-182 us).
 template <bool NORM>
 struct Ring {
-  static constexpr int kStages = kIConsumers * (NORM ? 2 : 3);
+  static constexpr int kStages = kIConsumers * 2;
   static constexpr int kOffBars = kStages * kIStageBytes;
   static constexpr int kOffLayers = kOffBars + 2 * kStages * 8 + 16;
   static constexpr int kSmem = kOffLayers + kMaxLayers * (8 + 4);
