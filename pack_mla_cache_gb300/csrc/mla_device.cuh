@@ -15,7 +15,7 @@ namespace mla {
 enum Fmt : int { kBF16 = 0, kE4M3 = 1, kE5M2 = 2, kF16 = 3 };
 
 // Whether a format is a 16-bit float (bf16 or fp16).
-constexpr bool is16(int f) { return f == kBF16 || f == kF16; }
+__host__ __device__ constexpr bool is16(int f) { return f == kBF16 || f == kF16; }
 
 constexpr uint32_t kErrSlotOOB = 1u;
 constexpr uint32_t kErrBlockOOB = 2u;
