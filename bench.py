@@ -676,6 +676,62 @@ def run_profile_case(name: str, launches: int, tokens: int | None = None,
     return 0
 
 
+def run_small_batch() -> int:
+    """The small-batch inserts, each timed over 200 calls replayed from one CUDA
+    graph (one JSON line each):
+      * L=1, T=64, bf16 cache of 16 blocks x 64 x 576, raw insert;
+      * L=5, T in {1, 2, 4, 8}, e4m3 caches of 64 blocks x 64 x 576, one shared
+        mapping: one grouped call against five single-layer calls of the same
+        library (the comparison "PR #55356 [Kimi Perf] Group fp8 mla cache
+        insertion" makes for its small-batch speedup)."""
+    import torch
+    from pack_mla_cache_gb300 import ops
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = torch.device("cuda")
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
+    stream = torch.cuda.Stream()
+    calls = 200
+
+    def timed(fn):
+        gr = graph_of(lambda: [fn() for _ in range(calls)], stream)
+        return min(time_graph(gr, stream, 3) for _ in range(5)) / calls * 1e3  # us per call
+
+    # L=1, T=64 raw bf16
+    kv_c = torch.randn((1, 64, 512), generator=g, device=dev).to(torch.bfloat16)
+    k_pe = torch.randn((1, 64, 64), generator=g, device=dev).to(torch.bfloat16)
+    cache = torch.zeros(16 * 64 * ENTRY, dtype=torch.bfloat16, device=dev)
+    ptrs = torch.tensor([cache.data_ptr()], dtype=torch.int64, device=dev)
+    slots = torch.randperm(1024, generator=g, device=dev)[:64]
+    us = timed(lambda: ops.mla_cache_insert_grouped(kv_c, k_pe, slots, ptrs, None, 0, 16, 64,
+                                                    64 * ENTRY, ENTRY))
+    print(json.dumps({"small_batch": "L1_T64_bf16_raw", "us_per_call": us,
+                      "tokens_layers_per_s": 64 / (us * 1e-6),
+                      "bytes_per_call": 64 * (1152 + 8 + 1152)}), flush=True)
+    # L=5, T=1..8 e4m3, grouped vs per layer
+    L = 5
+    caches = [torch.zeros(64 * 64 * ENTRY, dtype=torch.uint8, device=dev) for _ in range(L)]
+    ptrs = torch.tensor([c.data_ptr() for c in caches], dtype=torch.int64, device=dev)
+    scales = torch.rand(L, generator=g, device=dev) * 0.015 + 0.005
+    for T in (1, 2, 4, 8):
+        kv_c = torch.randn((L, T, 512), generator=g, device=dev).to(torch.bfloat16)
+        k_pe = torch.randn((L, T, 64), generator=g, device=dev).to(torch.bfloat16)
+        slots = torch.randperm(4096, generator=g, device=dev)[:T]
+        grouped = timed(lambda: ops.mla_cache_insert_grouped(kv_c, k_pe, slots, ptrs, scales, 1,
+                                                             64, 64, 64 * ENTRY, ENTRY))
+
+        def per_layer():
+            for l in range(L):
+                ops.mla_cache_insert_grouped(kv_c[l:l + 1], k_pe[l:l + 1], slots, ptrs[l:l + 1],
+                                             scales[l:l + 1], 1, 64, 64, 64 * ENTRY, ENTRY)
+        five = timed(per_layer)
+        print(json.dumps({"small_batch": f"L5_T{T}_e4m3", "grouped_us": grouped,
+                          "five_single_layer_us": five, "speedup": five / grouped,
+                          "tokens_layers_per_s": L * T / (grouped * 1e-6)}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -683,11 +739,15 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["mine", "reference"], default="mine")
     ap.add_argument("--profile-case", default=None,
-                    help="run a few launches of one kernel (insert, insert_raw, insert_plain, gather, pack, pack_bf16)")
+                    help="run a few launches of one kernel (see run_profile_case)")
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--tokens", type=int, default=None, help="tokens of the profile case")
     ap.add_argument("--graph", action="store_true", help="replay the profile case's launches from a CUDA graph")
+    ap.add_argument("--small-batch", action="store_true",
+                    help="time the small-batch inserts (grouped vs five single-layer calls)")
     args = ap.parse_args()
+    if args.small_batch:
+        return run_small_batch()
     if args.profile_case:
         return run_profile_case(args.profile_case, args.launches, args.tokens, args.graph)
     if args.warmup < 3:
