@@ -683,11 +683,15 @@ def run_small_batch() -> int:
       * L=5, T in {1, 2, 4, 8}, e4m3 caches of 64 blocks x 64 x 576, one shared
         mapping: one grouped call against five single-layer calls of the same
         library (the comparison "PR #55356 [Kimi Perf] Group fp8 mla cache
-        insertion" makes for its small-batch speedup)."""
+        insertion" makes for its small-batch speedup);
+      * L=5, T=4096 with RMSNorm + RoPE, e4m3 / e5m2, shared / per-layer
+        mapping, with one input set (L2-resident) and 6 rotating sets."""
     import torch
     from pack_mla_cache_gb300 import ops
+    from pack_mla_cache_gb300 import workloads as Wl
     import __graft_entry__
     __graft_entry__.build()
+    W_MAX_POSITION = lambda: Wl.MAX_POSITION  # noqa: E731
     dev = torch.device("cuda")
     g = torch.Generator(device="cuda")
     g.manual_seed(0)
@@ -729,6 +733,45 @@ def run_small_batch() -> int:
         print(json.dumps({"small_batch": f"L5_T{T}_e4m3", "grouped_us": grouped,
                           "five_single_layer_us": five, "speedup": five / grouped,
                           "tokens_layers_per_s": L * T / (grouped * 1e-6)}), flush=True)
+    # L=5, T=4096, RMSNorm + RoPE into 512-block caches: e4m3 / e5m2 x shared / per-layer
+    # mapping; one input and cache set (L2-resident) and 6 rotating sets (219 MB > L2)
+    T, NB = 4096, 512
+    table = torch.empty((W_MAX_POSITION(), 64), dtype=torch.float32, device=dev)
+    ops.mla_rope_cos_sin_cache(table, 1e4)
+    gamma = (1 + 0.1 * torch.randn((L, 512), generator=g, device=dev)).to(torch.bfloat16)
+
+    def make_set(shared):
+        kv_c = torch.randn((L, T, 512), generator=g, device=dev).to(torch.bfloat16)
+        k_pe = torch.randn((L, T, 64), generator=g, device=dev).to(torch.bfloat16)
+        rows = 1 if shared else L
+        sl = torch.stack([torch.randperm(NB * 64, generator=g, device=dev)[:T] for _ in range(rows)])
+        sl = sl[0] if shared else sl
+        pos = torch.randint(0, W_MAX_POSITION(), (T,), generator=g, device=dev)
+        cs = [torch.zeros(NB * 64 * ENTRY, dtype=torch.uint8, device=dev) for _ in range(L)]
+        pt = torch.tensor([c.data_ptr() for c in cs], dtype=torch.int64, device=dev)
+        return kv_c, k_pe, sl, pos, cs, pt
+
+    for fmt in (1, 2):
+        for shared in (True, False):
+            sets = [make_set(shared) for _ in range(6)]
+            per_tok = 8 + 256 + (8 if shared else 8 * L)
+            nbytes = T * L * (1152 + 576) + T * per_tok
+
+            def call(st):
+                kv_c, k_pe, sl, pos, _, pt = st
+                ops.mla_cache_insert_grouped(kv_c, k_pe, sl, pt, scales, fmt, NB, 64, 64 * ENTRY,
+                                             ENTRY, gamma=gamma, eps=1e-6, positions=pos,
+                                             cos_sin_cache=table)
+            resident = timed(lambda: call(sets[0]))
+            rot_graph = graph_of(lambda: [call(sets[i % 6]) for i in range(calls)], stream)
+            rotating = min(time_graph(rot_graph, stream, 3) for _ in range(5)) / calls * 1e3
+            print(json.dumps({"small_batch": f"L5_T4096_norm_rope_{'e4m3' if fmt == 1 else 'e5m2'}_"
+                              f"{'shared' if shared else 'per_layer'}_slots",
+                              "bytes_per_call": nbytes,
+                              "l2_resident_us": resident, "l2_resident_gbs": nbytes / resident / 1e3,
+                              "rotating_6_sets_us": rotating,
+                              "rotating_gbs": nbytes / rotating / 1e3}), flush=True)
+            del sets
     return 0
 
 

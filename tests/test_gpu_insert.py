@@ -171,6 +171,29 @@ def test_raw_fp8_insert_large_exact(orc, bulk):
     assert_exact(gpu, ref)
 
 
+def test_maximum_layer_count(orc, bulk):
+    """128 layers (the most one call takes) x 64 tokens with a mapping per
+    layer: 8192 rows, so the bulk-copy shape runs over items of every layer
+    index; bit-exact raw fp8 with a different k_scale per layer."""
+    wl = W.insert_workload(128, 64, 1, num_blocks=2, block_size=64, shared_slots=False, seed=17)
+    gpu, guards, _ = D.gpu_insert(wl)
+    ref, _ = oracle_insert(orc, wl)
+    assert guards
+    assert_exact(gpu, ref)
+
+
+def test_odd_layer_count_with_norm_rope_and_per_layer_slots(orc, bulk):
+    """37 layers x 300 tokens (item index -> (run, layer) with a layer count
+    that divides nothing), RMSNorm + RoPE into a bf16 cache, a mapping per
+    layer: within 1 bf16 ulp."""
+    wl = W.insert_workload(37, 300, 0, num_blocks=5, block_size=64, shared_slots=False,
+                           norm=True, rope=True, seed=18)
+    gpu, guards, _ = D.gpu_insert(wl, cos_sin=D.gpu_rope_table())
+    ref, _ = oracle_insert(orc, wl, orc.rope_cos_sin_cache(W.MAX_POSITION, 64, W.ROPE_BASE))
+    assert guards
+    assert_within_tolerance(gpu, ref, 0)
+
+
 def test_out_of_range_data_is_skipped_and_reported(orc):
     wl = W.insert_workload(2, 8, 1, num_blocks=4, block_size=16, norm=True, rope=True, seed=5)
     wl.slot_mapping = np.array([[0, 1, -1, 64, 2, 3, 4, 5]] * 2, np.int64)
