@@ -556,6 +556,7 @@ def run_profile_case(name: str, launches: int, tokens: int | None = None,
       gather_kv_c    the raw gather of the 512 kv_c columns only
       pack    32768 tokens, 16 heads, fp8 e4m3 out, fp8 k_pe
       pack_bf16  the same with bf16 output and a bf16 k_pe
+      pack_f16   the fp8 pack of an fp16 kv_b_proj output
       pack_paged the fp8 pack reading k_pe from a 4096-block fp8 cache
       norm_rope  65536 tokens x 5 layers of the [T, L, 576] projection, RMSNorm +
                  RoPE into layer-major outputs"""
@@ -606,10 +607,11 @@ def run_profile_case(name: str, launches: int, tokens: int | None = None,
             fn = lambda: ops.mla_context_gather(cache, 1, nb, BS, BS * ENTRY, ENTRY, cols, table,
                                                 cu, st, out, 1)
             nbytes = T * 2 * cols + (T // BS) * 4
-    elif name in ("pack", "pack_bf16"):
+    elif name in ("pack", "pack_bf16", "pack_f16"):
         T = tokens or 32768
         bf = name == "pack_bf16"
-        kvb = torch.randn((T, ROW_STRIDE), generator=g, device=dev).to(torch.bfloat16)
+        kvb = torch.randn((T, ROW_STRIDE), generator=g, device=dev).to(
+            torch.float16 if name == "pack_f16" else torch.bfloat16)
         heads = kvb[:, :HEADS * 256].view(T, HEADS, 256)
         if bf:
             ws = torch.randn((T, ENTRY), generator=g, device=dev).to(torch.bfloat16)
