@@ -550,7 +550,7 @@ def run_profile_case(name: str, launches: int, tokens: int | None = None,
     a few hundred MB on the device), for ncu captures:
       insert  32768 tokens x 5 layers, e4m3, RMSNorm+RoPE, 2048-block caches
       insert_raw the same without RMSNorm / RoPE
-      insert_plain the insert with the bulk-copy pipeline shape disabled
+      insert_plain the insert with the bulk-copy pipeline shape disabled (row per warp)
       gather  262144 context rows from a 4096-block fp8 cache, raw
       gather_scaled  the gather widened to bf16 times a k_scale
       gather_kv_c    the raw gather of the 512 kv_c columns only
@@ -571,7 +571,7 @@ def run_profile_case(name: str, launches: int, tokens: int | None = None,
     if name in ("insert", "insert_raw", "insert_plain"):
         T = tokens or 32768
         raw = name == "insert_raw"
-        ops.mla_set_bulk_copy(name != "insert_plain")
+        ops.mla_set_bulk_copy(0 if name == "insert_plain" else 1)
         kv_c = torch.randn((L_LAYERS, T, 512), generator=g, device=dev).to(torch.bfloat16)
         k_pe = torch.randn((L_LAYERS, T, 64), generator=g, device=dev).to(torch.bfloat16)
         slots = torch.randperm(NB_INSERT * BS, generator=g, device=dev)[:T]

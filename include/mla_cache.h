@@ -97,12 +97,13 @@ const char* mla_version(void);
  * every later launch from this process.  Returns the previous setting. */
 int mla_set_pdl(int enable);
 
-/* Enable (1, the default) or disable (0) the bulk-copy pipeline shape of the
- * grouped insert (shared-memory staging by cp.async.bulk) for every later
- * launch from this process; when disabled, or when a call's layout does not
- * qualify, a plain vectorised shape runs.  Both compute identical results.
- * Returns the previous setting. */
-int mla_set_bulk_copy(int enable);
+/* When the grouped insert uses its bulk-copy pipeline shape (shared-memory
+ * staging by cp.async.bulk) for every later launch from this process:
+ * 1 (the default) for calls of 131072 rows (tokens x layers) or more, 2 for
+ * every call, 0 never.  A call whose layout does not qualify, and every call
+ * the mode leaves out, runs the row-per-warp shape.  Both shapes compute
+ * identical results.  Returns the previous mode (other values set 1). */
+int mla_set_bulk_copy(int mode);
 
 /*
  * Optional pre-processing of the grouped insert ("PR #50585", Source snippets:
@@ -170,7 +171,7 @@ typedef struct {
  * num_layers must be at most 128 (else MLA_ERR_UNSUPPORTED).
  * Valid slots must be distinct within a layer (else the row written last is
  * unspecified).
- * For 4096 or more rows with dense layer-major inputs (token strides 512 and
+ * For 131072 or more rows with dense layer-major inputs (token strides 512 and
  * 64), a 16-byte aligned slot mapping (and positions) and an even
  * slot_layer_stride, the bulk-copy pipeline shape runs (see mla_set_bulk_copy);
  * err_word then also receives MLA_ERRBIT_TIMEOUT if a pipeline wait ever gave

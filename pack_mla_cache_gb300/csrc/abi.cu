@@ -227,7 +227,7 @@ const char* mla_version(void) { return "mla_cache 1.0 sm_103a"; }
 
 int mla_set_pdl(int enable) { return g_pdl.exchange(enable ? 1 : 0); }
 
-int mla_set_bulk_copy(int enable) { return g_bulk.exchange(enable ? 1 : 0); }
+int mla_set_bulk_copy(int mode) { return g_bulk.exchange(mode >= 0 && mode <= 2 ? mode : 1); }
 
 mla_status_t mla_cache_insert_grouped(
     const void* kv_c, int64_t kvc_token_stride, int64_t kvc_layer_stride, const void* k_pe,
@@ -314,7 +314,7 @@ mla_status_t mla_cache_insert_grouped(
     a.max_position = norm_rope->max_position;
   }
   a.err = err_word;
-  a.use_tma = g_bulk.load() != 0;
+  a.bulk_mode = g_bulk.load();
   return launched(mla::launch_insert(a, (int)cache_dtype, norm, rope, cfg_for(stream)),
                   "mla_cache_insert_grouped");
 }

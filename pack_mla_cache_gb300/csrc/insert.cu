@@ -22,12 +22,13 @@
 //   * fp8: a correctly rounded division per element on packed fp32x2 pairs
 //     (one reciprocal per row), then the hardware .satfinite pairwise
 //     converter;
-//   * three launch shapes: small batches run one warp per (token, layer) row
-//     so the few rows spread over the most SMs (latency); large batches of
-//     dense layer-major rows run the bulk-copy pipeline (below); other large
-//     batches (e.g. the [T, L, 576] projection read in place) run one warp per
-//     token over its layers, kLG rows' loads issued before the first is
-//     processed; all loop over a grid capped at the resident-CTA count;
+//   * two launch shapes: one warp per (token, layer) row, rows in token-major
+//     order, for any strides (e.g. the [T, L, 576] projection read in place)
+//     and for every batch below 131072 rows; above that, dense layer-major
+//     rows run the bulk-copy pipeline (below), which only pays once its ring
+//     is full for long (measured: the row shape is as fast or faster up to
+//     32768 tokens x 5 layers with RMSNorm + RoPE, 16384 x 5 raw); both loop
+//     over a grid capped at the resident-CTA count;
 //   * dtype, norm and rope are template parameters: no runtime format branches
 //     in the hot loop.
 #include "mla_device.cuh"
@@ -40,14 +41,13 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kR = 512;  // kv_lora_rank
 constexpr int kP = 64;   // pe_dim
-constexpr int kLG = 4;   // rows of one token loaded together (token-loop shape)
+
+constexpr int kMaxLayers = 128;
 
 struct RowIn {
   uint4 x0, x1;     // kv_c elements [8l, 8l+8) and [256+8l, 256+8l+8)
   uint32_t pe;      // k_pe elements l (low half) and l+32 (high half)
   int64_t slot;
-  int64_t cptr;     // cache base of the row's layer
-  float scale;      // k_scale of the row's layer (fp8 caches)
 };
 
 __device__ __forceinline__ uint32_t ld_u16(const uint8_t* p) {
@@ -67,9 +67,6 @@ __device__ __forceinline__ void load_row(const InsertArgs& a, int64_t t, int l, 
   const uint8_t* pe = a.k_pe + t * a.kpe_ts + (int64_t)l * a.kpe_ls;
   r.pe = ld_u16(pe + lane * 2) | (ld_u16(pe + 64 + lane * 2) << 16);
   r.slot = a.slots[(int64_t)l * a.slot_ls + t];
-  r.cptr = a.cache_ptrs[l];
-  r.scale = 1.0f;
-  if constexpr (F != kBF16) r.scale = a.scales[l];
 }
 
 // Store one finished row: bf16 words y0 / y1 (kv_c) and p (k_pe pair), raw
@@ -98,24 +95,19 @@ __device__ __forceinline__ void write_row_dc(uint8_t* dst, int lane, const uint4
   else write_row_k<F, false>(dst, lane, y0, y1, p, k);
 }
 
-template <int F>
-__device__ __forceinline__ void write_row(uint8_t* dst, int lane, const uint4& y0,
-                                          const uint4& y1, uint32_t p, float scale) {
-  DivConst k{};
-  if constexpr (F != kBF16) k = div_const(scale);
-  write_row_dc<F>(dst, lane, y0, y1, p, k);
-}
-
-// Normalise / rotate / convert one loaded row and store it.  `cs` = (cos, sin)
-// of this lane's rotary pair.  Returns the error bits of a skipped row.
+// Normalise / rotate / convert one loaded row and store it into the cache at
+// `cptr` (its layer's base; `k` its layer's division constants).  `cs` =
+// (cos, sin) of this lane's rotary pair.  Returns the error bits of a skipped
+// row.
 template <int F, bool NORM, bool ROPE>
 __device__ __forceinline__ uint32_t store_row(const InsertArgs& a, int l, int lane, const RowIn& r,
-                                              bool pos_ok, float2 cs) {
+                                              bool pos_ok, float2 cs, int64_t cptr,
+                                              const DivConst& k) {
   const int64_t s = r.slot;
   if (s < 0) return 0;  // padding slot (uniform across the warp)
   if (s >= a.capacity) return kErrSlotOOB;
   if (ROPE && !pos_ok) return kErrPosOOB;
-  if (r.cptr & 15) return kErrMisaligned;
+  if (cptr & 15) return kErrMisaligned;
   int64_t blk, off;
   if (a.bs_shift >= 0) {
     blk = s >> a.bs_shift;
@@ -124,7 +116,7 @@ __device__ __forceinline__ uint32_t store_row(const InsertArgs& a, int l, int la
     blk = s / a.block_size;
     off = s - blk * a.block_size;
   }
-  uint8_t* dst = reinterpret_cast<uint8_t*>(r.cptr) + blk * a.block_stride + off * a.entry_stride;
+  uint8_t* dst = reinterpret_cast<uint8_t*>(cptr) + blk * a.block_stride + off * a.entry_stride;
 
   // kv_c (optionally RMSNorm-ed) as bf16 words
   uint4 y0 = r.x0, y1 = r.x1;
@@ -137,7 +129,7 @@ __device__ __forceinline__ uint32_t store_row(const InsertArgs& a, int l, int la
   uint32_t p = r.pe;
   if constexpr (ROPE) p = rope_pair(r.pe, cs);
 
-  write_row<F>(dst, lane, y0, y1, p, r.scale);
+  write_row_dc<F>(dst, lane, y0, y1, p, k);
   return 0;
 }
 
@@ -152,55 +144,55 @@ __device__ __forceinline__ bool load_rope(const InsertArgs& a, int64_t t, int la
   return true;
 }
 
-// Shape 1: one warp per (token, layer) row, rows in token-major order.
+// Shape 1: one warp per (token, layer) row, rows in token-major order.  For
+// more than a few rows per warp each CTA first puts the layers' cache bases
+// and division constants in shared memory; tiny calls (decode) skip that step,
+// which would sit on their critical path, and load them per row.
+constexpr int64_t kRowPreloadMinRows = 2048;
+
 template <int F, bool NORM, bool ROPE>
 __global__ void __launch_bounds__(kThreads) insert_row_kernel(const InsertArgs a) {
+  __shared__ int64_t s_cptr[kMaxLayers];
+  __shared__ DivConst s_k[F == kBF16 ? 1 : kMaxLayers];
   pdl_trigger();
   pdl_wait();
+  const bool pre = a.num_rows >= kRowPreloadMinRows;  // uniform across the grid
+  if (pre) {
+    for (int l = threadIdx.x; l < a.num_layers; l += kThreads) {
+      s_cptr[l] = a.cache_ptrs[l];
+      if constexpr (F != kBF16) s_k[l] = div_const(a.scales[l]);
+    }
+    __syncthreads();
+  }
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
+  const bool rows32 = a.num_rows < (int64_t(1) << 32);
   uint32_t errbits = 0;
   for (int64_t r = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5; r < a.num_rows;
        r += nwarps) {
-    const int64_t t = r / a.num_layers;
-    const int l = (int)(r - t * a.num_layers);
+    int64_t t;
+    int l;
+    if (rows32) {
+      const uint32_t tu = (uint32_t)r / (uint32_t)a.num_layers;
+      t = tu;
+      l = (int)((uint32_t)r - tu * (uint32_t)a.num_layers);
+    } else {
+      t = r / a.num_layers;
+      l = (int)(r - t * a.num_layers);
+    }
     RowIn in;
     load_row<F, ROPE>(a, t, l, lane, in);
     float2 cs;
     const bool pos_ok = load_rope<ROPE>(a, t, lane, cs);
-    errbits |= store_row<F, NORM, ROPE>(a, l, lane, in, pos_ok, cs);
+    DivConst k{};
+    if constexpr (F != kBF16) k = pre ? s_k[l] : div_const(a.scales[l]);
+    const int64_t cptr = pre ? s_cptr[l] : a.cache_ptrs[l];
+    errbits |= store_row<F, NORM, ROPE>(a, l, lane, in, pos_ok, cs, cptr, k);
   }
   if (errbits && lane == 0 && a.err) atomicOr(a.err, errbits);
 }
 
-// Shape 2: one warp per token, its layers kLG rows at a time.
-template <int F, bool NORM, bool ROPE>
-__global__ void __launch_bounds__(kThreads) insert_token_kernel(const InsertArgs a) {
-  pdl_trigger();
-  pdl_wait();
-  const int lane = threadIdx.x & 31;
-  const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
-  uint32_t errbits = 0;
-  for (int64_t t = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5; t < a.num_tokens;
-       t += nwarps) {
-    float2 cs;
-    const bool pos_ok = load_rope<ROPE>(a, t, lane, cs);
-    for (int l0 = 0; l0 < a.num_layers; l0 += kLG) {
-      RowIn in[kLG];
-#pragma unroll
-      for (int k = 0; k < kLG; ++k) {
-        if (l0 + k < a.num_layers) load_row<F, ROPE>(a, t, l0 + k, lane, in[k]);
-        else in[k].slot = -1;
-      }
-#pragma unroll
-      for (int k = 0; k < kLG; ++k)
-        errbits |= store_row<F, NORM, ROPE>(a, l0 + k, lane, in[k], pos_ok, cs);
-    }
-  }
-  if (errbits && lane == 0 && a.err) atomicOr(a.err, errbits);
-}
-
-// Shape 3 (bulk-copy pipeline): for dense per-layer rows (kv_c token stride
+// Shape 2 (bulk-copy pipeline): for dense per-layer rows (kv_c token stride
 // 512, k_pe token stride 64 -- the layer-major [L, T, .] buffers), one layer's
 // run of kRun consecutive tokens is contiguous.  A work item is such a run: a
 // producer warp streams its kv_c rows, k_pe rows, slots and positions into a
@@ -220,7 +212,6 @@ constexpr int kOffPe = kRun * 2 * kR;              // k_pe rows after the kv_c r
 constexpr int kOffSlot = kOffPe + kRun * 2 * kP;   // then the slots
 constexpr int kOffPos = kOffSlot + kRun * 8;       // then the positions
 constexpr int kIStageBytes = kOffPos + kRun * 8;   // 4672
-constexpr int kMaxLayers = 128;
 // The ring: 2 stages per consumer, 46 in all (producer lanes 0-13 own two).
 // 23 consumers of one row at a time (77 registers: 6 warps per SM
 // sub-partition) beat 16 consumers of two rows in lockstep (91 registers):
@@ -465,13 +456,13 @@ __global__ void __launch_bounds__(kIThreads, 1) insert_tma_kernel(const InsertAr
 // The bulk-copy shape needs dense per-layer token rows and 16-byte aligned
 // slot / position runs.
 bool insert_tma_layout(const InsertArgs& a, bool rope) {
-  return a.use_tma && a.kvc_ts == 2 * kR && a.kpe_ts == 2 * kP && a.num_layers <= kMaxLayers &&
+  return a.kvc_ts == 2 * kR && a.kpe_ts == 2 * kP && a.num_layers <= kMaxLayers &&
          (reinterpret_cast<uintptr_t>(a.slots) & 15) == 0 && ((a.slot_ls * 8) & 15) == 0 &&
          (!rope || (reinterpret_cast<uintptr_t>(a.positions) & 15) == 0);
 }
 
-// Below this many rows the row-per-warp shape wins (more SMs on few rows).
-constexpr int64_t kTokenShapeMinRows = 4096;
+// From this many rows the bulk-copy shape runs by default.
+constexpr int64_t kBulkMinRows = 131072;
 
 template <int F, bool NORM, bool ROPE>
 cudaError_t launch_tma(const InsertArgs& a, const LaunchCfg& cfg) {
@@ -500,15 +491,12 @@ cudaError_t launch_tma(const InsertArgs& a, const LaunchCfg& cfg) {
 
 template <int F, bool NORM, bool ROPE>
 cudaError_t launch_t(const InsertArgs& a, const LaunchCfg& cfg) {
-  if (a.num_rows >= kTokenShapeMinRows && insert_tma_layout(a, ROPE))
-    return launch_tma<F, NORM, ROPE>(a, cfg);
-  const bool token_shape = a.num_rows >= kTokenShapeMinRows;
-  const void* kern = token_shape ? reinterpret_cast<const void*>(insert_token_kernel<F, NORM, ROPE>)
-                                 : reinterpret_cast<const void*>(insert_row_kernel<F, NORM, ROPE>);
-  const int64_t warps = token_shape ? a.num_tokens : a.num_rows;
-  const int64_t ctas = (warps + kThreads / 32 - 1) / (kThreads / 32);
+  const bool bulk = a.bulk_mode == 2 || (a.bulk_mode == 1 && a.num_rows >= kBulkMinRows);
+  if (bulk && insert_tma_layout(a, ROPE)) return launch_tma<F, NORM, ROPE>(a, cfg);
+  auto kern = insert_row_kernel<F, NORM, ROPE>;
+  const int64_t ctas = (a.num_rows + kThreads / 32 - 1) / (kThreads / 32);
   cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3(capped_grid(kern, kThreads, ctas));
+  lc.gridDim = dim3(capped_grid(reinterpret_cast<const void*>(kern), kThreads, ctas));
   lc.blockDim = dim3(kThreads);
   lc.stream = cfg.stream;
   cudaLaunchAttribute attr[1];
@@ -516,8 +504,7 @@ cudaError_t launch_t(const InsertArgs& a, const LaunchCfg& cfg) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = cfg.pdl ? 1 : 0;
-  if (token_shape) return cudaLaunchKernelEx(&lc, insert_token_kernel<F, NORM, ROPE>, a);
-  return cudaLaunchKernelEx(&lc, insert_row_kernel<F, NORM, ROPE>, a);
+  return cudaLaunchKernelEx(&lc, kern, a);
 }
 
 template <int F>

@@ -30,7 +30,7 @@ struct InsertArgs {
   const float* cos_sin;
   int64_t max_position;
   uint32_t* err;
-  bool use_tma;  // allow the bulk-copy pipeline shape
+  int bulk_mode;  // bulk-copy pipeline shape: 0 never, 1 large calls, 2 always
 };
 
 // A paged cache and the chunk's sequences: chunk token i of sequence s

@@ -133,8 +133,10 @@ def mla_set_pdl(enable: bool) -> bool:
     return bool(lib().mla_set_pdl(1 if enable else 0))
 
 
-def mla_set_bulk_copy(enable: bool) -> bool:
-    return bool(lib().mla_set_bulk_copy(1 if enable else 0))
+def mla_set_bulk_copy(mode: int) -> int:
+    """0 never, 1 large calls (default), 2 every call whose layout qualifies;
+    returns the previous mode."""
+    return int(lib().mla_set_bulk_copy(int(mode)))
 
 
 def mla_cache_insert_grouped(kv_c, k_pe, slot_mapping, kv_cache_ptrs, kv_scales, cache_dtype,

@@ -23,10 +23,11 @@ def orc():
     return oracle
 
 
-@pytest.fixture(params=[True, False], ids=["bulk", "plain"])
+@pytest.fixture(params=[2, 0], ids=["bulk", "plain"])
 def bulk(request):
-    """Run a GPU test with the bulk-copy pipeline variants allowed, then with
-    only the plain variants (both must give identical results)."""
+    """Run a GPU test with the insert's bulk-copy pipeline shape for every
+    call whose layout qualifies, then with the row-per-warp shape only (both
+    must give identical results)."""
     from pack_mla_cache_gb300 import build, ops
 
     build.build()

@@ -65,9 +65,10 @@ def test_pdl_and_bulk_copy_toggles(L):
     prev = ops.mla_set_pdl(False)
     assert ops.mla_set_pdl(True) is False
     ops.mla_set_pdl(prev)
-    prev = ops.mla_set_bulk_copy(False)
-    assert ops.mla_set_bulk_copy(True) is False
-    ops.mla_set_bulk_copy(prev)
+    prev = ops.mla_set_bulk_copy(0)
+    assert ops.mla_set_bulk_copy(2) == 0
+    assert ops.mla_set_bulk_copy(7) == 2      # out of range sets the default
+    assert ops.mla_set_bulk_copy(prev) == 1
 
 
 def insert(L, **kw):

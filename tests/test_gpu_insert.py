@@ -106,7 +106,7 @@ def test_fp8_conversion_exhaustive_over_bf16(orc, dtype, scale):
 @pytest.mark.parametrize("dtype", [1, 2])
 def test_fp8_conversion_exhaustive_through_every_shape(orc, bulk, dtype):
     """All 2^16 bf16 patterns tiled over 4096 tokens (the bulk-copy shape when
-    allowed, else the token-loop shape): bit-exact, including zeros of both
+    forced, else the row-per-warp shape): bit-exact, including zeros of both
     signs, subnormals, values whose quotient overflows, infinities and NaNs."""
     wl = W.insert_workload(1, 4096, dtype, num_blocks=64, block_size=64, seed=16)
     pats = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
@@ -133,8 +133,8 @@ def test_ragged_non_power_of_two_blocks_and_large_rows(orc):
 @pytest.mark.parametrize("T", [257, 1000])
 def test_dspark_projection_layout_input(orc, T):
     """kv_c / k_pe read straight from a [T, L, 576] projection output (no
-    permute().contiguous()), as strided views: the row-per-warp shape below
-    4096 rows, the token-loop shape above."""
+    permute().contiguous()), as strided views (the row-per-warp shape, the only
+    one that takes these strides)."""
     wl = W.insert_workload(5, T, 1, num_blocks=16, block_size=64, seed=12, norm=True, rope=True)
     T, L = wl.num_tokens, wl.num_layers
     proj = np.concatenate([wl.kv_c, wl.k_pe], axis=2).transpose(1, 0, 2).copy()  # [T, L, 576]
