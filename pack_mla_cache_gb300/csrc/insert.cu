@@ -31,6 +31,8 @@
 //     over a grid capped at the resident-CTA count;
 //   * dtype, norm and rope are template parameters: no runtime format branches
 //     in the hot loop.
+#include <atomic>
+
 #include "mla_device.cuh"
 #include "mla_internal.h"
 #include "norm_rope.cuh"
@@ -467,12 +469,17 @@ constexpr int64_t kBulkMinRows = 131072;
 template <int F, bool NORM, bool ROPE>
 cudaError_t launch_tma(const InsertArgs& a, const LaunchCfg& cfg) {
   auto kern = insert_tma_kernel<F, NORM, ROPE>;
-  static bool configured = false;  // per instance
-  if (!configured) {
+  // the shared-memory opt-in is a per-device attribute: set once per device
+  // (devices 0-63; others set it on every launch)
+  static std::atomic<uint64_t> configured{0};  // per instance
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaGetLastError();
+  const uint64_t bit = dev < 64 ? uint64_t(1) << dev : 0;
+  if (!bit || !(configured.load(std::memory_order_acquire) & bit)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Ring<NORM>::kSmem);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured.fetch_or(bit, std::memory_order_release);
   }
   const int64_t items = ((int64_t)a.num_tokens + kRun - 1) / kRun * a.num_layers;
   cudaLaunchConfig_t lc = {};
