@@ -46,6 +46,7 @@ B_INSERT_ROW = 1152 + 576           # per (token, layer)
 B_INSERT_TOK = 8 + 8 + 256          # slot, position, cos/sin per token
 B_GATHER_TOK = 576 + 576            # fp8 row read + raw write
 B_PACK_TOK = HEADS * 256 * 2 + 64 + HEADS * 192 + HEADS * 128  # 13376
+B_PACK_TOK_BF16 = HEADS * 256 * 2 + 128 + 2 * (HEADS * 192 + HEADS * 128)  # 18496
 
 METRIC = "grouped MLA insert & context K/V pack: HBM GB/s (% of peak), tokens·layers/s"
 WORKLOAD = ("grouped 5-layer fp8 e4m3 insert of 65536 tokens with RMSNorm+RoPE into caches of "
@@ -687,7 +688,9 @@ def run_small_batch() -> int:
         library (the comparison "PR #55356 [Kimi Perf] Group fp8 mla cache
         insertion" makes for its small-batch speedup);
       * L=5, T=4096 with RMSNorm + RoPE, e4m3 / e5m2, shared / per-layer
-        mapping, with one input set (L2-resident) and 6 rotating sets."""
+        mapping, with one input set (L2-resident) and 6 rotating sets;
+      * 32768 context tokens in 4 chunks of 8192: gather + pack per chunk,
+        fp8 e4m3 and bf16 output."""
     import torch
     from pack_mla_cache_gb300 import ops
     from pack_mla_cache_gb300 import workloads as Wl
@@ -774,6 +777,40 @@ def run_small_batch() -> int:
                               "rotating_6_sets_us": rotating,
                               "rotating_gbs": nbytes / rotating / 1e3}), flush=True)
             del sets
+    # cfg 4: one sequence of 32768 context tokens in 4 chunks of 8192 from a 1024-block fp8
+    # cache; per chunk a gather then a pack, fp8 e4m3 out (raw fp8 k_pe) and bf16 out (the
+    # gather widens to bf16 for a bf16 kv_b_proj)
+    C, NC, NBC = 8192, 4, 1024
+    ctx = torch.randint(0, 126, (NBC * 64 * ENTRY,), generator=g, device=dev,
+                        dtype=torch.int32).to(torch.uint8)
+    btab = torch.randperm(NBC, generator=g, device=dev)[:NC * C // 64].to(torch.int32)[None, :].contiguous()
+    cu = torch.tensor([0, C], dtype=torch.int32, device=dev)
+    starts = [torch.tensor([c * C], dtype=torch.int32, device=dev) for c in range(NC)]
+    kvbs = [torch.randn((C, ROW_STRIDE), generator=g, device=dev).to(torch.bfloat16)
+            for _ in range(NC)]
+    sc = torch.tensor([OUT_SCALE], dtype=torch.float32, device=dev)
+    for out in ("e4m3", "bf16"):
+        bf = out == "bf16"
+        ws = torch.empty((C, ENTRY), dtype=torch.bfloat16 if bf else torch.uint8, device=dev)
+        odt = torch.bfloat16 if bf else torch.uint8
+        keys = [torch.empty((C, HEADS, 192), dtype=odt, device=dev) for _ in range(NC)]
+        vs = [torch.empty((C, HEADS, 128), dtype=odt, device=dev) for _ in range(NC)]
+
+        def chunks():
+            for c in range(NC):
+                ops.mla_context_gather(ctx, 1, NBC, 64, 64 * ENTRY, ENTRY, ENTRY, btab, cu,
+                                       starts[c], ws, 0 if bf else 1)
+                h = kvbs[c][:, :HEADS * 256].view(C, HEADS, 256)
+                ops.mla_context_kv_pack(h[:, :, :128], h[:, :, 128:], ws[:, 512:], keys[c], vs[c],
+                                        0 if bf else 1, kpe_dtype=0 if bf else 1,
+                                        out_scale=None if bf else sc)
+        gr = graph_of(chunks, stream)
+        ms = min(time_graph(gr, stream, 5) for _ in range(5))
+        per_tok = (576 + (1152 if bf else 576) + 4 / 64 + (B_PACK_TOK_BF16 if bf else B_PACK_TOK))
+        nbytes = NC * C * per_tok
+        print(json.dumps({"small_batch": f"cfg4_32768_context_4x8192_{out}", "us": ms * 1e3,
+                          "bytes": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9,
+                          "context_tokens_per_s": NC * C / (ms * 1e-3)}), flush=True)
     return 0
 
 
