@@ -46,7 +46,7 @@ B_INSERT_ROW = 1152 + 576           # per (token, layer)
 B_INSERT_TOK = 8 + 8 + 256          # slot, position, cos/sin per token
 B_GATHER_TOK = 576 + 576            # fp8 row read + raw write
 B_PACK_TOK = HEADS * 256 * 2 + 64 + HEADS * 192 + HEADS * 128  # 13376
-B_PACK_TOK_BF16 = HEADS * 256 * 2 + 128 + 2 * (HEADS * 192 + HEADS * 128)  # 18496
+B_PACK_TOK_BF16 = HEADS * 256 * 2 + 128 + 2 * (HEADS * 192 + HEADS * 128)  # 18560 (bf16 k_pe)
 
 METRIC = "grouped MLA insert & context K/V pack: HBM GB/s (% of peak), tokens·layers/s"
 WORKLOAD = ("grouped 5-layer fp8 e4m3 insert of 65536 tokens with RMSNorm+RoPE into caches of "
