@@ -10,12 +10,13 @@
 // item 1 and Source snippets: fused_mla_kv_concat /
 // fused_mla_kv_concat_quant_fp8).
 //
-// Design: a work item is one token's group of up to 8 heads (4 KB of k_nope +
-// v), so a 16-head token is two items; one warp per item, its 8 16-byte loads
-// per lane issued before the first store (74 registers, 3 CTAs and 24 warps --
-// 96 KB of loads -- in flight per SM, enough to keep HBM busy; staging the
-// items through shared memory with bulk copies measured slower, 19.8 vs 17.6 us
-// per 8192-token chunk).  The grid is capped at the resident CTAs and loops
+// Design: a work item is one token's group of up to 4 heads (2 KB of k_nope +
+// v), so a 16-head token is four items; one warp per item, its 4 16-byte loads
+// per lane issued before the first store.  Smaller items mean fewer registers,
+// more resident warps and a shorter tail: 19.7 vs 20.2 us per 8192-token chunk
+// in the benchmark's step with 8-head items, 22.1 us with 2-head items;
+// staging the items through shared memory with bulk copies measured slower
+// still (19.8 vs 17.6 us per chunk against the 8-head plain kernel).  The grid is capped at the resident CTAs and loops
 // over items (long contexts never grow the grid); lanes 0-15 write a head's
 // k_nope slice and lanes 16-31 its V slice, 8 elements each, so every warp
 // store is whole sectors; k_pe part (lane % 8) is loaded and converted once
@@ -38,20 +39,20 @@ namespace mla {
 namespace {
 
 constexpr int kNope = 128, kRope = 64, kV = 128, kKey = kNope + kRope;
-constexpr int kGroup = 8;  // heads per work item
+constexpr int kGroup = 4;  // heads per work item
 
 struct Item {
   int64_t t;
   int h0, nh;  // first head and head count of the item
 };
 
-// Item j -> (token, head group).  Item counts stay below 2^32 (tokens are
-// int32 and at most a few groups per token), so 32-bit division suffices; the
-// usual 16-head case (2 groups) is a shift.
-__device__ __forceinline__ Item item_of(int64_t j, int groups, int H) {
+// Item j -> (token, head group).  Item counts stay below 2^32 (checked by the
+// host), so 32-bit division suffices; a power-of-two group count (gshift >= 0,
+// e.g. 4 groups of 16 heads) is a shift.
+__device__ __forceinline__ Item item_of(int64_t j, int groups, int gshift, int H) {
   Item it;
   const uint32_t ju = (uint32_t)j;
-  it.t = groups == 2 ? (int64_t)(ju >> 1) : (int64_t)(ju / (uint32_t)groups);
+  it.t = gshift >= 0 ? (int64_t)(ju >> gshift) : (int64_t)(ju / (uint32_t)groups);
   const int g = (int)(ju - (uint32_t)it.t * (uint32_t)groups);
   it.h0 = g * kGroup;
   it.nh = min(kGroup, H - it.h0);
@@ -93,6 +94,7 @@ __device__ __forceinline__ void pack_plain_items(const PackArgs& a, const DivCon
   constexpr int OE = is16(OF) ? 2 : 1;
   const int lane = threadIdx.x & 31, H = a.num_heads;
   const int groups = (H + kGroup - 1) / kGroup;
+  const int gshift = (groups & (groups - 1)) ? -1 : __ffs(groups) - 1;
   const int64_t n_items = (int64_t)a.num_tokens * groups;
   const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
   const bool has_v = a.vout != nullptr;
@@ -102,7 +104,7 @@ __device__ __forceinline__ void pack_plain_items(const PackArgs& a, const DivCon
   if constexpr (PAGED) sl = load_seq_lanes(a.paged, lane);
   uint32_t errbits = 0;
   for (int64_t j = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5; j < n_items; j += nwarps) {
-    const Item it = item_of(j, groups, H);
+    const Item it = item_of(j, groups, gshift, H);
     const uint8_t* pe;
     if constexpr (PAGED) {
       pe = paged_row(a.paged, sl, lane, it.t, errbits);
