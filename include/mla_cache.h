@@ -270,7 +270,7 @@ mla_status_t mla_context_gather_scaled(
  *   k_pe                [T, rope_dim] with row stride kpe_token_stride, of type
  *                       kpe_dtype (in_dtype, or the cache's fp8).
  *   nope_dim, rope_dim, v_dim  must be 128, 64, 128 (else UNSUPPORTED).
- *   num_heads           any >= 1, with num_tokens * ceil(num_heads / 8) < 2^32.
+ *   num_heads           any >= 1, with num_tokens * ceil(num_heads / 4) < 2^32.
  *   out_dtype           in_dtype, MLA_FP8_E4M3 or MLA_FP8_E5M2.
  *   key_out             contiguous [T, H, nope_dim + rope_dim] of out_dtype.
  *   v_out               contiguous [T, H, v_dim] of out_dtype, or NULL = no V.

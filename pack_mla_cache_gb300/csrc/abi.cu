@@ -398,8 +398,8 @@ mla_status_t pack_impl(const void* k_nope, int64_t kn_token_stride, int64_t kn_h
                        uint32_t* err_word, mla_stream_t stream, const char* what) {
   if (num_tokens < 0) return fail(MLA_ERR_INVALID_ARG, "num_tokens must be >= 0");
   if (num_heads <= 0) return fail(MLA_ERR_INVALID_ARG, "num_heads must be >= 1");
-  if ((int64_t)num_tokens * ((num_heads + 7) / 8) >= (int64_t(1) << 32))
-    return fail(MLA_ERR_UNSUPPORTED, "num_tokens * ceil(num_heads / 8) must be below 2^32");
+  if ((int64_t)num_tokens * ((num_heads + 3) / 4) >= (int64_t(1) << 32))
+    return fail(MLA_ERR_UNSUPPORTED, "num_tokens * ceil(num_heads / 4) must be below 2^32");
   if (!valid_dtype(out_dtype) || !valid_dtype(kpe_dtype) || !valid_dtype(in_dtype))
     return fail(MLA_ERR_INVALID_ARG, "in_dtype / out_dtype / %s must be an mla_dtype_t value",
                 paged ? "cache_dtype" : "kpe_dtype");

@@ -16,8 +16,9 @@
 // more resident warps and a shorter tail: 19.7 vs 20.2 us per 8192-token chunk
 // in the benchmark's step with 8-head items, 22.1 us with 2-head items;
 // staging the items through shared memory with bulk copies measured slower
-// still (19.8 vs 17.6 us per chunk against the 8-head plain kernel).  The grid is capped at the resident CTAs and loops
-// over items (long contexts never grow the grid); lanes 0-15 write a head's
+// still (19.8 vs 17.6 us per chunk against the 8-head plain kernel).  The grid
+// is capped at the resident CTAs and loops over items (long contexts never
+// grow the grid); lanes 0-15 write a head's
 // k_nope slice and lanes 16-31 its V slice, 8 elements each, so every warp
 // store is whole sectors; k_pe part (lane % 8) is loaded and converted once
 // per item; fp8 output uses the exact division by the scale (fast path chosen
@@ -39,7 +40,11 @@ namespace mla {
 namespace {
 
 constexpr int kNope = 128, kRope = 64, kV = 128, kKey = kNope + kRope;
-constexpr int kGroup = 4;  // heads per work item
+// Heads per work item: 4 for the plain pack; 8 for the paged one, whose
+// per-item row lookup is then shared by twice as many heads (76.5 vs 70.3 us
+// for 32768 tokens under the profiler with 4- and 8-head items).
+template <bool PAGED>
+constexpr int group_of() { return PAGED ? 8 : 4; }
 
 struct Item {
   int64_t t;
@@ -49,6 +54,7 @@ struct Item {
 // Item j -> (token, head group).  Item counts stay below 2^32 (checked by the
 // host), so 32-bit division suffices; a power-of-two group count (gshift >= 0,
 // e.g. 4 groups of 16 heads) is a shift.
+template <int kGroup>
 __device__ __forceinline__ Item item_of(int64_t j, int groups, int gshift, int H) {
   Item it;
   const uint32_t ju = (uint32_t)j;
@@ -92,6 +98,7 @@ constexpr int kThreads = 256;
 template <int OF, int KF, int IF, bool FAST, bool PAGED>
 __device__ __forceinline__ void pack_plain_items(const PackArgs& a, const DivConst& k) {
   constexpr int OE = is16(OF) ? 2 : 1;
+  constexpr int kGroup = group_of<PAGED>();
   const int lane = threadIdx.x & 31, H = a.num_heads;
   const int groups = (H + kGroup - 1) / kGroup;
   const int gshift = (groups & (groups - 1)) ? -1 : __ffs(groups) - 1;
@@ -104,7 +111,7 @@ __device__ __forceinline__ void pack_plain_items(const PackArgs& a, const DivCon
   if constexpr (PAGED) sl = load_seq_lanes(a.paged, lane);
   uint32_t errbits = 0;
   for (int64_t j = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5; j < n_items; j += nwarps) {
-    const Item it = item_of(j, groups, gshift, H);
+    const Item it = item_of<kGroup>(j, groups, gshift, H);
     const uint8_t* pe;
     if constexpr (PAGED) {
       pe = paged_row(a.paged, sl, lane, it.t, errbits);
@@ -176,6 +183,7 @@ cudaLaunchConfig_t base_cfg(const LaunchCfg& cfg, cudaLaunchAttribute* attr) {
 template <int OF, int KF, int IF, bool PAGED>
 cudaError_t launch_plain_t(const PackArgs& a, const LaunchCfg& cfg) {
   auto kern = pack_kernel<OF, KF, IF, PAGED>;
+  constexpr int kGroup = group_of<PAGED>();
   const int64_t items = (int64_t)a.num_tokens * ((a.num_heads + kGroup - 1) / kGroup);
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t lc = base_cfg(cfg, attr);

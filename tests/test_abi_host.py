@@ -341,7 +341,7 @@ def pack(L, **kw):
     (dict(idt=3, odt=1, kdt=0), ops.MLA_ERR_UNSUPPORTED),  # bf16 k_pe with fp16 k_nope
     (dict(idt=0, odt=3, kdt=1), ops.MLA_ERR_UNSUPPORTED),  # fp16 output of bf16 input
     (dict(idt=3, odt=3, kdt=3, scale=A), ops.MLA_ERR_INVALID_ARG),
-    (dict(T=1 << 30, H=40), ops.MLA_ERR_UNSUPPORTED),  # 5 * 2^30 work items
+    (dict(T=1 << 30, H=20), ops.MLA_ERR_UNSUPPORTED),  # 5 * 2^30 work items
 ])
 def test_pack_argument_checks(L, kw, status):
     assert pack(L, **kw) == status
