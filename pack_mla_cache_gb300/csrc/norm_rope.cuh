@@ -7,7 +7,8 @@
 // Row layout in a warp: lane l holds kv_c elements [8l, 8l+8) (x0) and
 // [256+8l, 256+8l+8) (x1) and the rotary pair (l, l+32) of k_pe.
 //   * RMSNorm: 16 squares per lane on mixed-precision FMAs (bf16 operands,
-//     fp32 accumulator: no unpacking), a 5-step xor-shuffle sum, a correctly
+//     fp32 accumulator: no unpacking; unpacking into packed fp32x2 FMAs made
+//     the grouped insert 1% slower), a 5-step xor-shuffle sum, a correctly
 //     rounded reciprocal square root; y = (x * gamma, exact in fp32) * rstd,
 //     one fp32 rounding, then bf16 rounding;
 //   * RoPE: each rotated element is a difference of two products with an FMA
@@ -47,12 +48,14 @@ __device__ __forceinline__ float sum_sq16(const uint4& x0, const uint4& x1) {
 }
 
 // y = x * gamma * rstd for this lane's 16 elements (x * gamma is exact in
-// fp32), rounded to bf16.
+// fp32), rounded to bf16.  NEG gives -y instead (the same roundings, since
+// round-to-nearest-even is symmetric) for consumers that start from -y.
+template <bool NEG = false>
 __device__ __forceinline__ void scale16(const uint4& x0, const uint4& x1, const uint4& g0,
                                         const uint4& g1, float rstd, uint4& y0, uint4& y1) {
   const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
   const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-  const uint64_t rstd2 = f2(rstd, rstd);
+  const uint64_t rstd2 = NEG ? f2(-rstd, -rstd) : f2(rstd, rstd);
   uint32_t o[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
