@@ -39,8 +39,15 @@
  *   matching MLA_ERRBIT_* is OR-ed into *err_word when err_word is not NULL.
  * - num_tokens == 0 returns MLA_OK and launches nothing.
  * - Kernels are launched with programmatic dependent launch enabled (each
- *   kernel waits for the previous grid on the stream before touching memory),
- *   so back-to-back calls overlap launch latency; see mla_set_pdl().
+ *   kernel waits for the previous grid on the stream before touching memory
+ *   that grid may write), so back-to-back calls overlap launch latency; see
+ *   mla_set_pdl().  The one exception: the context gather reads its
+ *   block_table, cu_chunk_lens and chunk_starts before that wait.  With PDL on,
+ *   those three arrays must therefore be complete before the call is
+ *   enqueued, or be written by stream work that does not trigger its
+ *   dependents early (a copy, a host write or an ordinary kernel is fine; a
+ *   kernel that executes griddepcontrol.launch_dependents before it has
+ *   written them is not).
  */
 #ifndef MLA_CACHE_H
 #define MLA_CACHE_H
@@ -210,6 +217,8 @@ mla_status_t mla_cache_insert_grouped(
  *   cu_chunk_lens       int32 device [num_seqs + 1], non-decreasing.
  *   chunk_starts        int32 device [num_seqs].
  *   num_tokens          output rows; rows owned by no sequence are untouched.
+ * With PDL on, block_table, cu_chunk_lens and chunk_starts are read before the
+ * kernel waits for the previous grid (see the conventions above).
  */
 mla_status_t mla_context_gather(
     const void* kv_cache, mla_dtype_t cache_dtype, int64_t num_blocks, int32_t block_size,

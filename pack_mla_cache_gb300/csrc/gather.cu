@@ -14,7 +14,10 @@
 // stores); the row lookup (paged.cuh) costs a ballot and one block-table load.
 // A chunk of 8192 rows is latency-bound (sequence table -> block table -> row),
 // so as many warps as rows wins: 3.6 us per 8192-row chunk against 4.9 us with
-// 4 rows per warp; at 262144 rows both run at ~5.9 TB/s.
+// 4 rows per warp; at 262144 rows both run at ~5.9 TB/s.  A warp's first
+// lookup is done before the programmatic-launch wait (the tables are inputs
+// that no kernel here writes), so only the cache row load follows the previous
+// kernel.
 #include "mla_device.cuh"
 #include "mla_internal.h"
 #include "paged.cuh"
@@ -31,24 +34,36 @@ constexpr int kMaxChunks = 3;        // up to 96 x 16 B = 1536-byte rows
 template <int MODE, int OUT, bool SCALED>
 __global__ void __launch_bounds__(kThreads) gather_kernel(const GatherArgs a) {
   pdl_trigger();
-  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
+  uint32_t errbits = 0;
+  // The first rows' lookups read only the sequence and block tables, which no
+  // kernel of this library writes: they run before the wait on the previous
+  // grid, so two of the three dependent loads of a row overlap its tail.
   const SeqLanes sl = load_seq_lanes(a.src, lane);
+  const uint8_t* first[kRows];
+#pragma unroll
+  for (int k = 0; k < kRows; ++k) {
+    const int64_t r = warp * kRows + k;
+    first[k] = r < a.num_tokens ? paged_row(a.src, sl, lane, r, errbits) : nullptr;
+  }
+  pdl_wait();
   uint64_t s2 = 0;
   if constexpr (SCALED) {
     const float sc = *a.dequant_scale;
     s2 = f2(sc, sc);
   }
-  uint32_t errbits = 0;
 
   for (int64_t r0 = warp * kRows; r0 < a.num_tokens; r0 += nwarps * kRows) {
     const uint8_t* src[kRows];
 #pragma unroll
     for (int k = 0; k < kRows; ++k) {
-      src[k] = nullptr;
-      if (r0 + k < a.num_tokens) src[k] = paged_row(a.src, sl, lane, r0 + k, errbits);
+      src[k] = first[k];
+      if (r0 != warp * kRows) {
+        src[k] = nullptr;
+        if (r0 + k < a.num_tokens) src[k] = paged_row(a.src, sl, lane, r0 + k, errbits);
+      }
     }
 
     uint4 v[kRows][kMaxChunks];
