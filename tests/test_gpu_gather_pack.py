@@ -7,9 +7,10 @@ Covers: 32768 context tokens in 4 chunks of 8192 from an fp8 e4m3 cache
 (1024 blocks, random block table), raw and bf16-widened gathers, kv_b_proj
 output [8192, 4160] bf16 packed to fp8 e4m3 (scale 0.01) and to bf16, head
 counts 16 / 3 / 4 (runtime), 0 and ragged token counts, e5m2 output, bf16
-k_pe into fp8, no-V packs, several sequences per gather, bad block ids, the
-16-chunk programmatic-dependent-launch chain, and one 131072-token launch of
-the grid-capped grid-stride loop (sampled).
+k_pe into fp8, no-V packs, several sequences per gather, bad block ids, a
+32768-row gather whose warps loop, tables written by kernels just before each
+gather, the 16-chunk programmatic-dependent-launch chain, and one
+131072-token launch of the grid-capped grid-stride loop (sampled).
 """
 import numpy as np
 import pytest
@@ -87,6 +88,63 @@ def test_gather_many_sequences_and_bad_blocks(orc):
     np.testing.assert_array_equal(g, r)
     assert int(err.item()) == oerr
     assert oerr in (0, ops.MLA_ERRBIT_BLOCK_OOB)
+
+
+def test_gather_one_launch_of_32768_rows_with_bad_blocks(orc):
+    """One raw gather of 32768 rows: more rows than the capped grid has warps
+    (152 SMs x 64), so each warp's first row is looked up before the launch
+    wait and its later rows inside the loop.  A bad block id in the table row
+    of the first rows and one in that of rows the loop reaches: both skip their
+    rows and set the error bit."""
+    pw = W.pack_workload(32768, 8192, num_blocks=1024, seed=11)
+    table = pw.block_table.copy()
+    table[0, 0] = 1024          # rows 0..63: out of range (first lookups)
+    table[0, 500] = -1          # rows 32000..32063: negative (looped rows)
+    cu = np.array([0, 32768], np.int32)
+    st = np.array([0], np.int32)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    g = gpu_gather(pw, dev_cache(pw), table, cu, st, 32768, 1, err=err)
+    r, oerr = oracle_gather(orc, pw, table, cu, st, 32768, 1)
+    assert oerr == ops.MLA_ERRBIT_BLOCK_OOB
+    assert int(err.item()) == oerr
+    np.testing.assert_array_equal(g, r)
+
+
+def test_gather_sees_tables_written_just_before_it(orc):
+    """With programmatic dependent launch on, the gather reads its block table
+    and sequence tables before waiting on the previous grid.  Tables written by
+    ordinary kernels enqueued just before each call on the same stream (they
+    trigger no early launch) are still the ones it reads."""
+    pw = W.pack_workload(16448, 8192, num_blocks=512, seed=12)  # positions up to 16386
+    cache_t = dev_cache(pw)
+    src_table = D.dev(pw.block_table)
+    table_t = torch.zeros_like(src_table)
+    cu_t = torch.zeros(2, dtype=torch.int32, device="cuda")
+    st_t = torch.zeros(1, dtype=torch.int32, device="cuda")
+    outs = torch.zeros((2, 8192, ENTRY), dtype=torch.uint8, device="cuda")
+    prev = ops.mla_set_pdl(True)
+    try:
+        for c in range(2):
+            table_t.zero_()
+            table_t.add_(src_table)
+            cu_t.fill_(8192)
+            cu_t[0].fill_(0)
+            st_t.fill_(c * 8192 + 3)
+            ops.mla_context_gather(cache_t, 1, pw.num_blocks, 64, 64 * ENTRY, ENTRY, ENTRY,
+                                   table_t, cu_t, st_t, outs[c], 1)
+            if c == 0:
+                # scramble the tables after the first call (kernels again)
+                table_t.fill_(-1)
+                st_t.fill_(10 ** 6)
+        torch.cuda.synchronize()
+    finally:
+        ops.mla_set_pdl(prev)
+    for c in range(2):
+        cu = np.array([0, 8192], np.int32)
+        st = np.array([c * 8192 + 3], np.int32)
+        r, err = oracle_gather(orc, pw, pw.block_table, cu, st, 8192, 1)
+        assert err == 0
+        np.testing.assert_array_equal(D.host_u8(outs[c]), r)
 
 
 def test_gather_bf16_cache_raw(orc):
