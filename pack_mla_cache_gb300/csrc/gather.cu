@@ -40,13 +40,15 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const GatherArgs a) {
   uint32_t errbits = 0;
   // The first rows' lookups read only the sequence and block tables, which no
   // kernel of this library writes: they run before the wait on the previous
-  // grid, so two of the three dependent loads of a row overlap its tail.
+  // grid, so two of the three dependent loads of a row overlap its tail.  Each
+  // later lookup is done at the end of the previous iteration (the loop is
+  // rotated), which keeps the register count of the plain loop.
   const SeqLanes sl = load_seq_lanes(a.src, lane);
-  const uint8_t* first[kRows];
+  const uint8_t* src[kRows];
 #pragma unroll
   for (int k = 0; k < kRows; ++k) {
     const int64_t r = warp * kRows + k;
-    first[k] = r < a.num_tokens ? paged_row(a.src, sl, lane, r, errbits) : nullptr;
+    src[k] = r < a.num_tokens ? paged_row(a.src, sl, lane, r, errbits) : nullptr;
   }
   pdl_wait();
   uint64_t s2 = 0;
@@ -55,17 +57,7 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const GatherArgs a) {
     s2 = f2(sc, sc);
   }
 
-  for (int64_t r0 = warp * kRows; r0 < a.num_tokens; r0 += nwarps * kRows) {
-    const uint8_t* src[kRows];
-#pragma unroll
-    for (int k = 0; k < kRows; ++k) {
-      src[k] = first[k];
-      if (r0 != warp * kRows) {
-        src[k] = nullptr;
-        if (r0 + k < a.num_tokens) src[k] = paged_row(a.src, sl, lane, r0 + k, errbits);
-      }
-    }
-
+  for (int64_t r0 = warp * kRows; r0 < a.num_tokens;) {
     uint4 v[kRows][kMaxChunks];
 #pragma unroll
     for (int k = 0; k < kRows; ++k)
@@ -96,6 +88,10 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const GatherArgs a) {
         }
       }
     }
+    r0 += nwarps * kRows;
+#pragma unroll
+    for (int k = 0; k < kRows; ++k)
+      src[k] = r0 + k < a.num_tokens ? paged_row(a.src, sl, lane, r0 + k, errbits) : nullptr;
   }
   errbits = __reduce_or_sync(0xFFFFFFFFu, errbits);
   if (errbits && lane == 0 && a.err) atomicOr(a.err, errbits);
