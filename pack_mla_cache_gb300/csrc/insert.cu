@@ -239,8 +239,9 @@ __global__ void __launch_bounds__(kThreads) insert_row_kernel(const InsertArgs a
 // rotary cos/sin of the item's rows are loaded together, the layer's gamma once
 // per item).  Each consumer owns the stages s == warp (mod kIConsumers) and
 // takes their fills in order, so no parity wait can alias an older phase.
-// A consumer loads its item's rows into registers and hands the stage back
-// before computing them, so the producer refills it meanwhile.
+// A consumer hands the stage back as soon as the item's last row is in
+// registers (before that row is computed), so the producer refills it
+// meanwhile.
 constexpr int kRun = 4;
 constexpr int kILP = 1;  // rows of an item processed in lockstep
 constexpr int kIConsumers = 23;
@@ -250,7 +251,7 @@ constexpr int kOffSlot = kOffPe + kRun * 2 * kP;   // then the slots
 constexpr int kOffPos = kOffSlot + kRun * 8;       // then the positions
 constexpr int kIStageBytes = kOffPos + kRun * 8;   // 4672
 // The ring: 2 stages per consumer, 46 in all (producer lanes 0-13 own two).
-// 23 consumers of one row at a time (77 registers: 6 warps per SM
+// 23 consumers of one row at a time (72 registers: 6 warps per SM
 // sub-partition) beat 16 consumers of two rows in lockstep (91 registers):
 // 130.5 vs 137 us with RMSNorm + RoPE and 99.5 vs 101 us raw (65536 tokens x
 // 5 layers); one stage per consumer starves them (174-182 us), and 24
