@@ -232,12 +232,13 @@ __global__ void __launch_bounds__(kThreads) insert_row_kernel(const InsertArgs a
 // Shape 2 (bulk-copy pipeline): for dense per-layer rows (kv_c token stride
 // 512, k_pe token stride 64 -- the layer-major [L, T, .] buffers), one layer's
 // run of kRun consecutive tokens is contiguous.  A work item is such a run: a
-// producer warp streams its kv_c rows, k_pe rows, slots and positions into a
-// ring of 46 shared-memory stages (Ring below) with cp.async.bulk
-// (byte-counted on a per-stage mbarrier; lane s of the producer fills stages s
-// and s + 32), and 23 consumer warps process the rows from shared memory (the
-// rotary cos/sin of the item's rows are loaded together, the layer's gamma once
-// per item).  Each consumer owns the stages s == warp (mod kIConsumers) and
+// producer warp streams its kv_c and k_pe rows into a ring of 46 shared-memory
+// stages (Ring below) with cp.async.bulk (byte-counted on a per-stage
+// mbarrier; lane s of the producer fills stages s and s + 32), and 23 consumer
+// warps process the rows from shared memory (the item's slots and positions
+// are loaded from global memory while the consumer waits for its stage, the
+// rotary cos/sin of the item's rows together, the layer's gamma once per
+// item).  Each consumer owns the stages s == warp (mod kIConsumers) and
 // takes their fills in order, so no parity wait can alias an older phase.
 // A consumer hands the stage back as soon as the item's last row is in
 // registers (before that row is computed), so the producer refills it
@@ -247,9 +248,7 @@ constexpr int kILP = 1;  // rows of an item processed in lockstep
 constexpr int kIConsumers = 23;
 constexpr int kIThreads = (kIConsumers + 1) * 32;
 constexpr int kOffPe = kRun * 2 * kR;              // k_pe rows after the kv_c rows
-constexpr int kOffSlot = kOffPe + kRun * 2 * kP;   // then the slots
-constexpr int kOffPos = kOffSlot + kRun * 8;       // then the positions
-constexpr int kIStageBytes = kOffPos + kRun * 8;   // 4672
+constexpr int kIStageBytes = kOffPe + kRun * 2 * kP;  // 4608
 // The ring: 2 stages per consumer, 46 in all (producer lanes 0-13 own two).
 // 23 consumers of one row at a time (72 registers: 6 warps per SM
 // sub-partition) beat 16 consumers of two rows in lockstep (91 registers):
@@ -274,27 +273,11 @@ constexpr uint64_t kIWaitLimitNs = 2000000000ull;  // 2 s: a wait that long mean
 // chains to issue from instead of one.
 template <int F, bool NORM, bool ROPE, bool FAST>
 __device__ __forceinline__ uint32_t insert_consume_item(
-    const InsertArgs& a, uint32_t src, const uint8_t* stage, int64_t t0, int nt, int l,
-    int lane, int64_t cptr, const DivConst& k, uint32_t empty_bar) {
+    const InsertArgs& a, uint32_t src, int l, int lane, int64_t cptr, const DivConst& k,
+    uint32_t empty_bar, const int64_t* slot, const int64_t* pos) {
   uint32_t err = 0;
   // the fp8 fast path takes the normalised rows negated (write_row_neg)
   constexpr bool kNeg = NORM && F != kBF16 && FAST;
-  // per-row metadata: from the stage for a full run, from global for the tail
-  int64_t slot[kRun], pos[kRun];
-#pragma unroll
-  for (int r = 0; r < kRun; ++r) {
-    slot[r] = -1;
-    pos[r] = 0;
-    if (r < nt) {
-      if (nt == kRun) {
-        slot[r] = reinterpret_cast<const int64_t*>(stage + kOffSlot)[r];
-        if (ROPE) pos[r] = reinterpret_cast<const int64_t*>(stage + kOffPos)[r];
-      } else {
-        slot[r] = a.slots[(int64_t)l * a.slot_ls + t0 + r];
-        if (ROPE) pos[r] = a.positions[t0 + r];
-      }
-    }
-  }
   // validity and destination of every row (uniform across the warp)
   uint8_t* dst[kRun];
   bool ok[kRun];
@@ -441,16 +424,11 @@ __global__ void __launch_bounds__(kIThreads, 1) insert_tma_kernel(const InsertAr
       const int64_t t0 = run * kRun;
       const int nt = (int)min((int64_t)kRun, (int64_t)a.num_tokens - t0);
       const uint32_t dst = stage0 + (uint32_t)(s * kIStageBytes);
-      const uint32_t meta = nt == kRun ? (ROPE ? 2u : 1u) * kRun * 8u : 0u;
-      mbar_arrive_expect_tx(full0 + 8 * s, (uint32_t)nt * (2 * kR + 2 * kP) + meta);
+      mbar_arrive_expect_tx(full0 + 8 * s, (uint32_t)nt * (2 * kR + 2 * kP));
       bulk_g2s(dst, a.kv_c + t0 * a.kvc_ts + (int64_t)l * a.kvc_ls, (uint32_t)nt * 2 * kR,
                full0 + 8 * s);
       bulk_g2s(dst + kOffPe, a.k_pe + t0 * a.kpe_ts + (int64_t)l * a.kpe_ls,
                (uint32_t)nt * 2 * kP, full0 + 8 * s);
-      if (nt == kRun) {
-        bulk_g2s(dst + kOffSlot, a.slots + (int64_t)l * a.slot_ls + t0, kRun * 8, full0 + 8 * s);
-        if (ROPE) bulk_g2s(dst + kOffPos, a.positions + t0, kRun * 8, full0 + 8 * s);
-      }
       if (kIStages <= 32 || s < 32) fills0 = n + 1;
       else fills1 = n + 1;
       // next item of this lane: its second stage in this round, else its first
@@ -462,25 +440,39 @@ __global__ void __launch_bounds__(kIThreads, 1) insert_tma_kernel(const InsertAr
     // ---------------- consumers --------------------------------------------------
     for (int64_t i = warp; i < n_local; i += kIConsumers) {
       const int s = (int)((uint32_t)i % (uint32_t)kIStages);
-      if (!mbar_wait(full0 + 8 * s, ((uint32_t)i / (uint32_t)kIStages) & 1u, kIWaitLimitNs)) {
-        *abort_flag = 1;
-        break;
-      }
       const int64_t j = b + G * i;
       const int64_t run = (int64_t)((uint32_t)j / (uint32_t)L);
       const int l = (int)((uint32_t)j - (uint32_t)run * (uint32_t)L);
       const int64_t t0 = run * kRun;
       const int nt = (int)min((int64_t)kRun, (int64_t)a.num_tokens - t0);
+      // The item's slots and positions are read from global memory before the
+      // wait on its stage, so their latency overlaps it; bulk-copying them
+      // too doubled the copies per item, and the copy rate, not the bytes,
+      // then held the consumers back (129.6 vs 118.9 us for 65536 tokens x 5
+      // layers).
+      int64_t slot[kRun], pos[kRun];
+#pragma unroll
+      for (int r = 0; r < kRun; ++r) {
+        slot[r] = -1;
+        pos[r] = 0;
+        if (r < nt) {
+          slot[r] = __ldg(a.slots + (int64_t)l * a.slot_ls + t0 + r);
+          if (ROPE) pos[r] = __ldg(a.positions + t0 + r);
+        }
+      }
+      if (!mbar_wait(full0 + 8 * s, ((uint32_t)i / (uint32_t)kIStages) & 1u, kIWaitLimitNs)) {
+        *abort_flag = 1;
+        break;
+      }
       const uint32_t src = stage0 + (uint32_t)(s * kIStageBytes);
-      const uint8_t* stage = smem + (size_t)s * kIStageBytes;
       const DivConst k = div_const(s_scale[l]);
       const int64_t cptr = s_cptr[l];
       if (F == kBF16 || k.fast)
-        errbits |= insert_consume_item<F, NORM, ROPE, true>(a, src, stage, t0, nt, l, lane, cptr,
-                                                            k, empty0 + 8 * s);
+        errbits |= insert_consume_item<F, NORM, ROPE, true>(a, src, l, lane, cptr, k,
+                                                            empty0 + 8 * s, slot, pos);
       else
-        errbits |= insert_consume_item<F, NORM, ROPE, false>(a, src, stage, t0, nt, l, lane, cptr,
-                                                             k, empty0 + 8 * s);
+        errbits |= insert_consume_item<F, NORM, ROPE, false>(a, src, l, lane, cptr, k,
+                                                             empty0 + 8 * s, slot, pos);
     }
   }
   __syncthreads();
@@ -497,12 +489,9 @@ __global__ void __launch_bounds__(kIThreads, 1) insert_tma_kernel(const InsertAr
   if (errbits && lane == 0 && a.err) atomicOr(a.err, errbits);
 }
 
-// The bulk-copy shape needs dense per-layer token rows and 16-byte aligned
-// slot / position runs.
-bool insert_tma_layout(const InsertArgs& a, bool rope) {
-  return a.kvc_ts == 2 * kR && a.kpe_ts == 2 * kP && a.num_layers <= kMaxLayers &&
-         (reinterpret_cast<uintptr_t>(a.slots) & 15) == 0 && ((a.slot_ls * 8) & 15) == 0 &&
-         (!rope || (reinterpret_cast<uintptr_t>(a.positions) & 15) == 0);
+// The bulk-copy shape needs dense per-layer token rows.
+bool insert_tma_layout(const InsertArgs& a) {
+  return a.kvc_ts == 2 * kR && a.kpe_ts == 2 * kP && a.num_layers <= kMaxLayers;
 }
 
 // From this many rows the bulk-copy shape runs by default.
@@ -541,7 +530,7 @@ cudaError_t launch_tma(const InsertArgs& a, const LaunchCfg& cfg) {
 template <int F, bool NORM, bool ROPE>
 cudaError_t launch_t(const InsertArgs& a, const LaunchCfg& cfg) {
   const bool bulk = a.bulk_mode == 2 || (a.bulk_mode == 1 && a.num_rows >= kBulkMinRows);
-  if (bulk && insert_tma_layout(a, ROPE)) return launch_tma<F, NORM, ROPE>(a, cfg);
+  if (bulk && insert_tma_layout(a)) return launch_tma<F, NORM, ROPE>(a, cfg);
   auto kern = insert_row_kernel<F, NORM, ROPE>;
   const int64_t ctas = (a.num_rows + kThreads / 32 - 1) / (kThreads / 32);
   cudaLaunchConfig_t lc = {};
