@@ -106,8 +106,8 @@ int mla_set_pdl(int enable);
 
 /* When the grouped insert uses its bulk-copy pipeline shape (shared-memory
  * staging by cp.async.bulk) for every later launch from this process:
- * 1 (the default) for calls of 131072 rows (tokens x layers) or more, 2 for
- * every call, 0 never.  A call whose layout does not qualify, and every call
+ * 1 (the default) for calls of 131072 rows (tokens x layers) or more, or
+ * 40960 rows or more with RMSNorm, 2 for every call, 0 never.  A call whose layout does not qualify, and every call
  * the mode leaves out, runs the row-per-warp shape.  Both shapes compute
  * identical results.  Returns the previous mode (other values set 1). */
 int mla_set_bulk_copy(int mode);
@@ -178,9 +178,9 @@ typedef struct {
  * num_layers must be at most 128 (else MLA_ERR_UNSUPPORTED).
  * Valid slots must be distinct within a layer (else the row written last is
  * unspecified).
- * For 131072 or more rows with dense layer-major inputs (token strides 512 and
- * 64), a 16-byte aligned slot mapping (and positions) and an even
- * slot_layer_stride, the bulk-copy pipeline shape runs (see mla_set_bulk_copy);
+ * For 131072 or more rows (40960 with RMSNorm) with dense layer-major inputs
+ * (token strides 512 and 64), the bulk-copy pipeline shape runs (see
+ * mla_set_bulk_copy);
  * err_word then also receives MLA_ERRBIT_TIMEOUT if a pipeline wait ever gave
  * up (bounded at 2 s).
  */

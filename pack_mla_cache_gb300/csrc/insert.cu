@@ -24,11 +24,12 @@
 //     converter;
 //   * two launch shapes: one warp per (token, layer) row, rows in token-major
 //     order, for any strides (e.g. the [T, L, 576] projection read in place)
-//     and for every batch below 131072 rows; above that, dense layer-major
-//     rows run the bulk-copy pipeline (below), which only pays once its ring
-//     is full for long (measured: the row shape is as fast or faster up to
-//     32768 tokens x 5 layers with RMSNorm + RoPE, 16384 x 5 raw); both loop
-//     over a grid capped at the resident-CTA count;
+//     and for small batches; from 40960 rows with RMSNorm (131072 without),
+//     dense layer-major rows run the bulk-copy pipeline (below), which only
+//     pays once its ring is full for long (RMSNorm + RoPE, 5 layers, ring vs
+//     rows: 8192 tokens 16.8 vs 19.1 us, 16384 35.6 vs 36.3, 24576 49.9 vs
+//     53.6; raw: 8192 12.7 vs 14.5, 16384 28.6 vs 26.0, 24576 39.7 vs 41.5);
+//     both loop over a grid capped at the resident-CTA count;
 //   * dtype, norm and rope are template parameters: no runtime format branches
 //     in the hot loop.
 #include <atomic>
@@ -494,8 +495,10 @@ bool insert_tma_layout(const InsertArgs& a) {
   return a.kvc_ts == 2 * kR && a.kpe_ts == 2 * kP && a.num_layers <= kMaxLayers;
 }
 
-// From this many rows the bulk-copy shape runs by default.
+// From this many rows the bulk-copy shape runs by default (the RMSNorm
+// variant's heavier rows keep its ring full from a smaller batch).
 constexpr int64_t kBulkMinRows = 131072;
+constexpr int64_t kBulkMinRowsNorm = 40960;
 
 template <int F, bool NORM, bool ROPE>
 cudaError_t launch_tma(const InsertArgs& a, const LaunchCfg& cfg) {
@@ -529,7 +532,8 @@ cudaError_t launch_tma(const InsertArgs& a, const LaunchCfg& cfg) {
 
 template <int F, bool NORM, bool ROPE>
 cudaError_t launch_t(const InsertArgs& a, const LaunchCfg& cfg) {
-  const bool bulk = a.bulk_mode == 2 || (a.bulk_mode == 1 && a.num_rows >= kBulkMinRows);
+  const int64_t min_rows = NORM ? kBulkMinRowsNorm : kBulkMinRows;
+  const bool bulk = a.bulk_mode == 2 || (a.bulk_mode == 1 && a.num_rows >= min_rows);
   if (bulk && insert_tma_layout(a)) return launch_tma<F, NORM, ROPE>(a, cfg);
   auto kern = insert_row_kernel<F, NORM, ROPE>;
   const int64_t ctas = (a.num_rows + kThreads / 32 - 1) / (kThreads / 32);
