@@ -39,6 +39,7 @@ ERR_SLOT_OOB, ERR_BLOCK_OOB, ERR_POS_OOB = 1, 2, 4
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "mla_oracle.c")
+_SPLIT_SRC = os.path.join(_HERE, "mla_oracle_split.c")
 _HDR = os.path.join(_HERE, "mla_oracle.h")
 _OUT_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_OUT_DIR, "libmla_oracle.so")
@@ -51,10 +52,11 @@ GCC_FLAGS = ["-std=c11", "-O2", "-ffp-contract=off", "-fPIC", "-shared", "-Wall"
 def build(force: bool = False) -> str:
     """Compile the oracle with gcc (idempotent; rebuilds when the source is newer)."""
     os.makedirs(_OUT_DIR, exist_ok=True)
-    newest = max(os.path.getmtime(_SRC), os.path.getmtime(_HDR))
+    newest = max(os.path.getmtime(_SRC), os.path.getmtime(_SPLIT_SRC), os.path.getmtime(_HDR))
     if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < newest:
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", *GCC_FLAGS, _SRC, "-o", tmp, "-lm"])
+        subprocess.check_call(["gcc", *GCC_FLAGS, "-pthread", _SRC, _SPLIT_SRC, "-o", tmp,
+                               "-lm"])
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -107,6 +109,14 @@ def lib() -> ctypes.CDLL:
                 "orc_context_kv_pack_paged": (u32, [vp, i64, i64, vp, i64, i64, vp, i32, i64, i32,
                                                     i64, i64, i32, vp, i64, vp, vp, i32, i32, i32,
                                                     i32, i32, i32, vp, vp, i32, f32, i32]),
+                "orc_split_insert_grouped": (u32, [i32, vp, i64, i64, vp, i64, i64, i32, i32, i32,
+                                                   i32, vp, i64, vp, vp, i32, i64, i32, i64, i64,
+                                                   vp, i64, f32, vp, vp, i64]),
+                "orc_split_context_gather": (u32, [i32, vp, i32, i64, i32, i64, i64, i32, vp, i64,
+                                                   vp, vp, i32, i32, vp, i64, i32]),
+                "orc_split_context_kv_pack": (None, [i32, vp, i64, i64, vp, i64, i64, vp, i64, i32,
+                                                     i32, i32, i32, i32, i32, vp, vp, i32, f32,
+                                                     i32]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -364,3 +374,66 @@ def norm_rope_grouped(kv_c_buf, kvc_ts, kvc_ls, k_pe_buf, kpe_ts, kpe_ls, T, L, 
         0 if cos_sin_cache is None else cos_sin_cache.shape[0], _p(out_c), oc_ts, oc_ls,
         _p(out_p), op_ts, op_ls)
     return out_c, out_p, err
+
+
+# ------------------------------------------------------- split over host threads
+def host_threads() -> int:
+    """Host cores this process may run on (the multi-core baseline's thread count)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # not Linux
+        return os.cpu_count() or 1
+
+
+def insert_grouped_split(threads, kv_c, k_pe, slot_mapping, slot_layer_stride, caches, k_scales,
+                         cache_dtype, num_blocks, block_size, block_stride, entry_stride,
+                         gamma=None, eps=1e-6, positions=None, cos_sin_cache=None):
+    """``insert_grouped`` with its tokens split over ``threads`` host threads (the
+    unchanged single-threaded oracle per token range; byte-identical result)."""
+    _chk(kv_c, np.uint16), _chk(k_pe, np.uint16), _chk(slot_mapping, np.int64)
+    L, T, R = kv_c.shape
+    P = k_pe.shape[2]
+    ptrs = (ctypes.c_void_p * L)(*[c.ctypes.data for c in caches])
+    for c in caches:
+        assert c.flags["C_CONTIGUOUS"]
+    if k_scales is not None:
+        k_scales = np.ascontiguousarray(k_scales, dtype=np.float32)
+    if gamma is not None:
+        _chk(gamma, np.uint16)
+    if positions is not None:
+        _chk(positions, np.int64), _chk(cos_sin_cache, np.float32)
+    return lib().orc_split_insert_grouped(
+        int(threads), _p(kv_c), R, T * R, _p(k_pe), P, T * P, T, L, R, P, _p(slot_mapping),
+        slot_layer_stride, ctypes.cast(ptrs, ctypes.c_void_p), _p(k_scales), cache_dtype,
+        num_blocks, block_size, block_stride, entry_stride, _p(gamma),
+        0 if gamma is None else gamma.shape[-1], float(eps), _p(positions), _p(cos_sin_cache),
+        0 if cos_sin_cache is None else cos_sin_cache.shape[0])
+
+
+def context_gather_split(threads, cache, cache_dtype, num_blocks, block_size, block_stride,
+                         entry_stride, entry_dim, block_table, cu_chunk_lens, chunk_starts, out,
+                         out_dtype):
+    """``context_gather`` with its output rows split over ``threads`` host threads."""
+    _chk(block_table, np.int32), _chk(cu_chunk_lens, np.int32), _chk(chunk_starts, np.int32)
+    assert out.flags["C_CONTIGUOUS"] and cache.flags["C_CONTIGUOUS"]
+    S = chunk_starts.shape[0]
+    return lib().orc_split_context_gather(
+        int(threads), _p(cache), cache_dtype, num_blocks, block_size, block_stride, entry_stride,
+        entry_dim, _p(block_table), block_table.shape[1], _p(cu_chunk_lens), _p(chunk_starts), S,
+        out.shape[0], _p(out), out.shape[1], out_dtype)
+
+
+def context_kv_pack_split(threads, k_nope_buf, kn_token_stride, kn_head_stride, v_buf,
+                          v_token_stride, v_head_stride, k_pe_buf, kpe_token_stride, kpe_dtype, T,
+                          H, nope, rope, v_dim, out_dtype, out_scale=1.0, with_v=True,
+                          in_dtype=BF16):
+    """``context_kv_pack`` with its tokens split over ``threads`` host threads."""
+    odt = np.uint16 if out_dtype in (BF16, F16) else np.uint8
+    key = np.empty((T, H, nope + rope), odt)
+    vout = np.empty((T, H, v_dim), odt) if with_v else None
+    lib().orc_split_context_kv_pack(int(threads), _p(k_nope_buf), kn_token_stride,
+                                    kn_head_stride, _p(v_buf), v_token_stride, v_head_stride,
+                                    _p(k_pe_buf), kpe_token_stride, kpe_dtype, T, H, nope, rope,
+                                    v_dim, _p(key), _p(vout), out_dtype, float(out_scale),
+                                    in_dtype)
+    return key, vout

@@ -149,6 +149,36 @@ uint32_t orc_context_kv_pack_paged(
     int32_t num_tokens, int32_t num_heads, int32_t nope_dim, int32_t rope_dim, int32_t v_dim,
     void* key_out, void* v_out, int32_t out_dtype, float out_scale, int32_t in_dtype);
 
+/* ---- the row loops above split over host threads (mla_oracle_split.c) ---
+ * For the multi-core CPU baseline only: each cuts its rows into `threads`
+ * contiguous ranges and runs the unchanged function above on each range in its
+ * own thread; the output is byte-identical to the single-threaded call. */
+uint32_t orc_split_insert_grouped(
+    int32_t threads, const uint16_t* kv_c, int64_t kvc_token_stride, int64_t kvc_layer_stride,
+    const uint16_t* k_pe, int64_t kpe_token_stride, int64_t kpe_layer_stride,
+    int32_t num_tokens, int32_t num_layers, int32_t kv_lora_rank, int32_t pe_dim,
+    const int64_t* slot_mapping, int64_t slot_layer_stride, void* const* caches,
+    const float* k_scales, int32_t cache_dtype, int64_t num_blocks, int32_t block_size,
+    int64_t block_stride, int64_t entry_stride, const uint16_t* gamma,
+    int64_t gamma_layer_stride, float eps, const int64_t* positions,
+    const float* cos_sin_cache, int64_t max_position);
+
+uint32_t orc_split_context_gather(int32_t threads, const void* cache, int32_t cache_dtype,
+                                  int64_t num_blocks, int32_t block_size, int64_t block_stride,
+                                  int64_t entry_stride, int32_t entry_dim,
+                                  const int32_t* block_table, int64_t block_table_stride,
+                                  const int32_t* cu_chunk_lens, const int32_t* chunk_starts,
+                                  int32_t num_seqs, int32_t num_tokens, void* out,
+                                  int64_t out_row_stride, int32_t out_dtype);
+
+void orc_split_context_kv_pack(int32_t threads, const uint16_t* k_nope, int64_t kn_token_stride,
+                               int64_t kn_head_stride, const uint16_t* v, int64_t v_token_stride,
+                               int64_t v_head_stride, const void* k_pe, int64_t kpe_token_stride,
+                               int32_t kpe_dtype, int32_t num_tokens, int32_t num_heads,
+                               int32_t nope_dim, int32_t rope_dim, int32_t v_dim, void* key_out,
+                               void* v_out, int32_t out_dtype, float out_scale,
+                               int32_t in_dtype);
+
 #ifdef __cplusplus
 }
 #endif
