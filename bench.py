@@ -211,12 +211,18 @@ class Workload:
         self.starts = [torch.tensor([c * CHUNK], dtype=torch.int32, device=dev)
                        for c in range(pw.num_chunks)]
         self.h_kvb = [bf16(b) for b in pw.kv_b_proj]
-        self.kvb = [b.to(dev) for b in self.h_kvb]
+        # one contiguous kv_b_proj output, key and V for the whole context; the
+        # chunks are views of them (the one-launch pack reads them whole)
+        self.kvb_all = torch.cat([b.to(dev) for b in self.h_kvb])
+        self.kvb = [self.kvb_all[c * CHUNK:(c + 1) * CHUNK] for c in range(pw.num_chunks)]
         self.ws = torch.empty((CHUNK, ENTRY), dtype=torch.uint8, device=dev)
-        self.key = [torch.empty((CHUNK, HEADS, 192), dtype=torch.uint8, device=dev)
-                    for _ in range(pw.num_chunks)]
-        self.vout = [torch.empty((CHUNK, HEADS, 128), dtype=torch.uint8, device=dev)
-                     for _ in range(pw.num_chunks)]
+        self.key_all = torch.empty((T_CTX, HEADS, 192), dtype=torch.uint8, device=dev)
+        self.vout_all = torch.empty((T_CTX, HEADS, 128), dtype=torch.uint8, device=dev)
+        self.key = [self.key_all[c * CHUNK:(c + 1) * CHUNK] for c in range(pw.num_chunks)]
+        self.vout = [self.vout_all[c * CHUNK:(c + 1) * CHUNK] for c in range(pw.num_chunks)]
+        # the gather tables are uploaded once, before any step: the gathers may
+        # read them before their programmatic-launch wait
+        ops.mla_set_gather_early_tables(True)
         self.out_scale = torch.tensor([OUT_SCALE], dtype=torch.float32, device=dev)
         self.err = torch.zeros(2, dtype=torch.int32, device=dev)
 
@@ -243,6 +249,31 @@ class Workload:
         for c in range(self.pw.num_chunks):
             self.gather(c)
             self.pack(c)
+
+    # the whole context in one launch each (the grid-capped grid-stride loop)
+    def one_launch_setup(self):
+        import torch
+        dev = self.kvb_all.device
+        self.ws_all = torch.empty((T_CTX, ENTRY), dtype=torch.uint8, device=dev)
+        self.ws_all16 = torch.empty((T_CTX, ENTRY), dtype=torch.bfloat16, device=dev)
+        cu = torch.tensor([0, T_CTX], dtype=torch.int32, device=dev)
+        st = torch.tensor([0], dtype=torch.int32, device=dev)
+        for ws, odt in ((self.ws_all, 1), (self.ws_all16, 0)):
+            self.ops.mla_context_gather(self.ctx_cache, 1, NB_CTX, BS, BS * ENTRY, ENTRY, ENTRY,
+                                        self.block_table, cu, st, ws, odt)
+        self.key16 = torch.empty((T_CTX, HEADS, 192), dtype=torch.bfloat16, device=dev)
+        self.v16 = torch.empty((T_CTX, HEADS, 128), dtype=torch.bfloat16, device=dev)
+
+    def pack_one_launch(self, bf16_out=False):
+        heads = self.kvb_all[:, :HEADS * 256].view(T_CTX, HEADS, 256)
+        if bf16_out:
+            self.ops.mla_context_kv_pack(heads[:, :, :128], heads[:, :, 128:],
+                                         self.ws_all16[:, 512:], self.key16, self.v16, 0,
+                                         kpe_dtype=0)
+        else:
+            self.ops.mla_context_kv_pack(heads[:, :, :128], heads[:, :, 128:],
+                                         self.ws_all[:, 512:], self.key_all, self.vout_all, 1,
+                                         kpe_dtype=1, out_scale=self.out_scale)
 
     launches_per_step = 1 + 2 * (T_CTX // CHUNK)
 
@@ -437,6 +468,12 @@ def run(args):
         ms_insert = time_graph(g_ins, stream, reps)
         ms_gather = time_graph(g_gat, stream, reps) / nch
         ms_pack = time_graph(g_pack, stream, reps) / nch
+        # the whole 131072-token context packed by ONE launch (fp8 and bf16 out)
+        w.one_launch_setup()
+        g_one = graph_of(lambda: w.pack_one_launch(False), stream)
+        g_one16 = graph_of(lambda: w.pack_one_launch(True), stream)
+        ms_one = time_graph(g_one, stream, max(3, args.steps // 4))
+        ms_one16 = time_graph(g_one16, stream, max(3, args.steps // 4))
     clocks = clk.summary()
 
     ms = max_over_ranks(ms, world)
@@ -501,7 +538,9 @@ def run(args):
                      "traffic": profile_traffic("pack_fp8_h16")},
         "kernels": {"insert": kline(b_ins_launch, ms_insert),
                     "gather": kline(b_gat_launch, ms_gather),
-                    "pack": kline(b_pack_launch, ms_pack)},
+                    "pack": kline(b_pack_launch, ms_pack),
+                    "pack_one_launch_131072": kline(T_CTX * B_PACK_TOK, ms_one),
+                    "pack_one_launch_131072_bf16": kline(T_CTX * B_PACK_TOK_BF16, ms_one16)},
         "cpu_baseline": cpu,
         "e2e": {"value": job_throughput(sbytes, world, e2e["ms"]), "unit": "GB/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
@@ -708,6 +747,70 @@ def run_profile_case(name: str, launches: int, tokens: int | None = None,
     return 0
 
 
+def host_cost_row(T, kv_c, k_pe, slots, ptrs, scales, graph_us):
+    """Host cost of a decode-size insert without a CUDA graph: wall time per
+    call of 1000 back-to-back calls (then one synchronize), best of 5.
+      api      through the Python binding (argument marshalling included);
+      abi      the C entry point called through ctypes with its arguments
+               built once (what a C caller pays, plus the ctypes call);
+      floor    the same call with num_tokens = 0, which returns after the
+               argument checks that need no CUDA call (ctypes + validation);
+    each for one grouped call and for five single-layer calls, with the
+    per-call device-pointer checks on (default) and off."""
+    import torch
+    from pack_mla_cache_gb300 import ops
+
+    L = kv_c.shape[0]
+    lib = ops.lib()
+    fn = lib.mla_cache_insert_grouped
+    st = torch.cuda.current_stream().cuda_stream
+
+    def args_of(l0, nl, t):
+        return (kv_c[l0].data_ptr(), 512, T * 512, k_pe[l0].data_ptr(), 64, T * 64, t, nl, 512,
+                64, slots.data_ptr(), 0, ptrs[l0:].data_ptr(), scales[l0:].data_ptr(), 1, 64, 64,
+                64 * ENTRY, ENTRY, None, None, st)
+
+    grouped_args = args_of(0, L, T)
+    layer_args = [args_of(l, 1, T) for l in range(L)]
+    floor_args = args_of(0, L, 0)
+
+    def host_us(call, n=1000):
+        for _ in range(50):
+            call()
+        torch.cuda.synchronize()
+        best = float("inf")
+        for _ in range(5):
+            t0 = time.perf_counter()
+            for _ in range(n):
+                call()
+            torch.cuda.synchronize()
+            best = min(best, (time.perf_counter() - t0) / n * 1e6)
+        return best
+
+    def abi_grouped():
+        assert fn(*grouped_args) == 0
+
+    def abi_layers():
+        for a in layer_args:
+            fn(*a)
+
+    row = {"small_batch": f"host_L{L}_T{T}_e4m3", "graph_grouped_us": graph_us,
+           "api_grouped_us": host_us(lambda: ops.mla_cache_insert_grouped(
+               kv_c, k_pe, slots, ptrs, scales, 1, 64, 64, 64 * ENTRY, ENTRY)),
+           "abi_floor_us": host_us(lambda: fn(*floor_args)),
+           "abi_grouped_us": host_us(abi_grouped),
+           "abi_five_single_layer_us": host_us(abi_layers)}
+    prev = ops.mla_set_pointer_checks(False)
+    try:
+        row["abi_grouped_no_ptr_checks_us"] = host_us(abi_grouped)
+        row["abi_five_single_layer_no_ptr_checks_us"] = host_us(abi_layers)
+    finally:
+        ops.mla_set_pointer_checks(prev)
+    row["note"] = ("wall time per call of 1000 back-to-back calls; the kernel itself takes "
+                   "graph_grouped_us")
+    return row
+
+
 def run_small_batch() -> int:
     """The small-batch inserts, each timed over 200 calls replayed from one CUDA
     graph (one JSON line each):
@@ -767,6 +870,7 @@ def run_small_batch() -> int:
         print(json.dumps({"small_batch": f"L5_T{T}_e4m3", "grouped_us": grouped,
                           "five_single_layer_us": five, "speedup": five / grouped,
                           "tokens_layers_per_s": L * T / (grouped * 1e-6)}), flush=True)
+        print(json.dumps(host_cost_row(T, kv_c, k_pe, slots, ptrs, scales, grouped)), flush=True)
     # L=5, T=4096, RMSNorm + RoPE into 512-block caches: e4m3 / e5m2 x shared / per-layer
     # mapping; one input and cache set (L2-resident) and 6 rotating sets (219 MB > L2)
     T, NB = 4096, 512
@@ -810,6 +914,7 @@ def run_small_batch() -> int:
     # cache; per chunk a gather then a pack, fp8 e4m3 out (raw fp8 k_pe) and bf16 out (the
     # gather widens to bf16 for a bf16 kv_b_proj)
     C, NC, NBC = 8192, 4, 1024
+    ops.mla_set_gather_early_tables(True)  # the tables below are uploaded once, up front
     ctx = torch.randint(0, 126, (NBC * 64 * ENTRY,), generator=g, device=dev,
                         dtype=torch.int32).to(torch.uint8)
     btab = torch.randperm(NBC, generator=g, device=dev)[:NC * C // 64].to(torch.int32)[None, :].contiguous()

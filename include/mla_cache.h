@@ -21,10 +21,16 @@
  *   the stream it is given (NULL = the legacy default stream).  Every call
  *   returns as soon as its launch is queued.
  * - Pointers: every data pointer is a DEVICE pointer on the current CUDA
- *   device unless the comment says otherwise.  The small metadata arrays
- *   (per-layer cache pointers, slot mapping, scales, positions, tables) are
- *   checked with cudaPointerGetAttributes; a host pointer there is rejected
- *   with MLA_ERR_INVALID_ARG before any launch.
+ *   device unless the comment says otherwise.  Every pointer argument a kernel
+ *   dereferences (inputs, outputs, per-layer cache pointer array, slot
+ *   mapping, scales, positions, tables) is checked with
+ *   cudaPointerGetAttributes; a host pointer, or device memory of another
+ *   device, is rejected with MLA_ERR_INVALID_ARG before any launch.  These
+ *   checks cost host time on every call (about one CUDA runtime query per
+ *   pointer); a caller that guarantees its pointers can switch them off with
+ *   mla_set_pointer_checks(0).  The per-layer cache bases inside
+ *   kv_cache_ptrs live in device memory and are checked by the kernel only
+ *   for null and alignment (MLA_ERRBIT_MISALIGNED).
  * - Strides and sizes are in ELEMENTS of the named tensor's element type.
  * - Alignment: every row that is read or written must start on a 16-byte
  *   boundary (base pointer and strides), else MLA_ERR_MISALIGNED.  There is no
@@ -39,15 +45,11 @@
  *   matching MLA_ERRBIT_* is OR-ed into *err_word when err_word is not NULL.
  * - num_tokens == 0 returns MLA_OK and launches nothing.
  * - Kernels are launched with programmatic dependent launch enabled (each
- *   kernel waits for the previous grid on the stream before touching memory
- *   that grid may write), so back-to-back calls overlap launch latency; see
- *   mla_set_pdl().  The one exception: the context gather reads its
- *   block_table, cu_chunk_lens and chunk_starts before that wait.  With PDL on,
- *   those three arrays must therefore be complete before the call is
- *   enqueued, or be written by stream work that does not trigger its
- *   dependents early (a copy, a host write or an ordinary kernel is fine; a
- *   kernel that executes griddepcontrol.launch_dependents before it has
- *   written them is not).
+ *   kernel waits for the previous grid on the stream before touching any
+ *   memory), so back-to-back calls overlap launch latency while plain stream
+ *   order holds for every argument; see mla_set_pdl().  A caller whose
+ *   context-gather tables are complete before the call is enqueued may let the
+ *   gather read them before that wait (mla_set_gather_early_tables).
  */
 #ifndef MLA_CACHE_H
 #define MLA_CACHE_H
@@ -85,8 +87,9 @@ enum {
   MLA_ERRBIT_SLOT_OOB = 1u,   /* slot >= num_blocks * block_size */
   MLA_ERRBIT_BLOCK_OOB = 2u,  /* block table index or block id out of range */
   MLA_ERRBIT_POS_OOB = 4u,    /* position outside [0, max_position) */
-  MLA_ERRBIT_MISALIGNED = 8u, /* a per-layer cache base not 16-byte aligned */
-  MLA_ERRBIT_TIMEOUT = 16u     /* a pipeline wait gave up (see mla_context_kv_pack) */
+  MLA_ERRBIT_MISALIGNED = 8u, /* a per-layer cache base null or not 16-byte aligned */
+  MLA_ERRBIT_TIMEOUT = 16u     /* a pipeline wait of the grouped insert gave up (see
+                                  mla_cache_insert_grouped) */
 };
 
 /* Map a vLLM kv-cache-dtype string to mla_dtype_t; -1 if it is not one of
@@ -111,6 +114,37 @@ int mla_set_pdl(int enable);
  * the mode leaves out, runs the row-per-warp shape.  Both shapes compute
  * identical results.  Returns the previous mode (other values set 1). */
 int mla_set_bulk_copy(int mode);
+
+/* Enable (1, the default) or disable (0), for every later call from this
+ * process, the cudaPointerGetAttributes checks of pointer arguments (see the
+ * conventions above).  With the checks off a host pointer is not caught
+ * before the launch, and the kernel that dereferences it faults; every other
+ * argument check still runs.  Returns the previous setting. */
+int mla_set_pointer_checks(int enable);
+
+/* Let the context gathers (mla_context_gather, mla_context_gather_scaled)
+ * read block_table, cu_chunk_lens and chunk_starts BEFORE they wait for the
+ * previous grid on the stream (1), or keep plain stream order (0, the
+ * default), for every later call from this process.  With 1 and PDL on, those
+ * three arrays must be complete before the call is enqueued, or be written by
+ * stream work that does not trigger its dependents early (a copy, a host
+ * write or an ordinary kernel is fine; a kernel that executes
+ * griddepcontrol.launch_dependents before it has written them is not): the
+ * gather's first table lookups then overlap the previous kernel's tail.
+ * Returns the previous setting. */
+int mla_set_gather_early_tables(int enable);
+
+/* TESTING HOOK for the grouped insert's bulk-copy pipeline, applied to every
+ * later call from this process (not for production use).  wait_limit_ns: how
+ * long a pipeline wait may last before the kernel gives up (0 restores the
+ * default of 2 s).  skip_item >= 0: the producer of the pipeline's first CTA
+ * issues no copies for its local work item skip_item (a run of up to 4 tokens
+ * of one layer), so the consumer waiting for it runs out of time; -1 (the
+ * default) skips nothing.  A kernel that gives up sets MLA_ERRBIT_TIMEOUT,
+ * stops issuing work, waits (bounded by the same limit) for the copies it has
+ * issued, and returns; the rows it had not written are left untouched.
+ * Returns 0. */
+int mla_test_insert_timeout(uint64_t wait_limit_ns, int64_t skip_item);
 
 /*
  * Optional pre-processing of the grouped insert ("PR #50585", Source snippets:
@@ -180,9 +214,12 @@ typedef struct {
  * unspecified).
  * For 131072 or more rows (40960 with RMSNorm) with dense layer-major inputs
  * (token strides 512 and 64), the bulk-copy pipeline shape runs (see
- * mla_set_bulk_copy);
- * err_word then also receives MLA_ERRBIT_TIMEOUT if a pipeline wait ever gave
- * up (bounded at 2 s).
+ * mla_set_bulk_copy).  Its waits between the copy-issuing warp and the
+ * computing warps are bounded by wall-clock time (2 s); one that runs out
+ * (which means a fault, or a CTA stalled for seconds, e.g. by a debugger or a
+ * time-sliced GPU) makes the kernel stop, and the rows it had not yet written
+ * are left untouched.  err_word then receives MLA_ERRBIT_TIMEOUT: it is the
+ * only signal of those dropped rows, so pass one when that matters.
  */
 mla_status_t mla_cache_insert_grouped(
     const void* kv_c, int64_t kvc_token_stride, int64_t kvc_layer_stride,
@@ -217,8 +254,7 @@ mla_status_t mla_cache_insert_grouped(
  *   cu_chunk_lens       int32 device [num_seqs + 1], non-decreasing.
  *   chunk_starts        int32 device [num_seqs].
  *   num_tokens          output rows; rows owned by no sequence are untouched.
- * With PDL on, block_table, cu_chunk_lens and chunk_starts are read before the
- * kernel waits for the previous grid (see the conventions above).
+ * See mla_set_gather_early_tables for when the tables are read.
  */
 mla_status_t mla_context_gather(
     const void* kv_cache, mla_dtype_t cache_dtype, int64_t num_blocks, int32_t block_size,

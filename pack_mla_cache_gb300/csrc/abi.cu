@@ -25,6 +25,11 @@ namespace {
 thread_local std::string g_err;
 std::atomic<int> g_pdl{1};
 std::atomic<int> g_bulk{1};
+std::atomic<int> g_ptr_checks{1};
+std::atomic<int> g_gather_early{0};
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s: a wait that long means a fault
+std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
+std::atomic<int64_t> g_skip_item{-1};
 
 mla_status_t fail(mla_status_t st, const char* fmt, ...) {
   char buf[512];
@@ -50,8 +55,10 @@ inline int log2_exact(int64_t v) {
   return s;
 }
 
-// The pointer must be device (or managed) memory of the current device.
+// The pointer must be device (or managed) memory of the current device
+// (skipped while the caller has switched the checks off).
 mla_status_t check_device_ptr(const void* p, const char* name) {
+  if (!g_ptr_checks.load(std::memory_order_relaxed)) return MLA_OK;
   cudaPointerAttributes attr;
   cudaError_t e = cudaPointerGetAttributes(&attr, p);
   if (e != cudaSuccess) {
@@ -229,6 +236,17 @@ int mla_set_pdl(int enable) { return g_pdl.exchange(enable ? 1 : 0); }
 
 int mla_set_bulk_copy(int mode) { return g_bulk.exchange(mode >= 0 && mode <= 2 ? mode : 1); }
 
+int mla_set_pointer_checks(int enable) { return g_ptr_checks.exchange(enable ? 1 : 0); }
+
+int mla_set_gather_early_tables(int enable) { return g_gather_early.exchange(enable ? 1 : 0); }
+
+int mla_test_insert_timeout(uint64_t wait_limit_ns, int64_t skip_item) {
+  if (wait_limit_ns == 0) wait_limit_ns = kDefaultWaitNs;
+  g_wait_ns.store(wait_limit_ns);
+  g_skip_item.store(skip_item < 0 ? -1 : skip_item);
+  return 0;
+}
+
 mla_status_t mla_cache_insert_grouped(
     const void* kv_c, int64_t kvc_token_stride, int64_t kvc_layer_stride, const void* k_pe,
     int64_t kpe_token_stride, int64_t kpe_layer_stride, int32_t num_tokens, int32_t num_layers,
@@ -279,6 +297,8 @@ mla_status_t mla_cache_insert_grouped(
   if (!kv_c || !k_pe || !slot_mapping || !kv_cache_ptrs)
     return fail(MLA_ERR_INVALID_ARG, "kv_c, k_pe, slot_mapping and kv_cache_ptrs must be non-null");
 
+  MLA_TRY(check_device_ptr(kv_c, "kv_c"));
+  MLA_TRY(check_device_ptr(k_pe, "k_pe"));
   MLA_TRY(check_device_ptr(slot_mapping, "slot_mapping"));
   MLA_TRY(check_device_ptr(kv_cache_ptrs, "kv_cache_ptrs"));
   if (fp8) MLA_TRY(check_device_ptr(kv_scales, "kv_scales"));
@@ -315,6 +335,8 @@ mla_status_t mla_cache_insert_grouped(
   }
   a.err = err_word;
   a.bulk_mode = g_bulk.load();
+  a.wait_limit_ns = g_wait_ns.load();
+  a.skip_item = g_skip_item.load();
   return launched(mla::launch_insert(a, (int)cache_dtype, norm, rope, cfg_for(stream)),
                   "mla_cache_insert_grouped");
 }
@@ -359,6 +381,8 @@ mla_status_t gather_impl(const void* kv_cache, mla_dtype_t cache_dtype, int64_t 
   if (!kv_cache || !block_table || !cu_chunk_lens || !chunk_starts || !out)
     return fail(MLA_ERR_INVALID_ARG, "kv_cache, block_table, cu_chunk_lens, chunk_starts and out must be non-null");
 
+  MLA_TRY(check_device_ptr(kv_cache, "kv_cache"));
+  MLA_TRY(check_device_ptr(out, "out"));
   MLA_TRY(check_paged_ptrs(block_table, cu_chunk_lens, chunk_starts));
   if (dequant_scale) MLA_TRY(check_device_ptr(dequant_scale, "k_scale"));
 
@@ -371,6 +395,7 @@ mla_status_t gather_impl(const void* kv_cache, mla_dtype_t cache_dtype, int64_t 
   a.out_rs = out_row_stride * oe;
   a.dequant_scale = dequant_scale;
   a.err = err_word;
+  a.early_tables = g_gather_early.load() != 0;
   const int mode = (out_dtype == cache_dtype) ? 0 : (int)cache_dtype;
   return launched(mla::launch_gather(a, mode, (int)out_dtype, cfg_for(stream)), what);
 }
@@ -449,8 +474,19 @@ mla_status_t pack_impl(const void* k_nope, int64_t kn_token_stride, int64_t kn_h
                 paged ? "kv_cache, block_table, cu_chunk_lens and chunk_starts must be non-null"
                       : "k_pe must be non-null");
 
+  MLA_TRY(check_device_ptr(k_nope, "k_nope"));
+  if (v_out) {
+    MLA_TRY(check_device_ptr(v, "v"));
+    MLA_TRY(check_device_ptr(v_out, "v_out"));
+  }
+  MLA_TRY(check_device_ptr(key_out, "key_out"));
   if (out_scale) MLA_TRY(check_device_ptr(out_scale, "out_scale"));
-  if (paged) MLA_TRY(check_paged_ptrs(paged->block_table, paged->cu, paged->starts));
+  if (paged) {
+    MLA_TRY(check_device_ptr(paged->kv_cache, "kv_cache"));
+    MLA_TRY(check_paged_ptrs(paged->block_table, paged->cu, paged->starts));
+  } else {
+    MLA_TRY(check_device_ptr(k_pe, "k_pe"));
+  }
 
   mla::PackArgs a{};
   a.k_nope = static_cast<const uint8_t*>(k_nope);
@@ -578,6 +614,10 @@ mla_status_t mla_norm_rope_grouped(const void* kv_c, int64_t kvc_token_stride,
   if (num_tokens == 0) return MLA_OK;  // empty inputs may have null data pointers
   if (!kv_c || !k_pe || !kv_c_out || !k_pe_out)
     return fail(MLA_ERR_INVALID_ARG, "kv_c, k_pe, kv_c_out and k_pe_out must be non-null");
+  MLA_TRY(check_device_ptr(kv_c, "kv_c"));
+  MLA_TRY(check_device_ptr(k_pe, "k_pe"));
+  MLA_TRY(check_device_ptr(kv_c_out, "kv_c_out"));
+  MLA_TRY(check_device_ptr(k_pe_out, "k_pe_out"));
   MLA_TRY(check_norm_rope_ptrs(norm_rope, norm, rope));
 
   mla::NormRopeArgs a{};

@@ -14,10 +14,10 @@
 // stores); the row lookup (paged.cuh) costs a ballot and one block-table load.
 // A chunk of 8192 rows is latency-bound (sequence table -> block table -> row),
 // so as many warps as rows wins: 3.6 us per 8192-row chunk against 4.9 us with
-// 4 rows per warp; at 262144 rows both run at ~5.9 TB/s.  A warp's first
-// lookup is done before the programmatic-launch wait (the tables are inputs
-// that no kernel here writes), so only the cache row load follows the previous
-// kernel.
+// 4 rows per warp; at 262144 rows both run at ~5.9 TB/s.  When the caller
+// declares its tables complete before the call, a warp's first lookup is done
+// before the programmatic-launch wait, so only the cache row load follows the
+// previous kernel.
 #include "mla_device.cuh"
 #include "mla_internal.h"
 #include "paged.cuh"
@@ -38,11 +38,14 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const GatherArgs a) {
   const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
   uint32_t errbits = 0;
-  // The first rows' lookups read only the sequence and block tables, which no
-  // kernel of this library writes: they run before the wait on the previous
-  // grid, so two of the three dependent loads of a row overlap its tail.  Each
-  // later lookup is done at the end of the previous iteration (the loop is
-  // rotated), which keeps the register count of the plain loop.
+  // The first rows' lookups read only the sequence and block tables.  When the
+  // caller has declared them complete before the call (early_tables), they
+  // run before the wait on the previous grid, so two of the three dependent
+  // loads of a row overlap its tail; otherwise after it (plain stream order;
+  // the second wait below is then a no-op).  Each later lookup is done at the
+  // end of the previous iteration (the loop is rotated), which keeps the
+  // register count of the plain loop.
+  if (!a.early_tables) pdl_wait();
   const SeqLanes sl = load_seq_lanes(a.src, lane);
   const uint8_t* src[kRows];
 #pragma unroll

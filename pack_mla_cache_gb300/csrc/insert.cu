@@ -145,7 +145,7 @@ __device__ __forceinline__ uint32_t store_row(const InsertArgs& a, int l, int la
   if (s < 0) return 0;  // padding slot (uniform across the warp)
   if (s >= a.capacity) return kErrSlotOOB;
   if (ROPE && !pos_ok) return kErrPosOOB;
-  if (cptr & 15) return kErrMisaligned;
+  if (cptr == 0 || (cptr & 15)) return kErrMisaligned;
   int64_t blk, off;
   if (a.bs_shift >= 0) {
     blk = s >> a.bs_shift;
@@ -265,7 +265,6 @@ struct Ring {
   static_assert(kStages <= 64, "a producer lane owns at most two stages");
   static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
 };
-constexpr uint64_t kIWaitLimitNs = 2000000000ull;  // 2 s: a wait that long means a fault
 
 // One item (a layer's run of up to kRun tokens) from its shared-memory stage.
 // The rows are processed in lockstep -- validity and loads of every row, then
@@ -290,7 +289,7 @@ __device__ __forceinline__ uint32_t insert_consume_item(
     if (s < 0) continue;  // padding slot or past the tail
     if (s >= a.capacity) { err |= kErrSlotOOB; continue; }
     if (ROPE && (pos[r] < 0 || pos[r] >= a.max_position)) { err |= kErrPosOOB; continue; }
-    if (cptr & 15) { err |= kErrMisaligned; continue; }
+    if (cptr == 0 || (cptr & 15)) { err |= kErrMisaligned; continue; }
     int64_t blk, off;
     if (a.bs_shift >= 0) {
       blk = s >> a.bs_shift;
@@ -414,7 +413,7 @@ __global__ void __launch_bounds__(kIThreads, 1) insert_tma_kernel(const InsertAr
     for (int64_t i = lane; lane < kIStages && i < n_local;) {
       const int s = (int)((uint32_t)i % (uint32_t)kIStages);
       const int64_t n = (int64_t)((uint32_t)i / (uint32_t)kIStages);
-      if (n > 0 && !mbar_wait(empty0 + 8 * s, (uint32_t)((n - 1) & 1), kIWaitLimitNs)) {
+      if (n > 0 && !mbar_wait(empty0 + 8 * s, (uint32_t)((n - 1) & 1), a.wait_limit_ns)) {
         *abort_flag = 1;
         break;
       }
@@ -425,13 +424,15 @@ __global__ void __launch_bounds__(kIThreads, 1) insert_tma_kernel(const InsertAr
       const int64_t t0 = run * kRun;
       const int nt = (int)min((int64_t)kRun, (int64_t)a.num_tokens - t0);
       const uint32_t dst = stage0 + (uint32_t)(s * kIStageBytes);
-      mbar_arrive_expect_tx(full0 + 8 * s, (uint32_t)nt * (2 * kR + 2 * kP));
-      bulk_g2s(dst, a.kv_c + t0 * a.kvc_ts + (int64_t)l * a.kvc_ls, (uint32_t)nt * 2 * kR,
-               full0 + 8 * s);
-      bulk_g2s(dst + kOffPe, a.k_pe + t0 * a.kpe_ts + (int64_t)l * a.kpe_ls,
-               (uint32_t)nt * 2 * kP, full0 + 8 * s);
-      if (kIStages <= 32 || s < 32) fills0 = n + 1;
-      else fills1 = n + 1;
+      if (b != 0 || i != a.skip_item) {  // (the test hook issues nothing for one item)
+        mbar_arrive_expect_tx(full0 + 8 * s, (uint32_t)nt * (2 * kR + 2 * kP));
+        bulk_g2s(dst, a.kv_c + t0 * a.kvc_ts + (int64_t)l * a.kvc_ls, (uint32_t)nt * 2 * kR,
+                 full0 + 8 * s);
+        bulk_g2s(dst + kOffPe, a.k_pe + t0 * a.kpe_ts + (int64_t)l * a.kpe_ls,
+                 (uint32_t)nt * 2 * kP, full0 + 8 * s);
+        if (kIStages <= 32 || s < 32) fills0 = n + 1;
+        else fills1 = n + 1;
+      }
       // next item of this lane: its second stage in this round, else its first
       // stage in the next round
       if constexpr (kIStages <= 32) i += kIStages;
@@ -439,7 +440,7 @@ __global__ void __launch_bounds__(kIThreads, 1) insert_tma_kernel(const InsertAr
     }
   } else {
     // ---------------- consumers --------------------------------------------------
-    for (int64_t i = warp; i < n_local; i += kIConsumers) {
+    for (int64_t i = warp; i < n_local && !*abort_flag; i += kIConsumers) {
       const int s = (int)((uint32_t)i % (uint32_t)kIStages);
       const int64_t j = b + G * i;
       const int64_t run = (int64_t)((uint32_t)j / (uint32_t)L);
@@ -461,7 +462,7 @@ __global__ void __launch_bounds__(kIThreads, 1) insert_tma_kernel(const InsertAr
           if (ROPE) pos[r] = __ldg(a.positions + t0 + r);
         }
       }
-      if (!mbar_wait(full0 + 8 * s, ((uint32_t)i / (uint32_t)kIStages) & 1u, kIWaitLimitNs)) {
+      if (!mbar_wait(full0 + 8 * s, ((uint32_t)i / (uint32_t)kIStages) & 1u, a.wait_limit_ns)) {
         *abort_flag = 1;
         break;
       }
@@ -478,12 +479,16 @@ __global__ void __launch_bounds__(kIThreads, 1) insert_tma_kernel(const InsertAr
   }
   __syncthreads();
   if (*abort_flag) {
-    // Let every copy this CTA issued land before its shared memory is released.
+    // Let every copy this CTA issued land before its shared memory is released:
+    // a stage holds at most one fill in flight (the next one waits for the
+    // stage's release), so waiting for each stage's last issued fill suffices.
+    // A copy of a few KB from valid memory completes in microseconds; the wait
+    // is bounded all the same.
     if (warp == kIConsumers) {
       if (fills0 > 0)
-        (void)mbar_wait(full0 + 8 * lane, (uint32_t)((fills0 - 1) & 1), kIWaitLimitNs / 8);
+        (void)mbar_wait(full0 + 8 * lane, (uint32_t)((fills0 - 1) & 1), a.wait_limit_ns);
       if (kIStages > 32 && fills1 > 0)
-        (void)mbar_wait(full0 + 8 * (lane + 32), (uint32_t)((fills1 - 1) & 1), kIWaitLimitNs / 8);
+        (void)mbar_wait(full0 + 8 * (lane + 32), (uint32_t)((fills1 - 1) & 1), a.wait_limit_ns);
     }
     errbits |= kErrTimeout;
   }

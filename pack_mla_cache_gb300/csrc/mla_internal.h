@@ -31,6 +31,12 @@ struct InsertArgs {
   int64_t max_position;
   uint32_t* err;
   int bulk_mode;  // bulk-copy pipeline shape: 0 never, 1 large calls, 2 always
+  // bulk-copy shape only: how long a pipeline wait may last before the
+  // kernel gives up (MLA_ERRBIT_TIMEOUT), and a test hook: CTA 0's producer
+  // issues no copies for its local item `skip_item` (-1: none), so the
+  // consumer waiting for that item runs out of time.
+  uint64_t wait_limit_ns;
+  int64_t skip_item;
 };
 
 // A paged cache and the chunk's sequences: chunk token i of sequence s
@@ -56,6 +62,10 @@ struct GatherArgs {
   int64_t out_rs;
   const float* dequant_scale;  // scaled widening only
   uint32_t* err;
+  // read the sequence and block tables before waiting for the previous grid
+  // (programmatic dependent launch); only for callers whose tables are
+  // complete before the call is enqueued
+  bool early_tables;
 };
 
 struct PackArgs {

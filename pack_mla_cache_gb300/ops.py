@@ -47,6 +47,9 @@ SIGNATURES = {
     "mla_version": (ctypes.c_char_p, []),
     "mla_set_pdl": (ctypes.c_int, [ctypes.c_int]),
     "mla_set_bulk_copy": (ctypes.c_int, [ctypes.c_int]),
+    "mla_set_pointer_checks": (ctypes.c_int, [ctypes.c_int]),
+    "mla_set_gather_early_tables": (ctypes.c_int, [ctypes.c_int]),
+    "mla_test_insert_timeout": (ctypes.c_int, [ctypes.c_uint64, _i64]),
     "mla_cache_insert_grouped": (ctypes.c_int, [
         _vp, _i64, _i64, _vp, _i64, _i64, _i32, _i32, _i32, _i32, _vp, _i64, _vp, _vp,
         ctypes.c_int, _i64, _i32, _i64, _i64, ctypes.POINTER(NormRope), _vp, _vp]),
@@ -137,6 +140,25 @@ def mla_set_bulk_copy(mode: int) -> int:
     """0 never, 1 large calls (default), 2 every call whose layout qualifies;
     returns the previous mode."""
     return int(lib().mla_set_bulk_copy(int(mode)))
+
+
+def mla_set_pointer_checks(enable: bool) -> bool:
+    """Switch the per-call device-pointer checks on (default) or off; returns
+    the previous setting."""
+    return bool(lib().mla_set_pointer_checks(1 if enable else 0))
+
+
+def mla_set_gather_early_tables(enable: bool) -> bool:
+    """Let the context gathers read their tables before the programmatic
+    launch wait (the tables must be complete before each call is enqueued);
+    returns the previous setting."""
+    return bool(lib().mla_set_gather_early_tables(1 if enable else 0))
+
+
+def mla_test_insert_timeout(wait_limit_ns: int = 0, skip_item: int = -1) -> None:
+    """Testing hook of the insert's bulk-copy pipeline (see the C header);
+    ``mla_test_insert_timeout()`` restores the defaults."""
+    lib().mla_test_insert_timeout(int(wait_limit_ns), int(skip_item))
 
 
 def mla_cache_insert_grouped(kv_c, k_pe, slot_mapping, kv_cache_ptrs, kv_scales, cache_dtype,

@@ -71,6 +71,18 @@ def test_pdl_and_bulk_copy_toggles(L):
     assert ops.mla_set_bulk_copy(prev) == 1
 
 
+def test_pointer_check_early_table_and_timeout_hook_toggles(L):
+    prev = ops.mla_set_pointer_checks(False)
+    assert ops.mla_set_pointer_checks(True) is False
+    ops.mla_set_pointer_checks(prev)
+    assert prev is True  # checked by default
+    prev = ops.mla_set_gather_early_tables(True)
+    assert prev is False  # plain stream order by default
+    assert ops.mla_set_gather_early_tables(False) is True
+    assert L.mla_test_insert_timeout(1000, 5) == 0
+    assert L.mla_test_insert_timeout(0, -1) == 0  # defaults back
+
+
 def insert(L, **kw):
     args = dict(kv_c=A, kvc_ts=512, kvc_ls=512 * 8, k_pe=A + 4096, kpe_ts=64, kpe_ls=64 * 8,
                 T=8, nl=5, R=512, P=64, slots=A + 8192, sls=0, ptrs=A + 16384, scales=A + 32768,
@@ -135,6 +147,21 @@ def test_validated_call_without_gpu_reports_cuda_error(L):
         pytest.skip("this check is for machines without a GPU")
     assert insert(L) == ops.MLA_ERR_CUDA
     assert "cudaPointerGetAttributes" in ops.mla_last_error()
+    assert "kv_c" in ops.mla_last_error()  # the first pointer checked
+
+
+def test_pointer_checks_off_skips_the_runtime_queries_without_gpu(L):
+    """With the checks off nothing asks the runtime about the pointers; on a
+    machine without a GPU the call then fails at the launch.  (Never run with
+    these fake addresses where a GPU could dereference them.)"""
+    if torch.cuda.is_available():
+        pytest.skip("this check is for machines without a GPU")
+    prev = ops.mla_set_pointer_checks(False)
+    try:
+        assert insert(L) == ops.MLA_ERR_CUDA
+        assert "cudaPointerGetAttributes" not in ops.mla_last_error()
+    finally:
+        ops.mla_set_pointer_checks(prev)
 
 
 def gather(L, **kw):

@@ -79,15 +79,19 @@ def test_gather_many_sequences_and_bad_blocks(orc):
     table[5, 1] = 128    # block id out of range
     table[9, 0] = -3
     lens = rng.integers(0, 200, size=S)
-    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
     starts = rng.integers(0, 300, size=S).astype(np.int32)  # positions up to 500 < 8 * 64
+    # sequence 5 reaches its bad block 1 (positions 10..159), sequence 9 its
+    # bad block 0 (positions 0..19)
+    lens[5], starts[5] = 150, 10
+    lens[9], starts[9] = 20, 0
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
     T = int(cu[-1]) + 5  # 5 trailing rows owned by no sequence
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     g = gpu_gather(pw, cache_t, table, cu, starts, T, 1, err=err)
     r, oerr = oracle_gather(orc, pw, table, cu, starts, T, 1)
     np.testing.assert_array_equal(g, r)
+    assert oerr == ops.MLA_ERRBIT_BLOCK_OOB
     assert int(err.item()) == oerr
-    assert oerr in (0, ops.MLA_ERRBIT_BLOCK_OOB)
 
 
 def test_gather_one_launch_of_32768_rows_with_bad_blocks(orc):
@@ -110,11 +114,13 @@ def test_gather_one_launch_of_32768_rows_with_bad_blocks(orc):
     np.testing.assert_array_equal(g, r)
 
 
-def test_gather_sees_tables_written_just_before_it(orc):
-    """With programmatic dependent launch on, the gather reads its block table
-    and sequence tables before waiting on the previous grid.  Tables written by
-    ordinary kernels enqueued just before each call on the same stream (they
-    trigger no early launch) are still the ones it reads."""
+@pytest.mark.parametrize("early", [False, True], ids=["stream_order", "early_tables"])
+def test_gather_sees_tables_written_just_before_it(orc, early):
+    """With programmatic dependent launch on, tables written by ordinary
+    kernels enqueued just before each call on the same stream (they trigger no
+    early launch) are the ones the gather reads, both in plain stream order
+    (the default) and when the gather reads its tables before waiting on the
+    previous grid (mla_set_gather_early_tables)."""
     pw = W.pack_workload(16448, 8192, num_blocks=512, seed=12)  # positions up to 16386
     cache_t = dev_cache(pw)
     src_table = D.dev(pw.block_table)
@@ -123,6 +129,7 @@ def test_gather_sees_tables_written_just_before_it(orc):
     st_t = torch.zeros(1, dtype=torch.int32, device="cuda")
     outs = torch.zeros((2, 8192, ENTRY), dtype=torch.uint8, device="cuda")
     prev = ops.mla_set_pdl(True)
+    prev_early = ops.mla_set_gather_early_tables(early)
     try:
         for c in range(2):
             table_t.zero_()
@@ -139,12 +146,55 @@ def test_gather_sees_tables_written_just_before_it(orc):
         torch.cuda.synchronize()
     finally:
         ops.mla_set_pdl(prev)
+        ops.mla_set_gather_early_tables(prev_early)
     for c in range(2):
         cu = np.array([0, 8192], np.int32)
         st = np.array([c * 8192 + 3], np.int32)
         r, err = oracle_gather(orc, pw, pw.block_table, cu, st, 8192, 1)
         assert err == 0
         np.testing.assert_array_equal(D.host_u8(outs[c]), r)
+
+
+def test_gather_default_order_sees_a_table_written_by_a_pdl_kernel(orc):
+    """In the default (plain stream order) the gather reads its block table
+    only after the previous grid has completed, even when that grid is a
+    library kernel that lets its dependents launch at its start: here a first
+    gather (PDL on, early trigger) copies the second gather's block table out of
+    a cache row into the table buffer, which held only invalid block ids."""
+    pw = W.pack_workload(8192, 8192, num_blocks=256, seed=13)
+    cache_t = dev_cache(pw)
+    want = pw.block_table[0, :128].astype(np.int32)  # the 128 blocks of 8192 rows
+    # a one-block fp8 "cache" whose row 0 holds the table's bytes (576 B row)
+    src = np.zeros(64 * ENTRY, np.uint8)
+    src[:512] = want.view(np.uint8)
+    src_t = D.dev(src)
+    one = torch.zeros((1, 144), dtype=torch.int32, device="cuda")  # out: 576 B = 144 int32
+    one.fill_(-1)
+    cu1 = D.dev(np.array([0, 1], np.int32))
+    st1 = D.dev(np.array([0], np.int32))
+    bt1 = D.dev(np.zeros((1, 1), np.int32))
+    cu = D.dev(np.array([0, 8192], np.int32))
+    st = D.dev(np.array([0], np.int32))
+    out = torch.zeros((8192, ENTRY), dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    prev = ops.mla_set_pdl(True)
+    prev_early = ops.mla_set_gather_early_tables(False)
+    try:
+        for _ in range(3):
+            one.fill_(-1)
+            ops.mla_context_gather(src_t, 1, 1, 64, 64 * ENTRY, ENTRY, ENTRY, bt1, cu1, st1,
+                                   one.view(torch.uint8).view(1, 576), 1)
+            ops.mla_context_gather(cache_t, 1, pw.num_blocks, 64, 64 * ENTRY, ENTRY, ENTRY,
+                                   one[:, :128], cu, st, out, 1, err_word=err)
+        torch.cuda.synchronize()
+    finally:
+        ops.mla_set_pdl(prev)
+        ops.mla_set_gather_early_tables(prev_early)
+    assert int(err.item()) == 0
+    r, oerr = oracle_gather(orc, pw, pw.block_table, np.array([0, 8192], np.int32),
+                            np.array([0], np.int32), 8192, 1)
+    assert oerr == 0
+    np.testing.assert_array_equal(D.host_u8(out), r)
 
 
 def test_gather_bf16_cache_raw(orc):

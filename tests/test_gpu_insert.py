@@ -120,8 +120,9 @@ def test_fp8_conversion_exhaustive_through_every_shape(orc, bulk, dtype):
 
 
 def test_ragged_non_power_of_two_blocks_and_large_rows(orc):
-    """1000 tokens x 3 layers (rows not a multiple of any tile), block_size 48
-    (division path), 32768+ rows so the multi-row-per-warp instance runs."""
+    """11111 tokens x 3 layers with per-layer mappings (33333 rows: not a
+    multiple of any tile, more rows than the capped grid has warps, so warps
+    loop), block_size 48 (the division path instead of the shift)."""
     wl = W.insert_workload(3, 11111, 1, num_blocks=300, block_size=48, shared_slots=False,
                            seed=11)
     gpu, guards, _ = D.gpu_insert(wl)
@@ -240,6 +241,115 @@ def test_host_pointer_for_scales_is_rejected():
         ops.mla_cache_insert_grouped(D.dev_bf16(wl.kv_c), D.dev_bf16(wl.k_pe),
                                      D.dev(np.ascontiguousarray(wl.slot_mapping[0])), ptrs,
                                      host_scales, 1, 1, 64, 64 * 576, 576)
+
+
+def test_host_pointer_for_kv_c_is_rejected():
+    wl = W.insert_workload(5, 4, 1, num_blocks=1, block_size=64, seed=0)
+    c = D.Guarded(64 * 576)
+    ptrs = torch.tensor([c.ptr()] * 5, dtype=torch.int64, device="cuda")
+    host_kv_c = torch.zeros((5, 4, 512), dtype=torch.bfloat16)
+    with pytest.raises(ops.MlaError, match="kv_c must be device memory"):
+        ops.mla_cache_insert_grouped(host_kv_c, D.dev_bf16(wl.k_pe),
+                                     D.dev(np.ascontiguousarray(wl.slot_mapping[0])), ptrs,
+                                     D.dev(wl.k_scales), 1, 1, 64, 64 * 576, 576)
+    assert c.guards_intact() and bool((c.t == D.CANARY).all().item())
+
+
+def test_pointer_checks_off_runs_the_same_insert(orc):
+    """With the per-call device-pointer checks switched off (device pointers
+    only), the insert writes exactly what it writes with them on."""
+    wl = W.insert_workload(5, 8, 1, num_blocks=4, block_size=64, seed=3)
+    prev = ops.mla_set_pointer_checks(False)
+    try:
+        gpu, guards, _ = D.gpu_insert(wl)
+    finally:
+        ops.mla_set_pointer_checks(prev)
+    ref, _ = oracle_insert(orc, wl)
+    assert guards
+    assert_exact(gpu, ref)
+
+
+def test_null_layer_cache_pointer_skips_that_layer(orc, bulk):
+    """A null entry in kv_cache_ptrs: that layer's rows are skipped with
+    MLA_ERRBIT_MISALIGNED (no write near address 0); the other layers are
+    exact.  8192 tokens x 5 layers so the bulk-copy shape runs when forced."""
+    wl = W.insert_workload(5, 8192, 1, num_blocks=256, block_size=64, seed=4)
+    nbytes = wl.num_blocks * wl.block_size * W.ENTRY
+    caches = [D.Guarded(nbytes) for _ in range(5)]
+    for c in caches:
+        c.t.fill_(0x44)
+    ptrs = torch.tensor([c.ptr() for c in caches], dtype=torch.int64, device="cuda")
+    ptrs[2] = 0
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ops.mla_cache_insert_grouped(D.dev_bf16(wl.kv_c), D.dev_bf16(wl.k_pe),
+                                 D.dev(np.ascontiguousarray(wl.slot_mapping[0])), ptrs,
+                                 D.dev(wl.k_scales), 1, wl.num_blocks, 64, 64 * 576, 576,
+                                 err_word=err)
+    torch.cuda.synchronize()
+    ref, oerr = oracle_insert(orc, wl, fill=0x44)
+    assert oerr == 0
+    assert int(err.item()) == ops.MLA_ERRBIT_MISALIGNED
+    for l, c in enumerate(caches):
+        assert c.guards_intact()
+        h = c.host()
+        if l == 2:
+            assert (h == 0x44).all()
+        else:
+            np.testing.assert_array_equal(h, ref[l])
+
+
+def test_bulk_ring_timeout_path_returns_and_reports(orc):
+    """The bulk-copy ring's bounded waits: with a 1 ms limit and the producer
+    of the first CTA issuing no copies for its local item 3 (a testing hook),
+    the consumer waiting for that item runs out of time.  The call returns,
+    MLA_ERRBIT_TIMEOUT is set, every row is either the oracle's or untouched
+    (the skipped item's rows untouched), the guard bands hold, and the next
+    call with the default limit is exact.  No fault is involved: only a wait
+    that gives up."""
+    wl = W.insert_workload(5, 512, 1, num_blocks=16, block_size=64, seed=5)
+    ref, _ = oracle_insert(orc, wl, fill=0x3C)
+    prev = ops.mla_set_bulk_copy(2)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    try:
+        ops.mla_test_insert_timeout(1_000_000, 3)
+        gpu, guards, _ = D.gpu_insert(wl, fill=0x3C, err=err)
+    finally:
+        ops.mla_test_insert_timeout()
+    try:
+        assert guards
+        assert int(err.item()) & ops.MLA_ERRBIT_TIMEOUT
+        # item 3 of CTA 0 is global item G * 3 (G CTAs; items are (4-token run, layer))
+        items = (512 // 4) * 5
+        G = min(ops_grid_ctas(), -(-items // 23))
+        j = G * 3
+        run, layer = j // 5, j % 5
+        slots = wl.slot_mapping[0]
+        written = 0
+        for l in range(5):
+            g = gpu[l].reshape(-1, 576)
+            r = ref[l].reshape(-1, 576)
+            unnamed = np.ones(g.shape[0], bool)
+            unnamed[slots] = False
+            assert (g[unnamed] == 0x3C).all()
+            for t in range(512):
+                row = g[slots[t]]
+                untouched = bool((row == 0x3C).all())
+                if l == layer and run * 4 <= t < run * 4 + 4:
+                    assert untouched, ("the skipped item's row was written", l, t)
+                elif not untouched:  # rows after the timeout may be dropped
+                    np.testing.assert_array_equal(row, r[slots[t]])
+                    written += 1
+        assert written > 0
+        gpu2, guards2, _ = D.gpu_insert(wl, fill=0x3C)
+        assert guards2
+        assert_exact(gpu2, ref)
+    finally:
+        ops.mla_set_bulk_copy(prev)
+
+
+def ops_grid_ctas():
+    """CTAs of the bulk-copy ring that can be resident: one per SM."""
+    return torch.cuda.get_device_properties(0).multi_processor_count
 
 
 # ------------------------------------------------------------ norm + rope inserts
