@@ -250,6 +250,43 @@ class Workload:
             self.gather(c)
             self.pack(c)
 
+    # the chunk loop software-pipelined: chunk c's pack and chunk c + 1's gather
+    # in one launch, the gathers alternating between two workspaces
+    def pipelined_setup(self):
+        import torch
+        ops = self.ops
+        if getattr(self, "fused_descs", None):
+            return
+        self.ws_pair = [self.ws, torch.empty_like(self.ws)]
+        n = self.pw.num_chunks
+        cu_empty = torch.tensor([0, 0], dtype=torch.int32, device=self.ws.device)
+        self.fused_descs = []
+        for c in range(n):
+            heads = self.kvb[c][:, :HEADS * 256].view(CHUNK, HEADS, 256)
+            pk = ops.kv_pack_desc(heads[:, :, :128], heads[:, :, 128:], self.ws_pair[c % 2][:, 512:],
+                                  self.key[c], self.vout[c], 1, kpe_dtype=1,
+                                  out_scale=self.out_scale)
+            nxt = c + 1 < n
+            gd = ops.context_gather_desc(self.ctx_cache, 1, NB_CTX, BS, BS * ENTRY, ENTRY, ENTRY,
+                                         self.block_table, self.cu if nxt else cu_empty,
+                                         self.starts[c + 1 if nxt else c],
+                                         self.ws_pair[(c + 1) % 2], 1,
+                                         num_tokens=CHUNK if nxt else 0)
+            self.fused_descs.append((pk, gd))
+        self._keep = cu_empty
+
+    def pack_gather(self, c):
+        pk, gd = self.fused_descs[c]
+        self.ops.mla_context_kv_pack_gather(pk, gd, err_word=self.err[1:2])
+
+    def step_pipelined(self):
+        self.insert()
+        self.ops.mla_context_gather(self.ctx_cache, 1, NB_CTX, BS, BS * ENTRY, ENTRY, ENTRY,
+                                    self.block_table, self.cu, self.starts[0], self.ws_pair[0], 1,
+                                    err_word=self.err[1:2])
+        for c in range(self.pw.num_chunks):
+            self.pack_gather(c)
+
     # the whole context in one launch each (the grid-capped grid-stride loop)
     def one_launch_setup(self):
         import torch

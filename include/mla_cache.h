@@ -371,6 +371,72 @@ mla_status_t mla_context_kv_pack_paged(
     uint32_t* err_word, mla_stream_t stream);
 
 /*
+ * The arguments of mla_context_kv_pack (non-paged) and of mla_context_gather
+ * as structs, for mla_context_kv_pack_gather below.  Each field has the
+ * meaning, layout and rules of the same-named argument there.
+ */
+typedef struct {
+  const void* k_nope;
+  int64_t kn_token_stride, kn_head_stride;
+  const void* v;
+  int64_t v_token_stride, v_head_stride;
+  mla_dtype_t in_dtype;
+  const void* k_pe;
+  int64_t kpe_token_stride;
+  mla_dtype_t kpe_dtype;
+  int32_t num_tokens, num_heads, nope_dim, rope_dim, v_dim;
+  void* key_out;
+  void* v_out;
+  mla_dtype_t out_dtype;
+  const float* out_scale;
+} mla_kv_pack_t;
+
+typedef struct {
+  const void* kv_cache;
+  mla_dtype_t cache_dtype;
+  int64_t num_blocks;
+  int32_t block_size;
+  int64_t block_stride, entry_stride;
+  int32_t entry_dim;
+  const int32_t* block_table;
+  int64_t block_table_stride;
+  const int32_t* cu_chunk_lens;
+  const int32_t* chunk_starts;
+  int32_t num_seqs, num_tokens;
+  void* out;
+  int64_t out_row_stride;
+  mla_dtype_t out_dtype;
+} mla_context_gather_t;
+
+/*
+ * The pack of one context chunk and the gather of the NEXT chunk's latent
+ * rows in one launch: the result equals mla_context_kv_pack(*pack) followed by
+ * mla_context_gather(*next_gather) (gather errors into gather_err_word).
+ *
+ * In the chunked-context loop ("PR #51772 [Attention][MLA] Fuse Kimi-K3
+ * chunked-context K/V packing", Implementation items 1-2: per chunk, gather
+ * the latent rows, run kv_b_proj on them, then pack the key and V), chunk
+ * c + 1's gather depends only on the cache and its tables, so with two gather
+ * workspaces it can run inside chunk c's pack launch:
+ *     gather(0); for c: kv_b_proj(c); pack(c) + gather(c + 1) in one call
+ * -- one launch per chunk instead of two, with the gather's dependent row
+ * lookups overlapping the pack's streaming.
+ *
+ * Rules: those of the two calls, plus:
+ *   - the gather's out_dtype is its cache_dtype (raw copy) or the pack's
+ *     in_dtype (an fp8 cache widened exactly); no scaled dequantisation;
+ *   - the gather's output rows must not overlap any buffer of the pack
+ *     (k_nope, v, k_pe, key_out, v_out; checked: MLA_ERR_INVALID_ARG) -- in
+ *     particular the pack's k_pe must come from the OTHER workspace;
+ *   - either num_tokens may be 0 (that half is skipped).
+ * With mla_set_gather_early_tables(1) the gather's tables are read before the
+ * launch waits for the previous grid, as for mla_context_gather.
+ */
+mla_status_t mla_context_kv_pack_gather(const mla_kv_pack_t* pack,
+                                        const mla_context_gather_t* next_gather,
+                                        uint32_t* gather_err_word, mla_stream_t stream);
+
+/*
  * Grouped RMSNorm + RoPE on its own, for when the grouped insert is not the
  * consumer ("PR #50585 [K3 Perf] Optimize k3 dspark fused kv", Implementation
  * item 3 and Source snippets: _precompute_fused_context_kv splits the

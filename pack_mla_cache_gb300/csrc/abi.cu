@@ -347,14 +347,17 @@ namespace {
 
 // The gathers: out_dtype == cache_dtype (raw) or MLA_BF16 from an fp8 cache
 // (widened exactly, or times *dequant_scale when it is set).
-mla_status_t gather_impl(const void* kv_cache, mla_dtype_t cache_dtype, int64_t num_blocks,
+// Validates a gather and fills its launch arguments (a.num_tokens == 0: valid,
+// nothing to launch); *mode is 0 (raw copy) or the widened fp8 cache format.
+mla_status_t gather_prep(const void* kv_cache, mla_dtype_t cache_dtype, int64_t num_blocks,
                          int32_t block_size, int64_t block_stride, int64_t entry_stride,
                          int32_t entry_dim, const int32_t* block_table,
                          int64_t block_table_stride, const int32_t* cu_chunk_lens,
                          const int32_t* chunk_starts, int32_t num_seqs, int32_t num_tokens,
                          void* out, int64_t out_row_stride, mla_dtype_t out_dtype,
-                         const float* dequant_scale, uint32_t* err_word, mla_stream_t stream,
-                         const char* what) {
+                         const float* dequant_scale, uint32_t* err_word, mla::GatherArgs& a,
+                         int* mode) {
+  a = mla::GatherArgs{};
   if (num_tokens < 0) return fail(MLA_ERR_INVALID_ARG, "num_tokens must be >= 0");
   if (!valid_dtype(cache_dtype) || !valid_dtype(out_dtype))
     return fail(MLA_ERR_INVALID_ARG, "cache_dtype / out_dtype must be an mla_dtype_t value");
@@ -377,26 +380,51 @@ mla_status_t gather_impl(const void* kv_cache, mla_dtype_t cache_dtype, int64_t 
     return fail(MLA_ERR_MISALIGNED, "k_scale must be 4-byte aligned");
   if (err_word && (reinterpret_cast<uintptr_t>(err_word) & 3))
     return fail(MLA_ERR_MISALIGNED, "err_word must be 4-byte aligned");
+  *mode = (out_dtype == cache_dtype) ? 0 : (int)cache_dtype;
+  a.num_tokens = num_tokens;
   if (num_tokens == 0) return MLA_OK;  // empty inputs may have null data pointers
   if (!kv_cache || !block_table || !cu_chunk_lens || !chunk_starts || !out)
     return fail(MLA_ERR_INVALID_ARG, "kv_cache, block_table, cu_chunk_lens, chunk_starts and out must be non-null");
 
-  MLA_TRY(check_device_ptr(kv_cache, "kv_cache"));
-  MLA_TRY(check_device_ptr(out, "out"));
-  MLA_TRY(check_paged_ptrs(block_table, cu_chunk_lens, chunk_starts));
-  if (dequant_scale) MLA_TRY(check_device_ptr(dequant_scale, "k_scale"));
-
-  mla::GatherArgs a{};
   a.src = paged_src(kv_cache, num_blocks, block_size, block_stride, entry_stride, ce, block_table,
                     block_table_stride, cu_chunk_lens, chunk_starts, num_seqs);
   a.row_chunks = (int32_t)((int64_t)entry_dim * ce / 16);
-  a.num_tokens = num_tokens;
   a.out = static_cast<uint8_t*>(out);
   a.out_rs = out_row_stride * oe;
   a.dequant_scale = dequant_scale;
   a.err = err_word;
   a.early_tables = g_gather_early.load() != 0;
-  const int mode = (out_dtype == cache_dtype) ? 0 : (int)cache_dtype;
+  return MLA_OK;
+}
+
+// The device-pointer checks of a gather that gather_prep accepted with rows.
+mla_status_t gather_ptr_checks(const void* kv_cache, const void* out, const int32_t* block_table,
+                               const int32_t* cu_chunk_lens, const int32_t* chunk_starts,
+                               const float* dequant_scale) {
+  MLA_TRY(check_device_ptr(kv_cache, "kv_cache"));
+  MLA_TRY(check_device_ptr(out, "out"));
+  MLA_TRY(check_paged_ptrs(block_table, cu_chunk_lens, chunk_starts));
+  if (dequant_scale) MLA_TRY(check_device_ptr(dequant_scale, "k_scale"));
+  return MLA_OK;
+}
+
+mla_status_t gather_impl(const void* kv_cache, mla_dtype_t cache_dtype, int64_t num_blocks,
+                         int32_t block_size, int64_t block_stride, int64_t entry_stride,
+                         int32_t entry_dim, const int32_t* block_table,
+                         int64_t block_table_stride, const int32_t* cu_chunk_lens,
+                         const int32_t* chunk_starts, int32_t num_seqs, int32_t num_tokens,
+                         void* out, int64_t out_row_stride, mla_dtype_t out_dtype,
+                         const float* dequant_scale, uint32_t* err_word, mla_stream_t stream,
+                         const char* what) {
+  mla::GatherArgs a;
+  int mode = 0;
+  MLA_TRY(gather_prep(kv_cache, cache_dtype, num_blocks, block_size, block_stride, entry_stride,
+                      entry_dim, block_table, block_table_stride, cu_chunk_lens, chunk_starts,
+                      num_seqs, num_tokens, out, out_row_stride, out_dtype, dequant_scale,
+                      err_word, a, &mode));
+  if (num_tokens == 0) return MLA_OK;
+  MLA_TRY(gather_ptr_checks(kv_cache, out, block_table, cu_chunk_lens, chunk_starts,
+                            dequant_scale));
   return launched(mla::launch_gather(a, mode, (int)out_dtype, cfg_for(stream)), what);
 }
 
@@ -414,13 +442,16 @@ struct PagedKpe {
   int32_t num_seqs;
 };
 
-mla_status_t pack_impl(const void* k_nope, int64_t kn_token_stride, int64_t kn_head_stride,
+// Validates a pack and fills its launch arguments (a.num_tokens == 0: valid,
+// nothing to launch).
+mla_status_t pack_prep(const void* k_nope, int64_t kn_token_stride, int64_t kn_head_stride,
                        const void* v, int64_t v_token_stride, int64_t v_head_stride,
                        mla_dtype_t in_dtype, const void* k_pe, int64_t kpe_token_stride, mla_dtype_t kpe_dtype,
                        const PagedKpe* paged, int32_t num_tokens, int32_t num_heads,
                        int32_t nope_dim, int32_t rope_dim, int32_t v_dim, void* key_out,
                        void* v_out, mla_dtype_t out_dtype, const float* out_scale,
-                       uint32_t* err_word, mla_stream_t stream, const char* what) {
+                       uint32_t* err_word, mla::PackArgs& a) {
+  a = mla::PackArgs{};
   if (num_tokens < 0) return fail(MLA_ERR_INVALID_ARG, "num_tokens must be >= 0");
   if (num_heads <= 0) return fail(MLA_ERR_INVALID_ARG, "num_heads must be >= 1");
   if ((int64_t)num_tokens * ((num_heads + 3) / 4) >= (int64_t(1) << 32))
@@ -466,6 +497,7 @@ mla_status_t pack_impl(const void* k_nope, int64_t kn_token_stride, int64_t kn_h
     return fail(MLA_ERR_MISALIGNED, "out_scale must be 4-byte aligned");
   if (err_word && (reinterpret_cast<uintptr_t>(err_word) & 3))
     return fail(MLA_ERR_MISALIGNED, "err_word must be 4-byte aligned");
+  a.num_tokens = num_tokens;
   if (num_tokens == 0) return MLA_OK;  // empty inputs may have null data pointers
   if (!k_nope || !key_out || (v_out && !v))
     return fail(MLA_ERR_INVALID_ARG, "k_nope, key_out (and v when v_out is set) must be non-null");
@@ -474,21 +506,6 @@ mla_status_t pack_impl(const void* k_nope, int64_t kn_token_stride, int64_t kn_h
                 paged ? "kv_cache, block_table, cu_chunk_lens and chunk_starts must be non-null"
                       : "k_pe must be non-null");
 
-  MLA_TRY(check_device_ptr(k_nope, "k_nope"));
-  if (v_out) {
-    MLA_TRY(check_device_ptr(v, "v"));
-    MLA_TRY(check_device_ptr(v_out, "v_out"));
-  }
-  MLA_TRY(check_device_ptr(key_out, "key_out"));
-  if (out_scale) MLA_TRY(check_device_ptr(out_scale, "out_scale"));
-  if (paged) {
-    MLA_TRY(check_device_ptr(paged->kv_cache, "kv_cache"));
-    MLA_TRY(check_paged_ptrs(paged->block_table, paged->cu, paged->starts));
-  } else {
-    MLA_TRY(check_device_ptr(k_pe, "k_pe"));
-  }
-
-  mla::PackArgs a{};
   a.k_nope = static_cast<const uint8_t*>(k_nope);
   a.kn_ts = kn_token_stride * 2;
   a.kn_hs = kn_head_stride * 2;
@@ -509,10 +526,58 @@ mla_status_t pack_impl(const void* k_nope, int64_t kn_token_stride, int64_t kn_h
                         paged->block_table_stride, paged->cu, paged->starts, paged->num_seqs);
     a.pe_off = paged->rope_offset * ke;
   }
+  return MLA_OK;
+}
+
+// The device-pointer checks of a pack that pack_prep accepted with tokens.
+mla_status_t pack_ptr_checks(const void* k_nope, const void* v, const void* k_pe,
+                             const PagedKpe* paged, const void* key_out, const void* v_out,
+                             const float* out_scale) {
+  MLA_TRY(check_device_ptr(k_nope, "k_nope"));
+  if (v_out) {
+    MLA_TRY(check_device_ptr(v, "v"));
+    MLA_TRY(check_device_ptr(v_out, "v_out"));
+  }
+  MLA_TRY(check_device_ptr(key_out, "key_out"));
+  if (out_scale) MLA_TRY(check_device_ptr(out_scale, "out_scale"));
+  if (paged) {
+    MLA_TRY(check_device_ptr(paged->kv_cache, "kv_cache"));
+    return check_paged_ptrs(paged->block_table, paged->cu, paged->starts);
+  }
+  return check_device_ptr(k_pe, "k_pe");
+}
+
+mla_status_t pack_impl(const void* k_nope, int64_t kn_token_stride, int64_t kn_head_stride,
+                       const void* v, int64_t v_token_stride, int64_t v_head_stride,
+                       mla_dtype_t in_dtype, const void* k_pe, int64_t kpe_token_stride, mla_dtype_t kpe_dtype,
+                       const PagedKpe* paged, int32_t num_tokens, int32_t num_heads,
+                       int32_t nope_dim, int32_t rope_dim, int32_t v_dim, void* key_out,
+                       void* v_out, mla_dtype_t out_dtype, const float* out_scale,
+                       uint32_t* err_word, mla_stream_t stream, const char* what) {
+  mla::PackArgs a;
+  MLA_TRY(pack_prep(k_nope, kn_token_stride, kn_head_stride, v, v_token_stride, v_head_stride,
+                    in_dtype, k_pe, kpe_token_stride, kpe_dtype, paged, num_tokens, num_heads,
+                    nope_dim, rope_dim, v_dim, key_out, v_out, out_dtype, out_scale, err_word, a));
+  if (num_tokens == 0) return MLA_OK;
+  MLA_TRY(pack_ptr_checks(k_nope, v, k_pe, paged, key_out, v_out, out_scale));
   return launched(mla::launch_pack(a, (int)in_dtype, (int)out_dtype, (int)kpe_dtype,
                                    paged != nullptr, cfg_for(stream)),
                   what);
 }
+
+// [lo, hi) byte span of rows of `row_bytes` at `rows` row starts `stride` apart
+// (plus an inner head dimension), for the fused call's overlap check.
+struct Span {
+  uintptr_t lo, hi;
+};
+Span span_of(const void* base, int64_t rows, int64_t row_stride_b, int64_t heads,
+             int64_t head_stride_b, int64_t row_bytes) {
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(base);
+  if (!base || rows <= 0) return Span{lo, lo};
+  const int64_t last = (rows - 1) * row_stride_b + (heads - 1) * head_stride_b + row_bytes;
+  return Span{lo, lo + (uintptr_t)last};
+}
+bool overlaps(Span a, Span b) { return a.lo < b.hi && b.lo < a.hi; }
 
 }  // namespace
 
@@ -648,6 +713,71 @@ mla_status_t mla_norm_rope_grouped(const void* kv_c, int64_t kvc_token_stride,
   a.op_ls = out_pe_layer_stride * 2;
   a.err = err_word;
   return launched(mla::launch_norm_rope(a, norm, rope, cfg_for(stream)), "mla_norm_rope_grouped");
+}
+
+mla_status_t mla_context_kv_pack_gather(const mla_kv_pack_t* pack,
+                                        const mla_context_gather_t* next_gather,
+                                        uint32_t* gather_err_word, mla_stream_t stream) {
+  if (!pack || !next_gather)
+    return fail(MLA_ERR_INVALID_ARG, "pack and next_gather must be non-null");
+  const mla_kv_pack_t& p = *pack;
+  const mla_context_gather_t& g = *next_gather;
+  if (!is16(p.in_dtype))
+    return fail(valid_dtype(p.in_dtype) ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG,
+                "k_nope and v must be MLA_BF16 or MLA_FP16 (in_dtype)");
+  if (g.out_dtype != g.cache_dtype && g.out_dtype != p.in_dtype)
+    return fail(MLA_ERR_UNSUPPORTED,
+                "the gather's out_dtype must equal its cache_dtype (raw) or the pack's in_dtype "
+                "(widened from an fp8 cache)");
+  mla::PackArgs pa;
+  MLA_TRY(pack_prep(p.k_nope, p.kn_token_stride, p.kn_head_stride, p.v, p.v_token_stride,
+                    p.v_head_stride, p.in_dtype, p.k_pe, p.kpe_token_stride, p.kpe_dtype, nullptr,
+                    p.num_tokens, p.num_heads, p.nope_dim, p.rope_dim, p.v_dim, p.key_out,
+                    p.v_out, p.out_dtype, p.out_scale, nullptr, pa));
+  mla::GatherArgs ga;
+  int gmode = 0;
+  MLA_TRY(gather_prep(g.kv_cache, g.cache_dtype, g.num_blocks, g.block_size, g.block_stride,
+                      g.entry_stride, g.entry_dim, g.block_table, g.block_table_stride,
+                      g.cu_chunk_lens, g.chunk_starts, g.num_seqs, g.num_tokens, g.out,
+                      g.out_row_stride, g.out_dtype, nullptr, gather_err_word, ga, &gmode));
+  if (p.num_tokens > 0 && g.num_tokens > 0) {
+    // the gather writes nothing the pack reads or writes
+    const int ie = 2, oe = elt_size(p.out_dtype), ke = elt_size(p.kpe_dtype);
+    const Span out = span_of(g.out, g.num_tokens, g.out_row_stride * elt_size(g.out_dtype), 1, 0,
+                             (int64_t)g.entry_dim * elt_size(g.out_dtype));
+    const Span ins[] = {
+        span_of(p.k_nope, p.num_tokens, p.kn_token_stride * ie, p.num_heads, p.kn_head_stride * ie,
+                (int64_t)p.nope_dim * ie),
+        p.v_out ? span_of(p.v, p.num_tokens, p.v_token_stride * ie, p.num_heads,
+                          p.v_head_stride * ie, (int64_t)p.v_dim * ie)
+                : Span{0, 0},
+        span_of(p.k_pe, p.num_tokens, p.kpe_token_stride * ke, 1, 0, (int64_t)p.rope_dim * ke),
+        span_of(p.key_out, p.num_tokens, (int64_t)p.num_heads * (p.nope_dim + p.rope_dim) * oe, 1,
+                0, (int64_t)p.num_heads * (p.nope_dim + p.rope_dim) * oe),
+        p.v_out ? span_of(p.v_out, p.num_tokens, (int64_t)p.num_heads * p.v_dim * oe, 1, 0,
+                          (int64_t)p.num_heads * p.v_dim * oe)
+                : Span{0, 0}};
+    for (const Span& sp : ins)
+      if (overlaps(out, sp))
+        return fail(MLA_ERR_INVALID_ARG,
+                    "the gather's output overlaps a buffer of the pack (use a second workspace)");
+  }
+  if (p.num_tokens > 0)
+    MLA_TRY(pack_ptr_checks(p.k_nope, p.v, p.k_pe, nullptr, p.key_out, p.v_out, p.out_scale));
+  if (g.num_tokens > 0)
+    MLA_TRY(gather_ptr_checks(g.kv_cache, g.out, g.block_table, g.cu_chunk_lens, g.chunk_starts,
+                              nullptr));
+  if (p.num_tokens == 0 && g.num_tokens == 0) return MLA_OK;
+  if (p.num_tokens == 0)
+    return launched(mla::launch_gather(ga, gmode, (int)g.out_dtype, cfg_for(stream)),
+                    "mla_context_kv_pack_gather");
+  if (g.num_tokens == 0)
+    return launched(mla::launch_pack(pa, (int)p.in_dtype, (int)p.out_dtype, (int)p.kpe_dtype,
+                                     false, cfg_for(stream)),
+                    "mla_context_kv_pack_gather");
+  return launched(mla::launch_pack(pa, (int)p.in_dtype, (int)p.out_dtype, (int)p.kpe_dtype, false,
+                                   cfg_for(stream), &ga, gmode),
+                  "mla_context_kv_pack_gather");
 }
 
 mla_status_t mla_rope_cos_sin_cache(float* out, int64_t max_position, int32_t rot_dim,

@@ -119,9 +119,12 @@ cudaError_t launch_insert(const InsertArgs& a, int cache_fmt, bool norm, bool ro
 // bf16 times the scale when a.dequant_scale is set).
 cudaError_t launch_gather(const GatherArgs& a, int mode, int out_fmt, const LaunchCfg& cfg);
 // in_fmt: kBF16 or kF16 (k_nope / v); paged: k_pe from a.paged (kpe_fmt = the
-// cache's format) instead of a.k_pe.
+// cache's format) instead of a.k_pe.  next_gather (not paged): the same launch
+// also runs that gather (gather_mode 0: raw copy, or the cache's fp8 format
+// widened to in_fmt; its num_tokens > 0).
 cudaError_t launch_pack(const PackArgs& a, int in_fmt, int out_fmt, int kpe_fmt, bool paged,
-                        const LaunchCfg& cfg);
+                        const LaunchCfg& cfg, const GatherArgs* next_gather = nullptr,
+                        int gather_mode = 0);
 cudaError_t launch_norm_rope(const NormRopeArgs& a, bool norm, bool rope, const LaunchCfg& cfg);
 cudaError_t launch_rope_table(float* out, int64_t max_position, int32_t rot_dim, double base,
                               const LaunchCfg& cfg);

@@ -5,12 +5,15 @@
 namespace mla {
 
 cudaError_t launch_pack_f16(const PackArgs& a, int out_fmt, int kpe_fmt, bool paged,
+                            const GatherArgs* next_gather, int gather_mode,
                             const LaunchCfg& cfg);
 
 cudaError_t launch_pack(const PackArgs& a, int in_fmt, int out_fmt, int kpe_fmt, bool paged,
-                        const LaunchCfg& cfg) {
-  if (in_fmt == kF16) return launch_pack_f16(a, out_fmt, kpe_fmt, paged, cfg);
-  if (in_fmt == kBF16) return launch_pack_in<kBF16>(a, out_fmt, kpe_fmt, paged, cfg);
+                        const LaunchCfg& cfg, const GatherArgs* next_gather, int gather_mode) {
+  if (in_fmt == kF16)
+    return launch_pack_f16(a, out_fmt, kpe_fmt, paged, next_gather, gather_mode, cfg);
+  if (in_fmt == kBF16)
+    return launch_pack_in<kBF16>(a, out_fmt, kpe_fmt, paged, next_gather, gather_mode, cfg);
   return cudaErrorInvalidValue;
 }
 

@@ -6,8 +6,9 @@
 namespace mla {
 
 cudaError_t launch_pack_f16(const PackArgs& a, int out_fmt, int kpe_fmt, bool paged,
+                            const GatherArgs* next_gather, int gather_mode,
                             const LaunchCfg& cfg) {
-  return launch_pack_in<kF16>(a, out_fmt, kpe_fmt, paged, cfg);
+  return launch_pack_in<kF16>(a, out_fmt, kpe_fmt, paged, next_gather, gather_mode, cfg);
 }
 
 }  // namespace mla

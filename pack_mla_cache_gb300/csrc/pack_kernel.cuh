@@ -32,8 +32,11 @@
 // slice and, for a bad block index or id, sets MLA_ERRBIT_BLOCK_OOB.
 #pragma once
 
+#include <algorithm>
+
 #include "mla_device.cuh"
 #include "mla_internal.h"
+#include "gather_rows.cuh"
 #include "paged.cuh"
 
 namespace mla {
@@ -95,22 +98,23 @@ __device__ __forceinline__ void put_pe(uint8_t* dst, const uint4& o16, const uin
 // ---- plain vectorised variant -------------------------------------------------
 constexpr int kThreads = 256;
 
+// The items of one warp: warp0, warp0 + nwarps, ...
 template <int OF, int KF, int IF, bool FAST, bool PAGED>
-__device__ __forceinline__ void pack_plain_items(const PackArgs& a, const DivConst& k) {
+__device__ __forceinline__ void pack_plain_items(const PackArgs& a, const DivConst& k,
+                                                 int64_t warp0, int64_t nwarps) {
   constexpr int OE = is16(OF) ? 2 : 1;
   constexpr int kGroup = group_of<PAGED>();
   const int lane = threadIdx.x & 31, H = a.num_heads;
   const int groups = (H + kGroup - 1) / kGroup;
   const int gshift = (groups & (groups - 1)) ? -1 : __ffs(groups) - 1;
   const int64_t n_items = (int64_t)a.num_tokens * groups;
-  const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
   const bool has_v = a.vout != nullptr;
   const int part_pe = lane & 7;
   const int half = lane >> 4, part = lane & 15;  // v half (lanes 16-31) / unit in the half
   SeqLanes sl{};
   if constexpr (PAGED) sl = load_seq_lanes(a.paged, lane);
   uint32_t errbits = 0;
-  for (int64_t j = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5; j < n_items; j += nwarps) {
+  for (int64_t j = warp0; j < n_items; j += nwarps) {
     const Item it = item_of<kGroup>(j, groups, gshift, H);
     const uint8_t* pe;
     if constexpr (PAGED) {
@@ -153,9 +157,9 @@ __device__ __forceinline__ void pack_plain_items(const PackArgs& a, const DivCon
   }
 }
 
+// The pack's part of a launch: its warps are warp0, warp0 + nwarps, ...
 template <int OF, int KF, int IF, bool PAGED>
-__global__ void __launch_bounds__(kThreads) pack_kernel(const PackArgs a) {
-  pdl_trigger();
+__device__ __forceinline__ void pack_part(const PackArgs& a, int64_t warp0, int64_t nwarps) {
   pdl_wait();
   float scale = 1.0f;
   if constexpr (!is16(OF)) {
@@ -163,12 +167,58 @@ __global__ void __launch_bounds__(kThreads) pack_kernel(const PackArgs a) {
   }
   const DivConst k = div_const(scale);
   if constexpr (is16(OF)) {
-    pack_plain_items<OF, KF, IF, true, PAGED>(a, k);
+    pack_plain_items<OF, KF, IF, true, PAGED>(a, k, warp0, nwarps);
   } else {
-    if (k.fast) pack_plain_items<OF, KF, IF, true, PAGED>(a, k);
-    else pack_plain_items<OF, KF, IF, false, PAGED>(a, k);
+    if (k.fast) pack_plain_items<OF, KF, IF, true, PAGED>(a, k, warp0, nwarps);
+    else pack_plain_items<OF, KF, IF, false, PAGED>(a, k, warp0, nwarps);
   }
 }
+
+template <int OF, int KF, int IF, bool PAGED>
+__global__ void __launch_bounds__(kThreads) pack_kernel(const PackArgs a) {
+  pdl_trigger();
+  pack_part<OF, KF, IF, PAGED>(a, ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5,
+                               ((int64_t)gridDim.x * kThreads) >> 5);
+}
+
+// ---- the pack of one chunk and the gather of the next, one launch -------------
+// In the chunk loop (gather chunk c -> kv_b_proj -> pack chunk c), the gather
+// of chunk c + 1 depends only on the cache and its tables, so it can run in
+// chunk c's pack launch (into the other of two workspaces): one launch per
+// chunk instead of two.  Measured on the benchmark's chunks, each launch costs
+// a fixed ~2.4 us (pack) or ~1.5 us (gather) on top of its bytes at 6.4 TB/s
+// (ramp-up and drain around the programmatic-launch handoff); the gather's
+// dependent row lookups also hide under the pack's streaming here.  The first
+// gather_ctas CTAs gather (one row per warp per iteration, gather_rows.cuh),
+// the others pack; gmode is 0 (raw copy) or the cache's fp8 format widened to
+// the pack's 16-bit input format IF.
+template <int OF, int KF, int IF>
+__global__ void __launch_bounds__(kThreads) pack_gather_kernel(const PackArgs a,
+                                                               const GatherArgs g,
+                                                               int gather_ctas, int gmode) {
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  constexpr int kWarps = kThreads / 32;
+  if ((int)blockIdx.x < gather_ctas) {
+    uint32_t errbits = 0;
+    const int64_t w = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    const int64_t nw = (int64_t)gather_ctas * kWarps;
+    if (gmode == kE4M3) gather_rows<kE4M3, IF, false>(g, w, nw, lane, errbits);
+    else if (gmode == kE5M2) gather_rows<kE5M2, IF, false>(g, w, nw, lane, errbits);
+    else gather_rows<0, IF, false>(g, w, nw, lane, errbits);
+    errbits = __reduce_or_sync(0xFFFFFFFFu, errbits);
+    if (errbits && lane == 0 && g.err) atomicOr(g.err, errbits);
+    return;
+  }
+  pack_part<OF, KF, IF, false>(
+      a, (int64_t)(blockIdx.x - gather_ctas) * kWarps + (threadIdx.x >> 5),
+      (int64_t)(gridDim.x - gather_ctas) * kWarps);
+}
+
+// Share of the CTAs that gather when the grid is capped: the gather moves far
+// fewer bytes but its rows are a chain of dependent loads, so it gets about
+// twice its share of the bytes.
+constexpr int kGatherShareDiv = 6;
 
 cudaLaunchConfig_t base_cfg(const LaunchCfg& cfg, cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t lc = {};
@@ -194,7 +244,41 @@ cudaError_t launch_plain_t(const PackArgs& a, const LaunchCfg& cfg) {
 }
 
 template <int OF, int KF, int IF>
-cudaError_t launch_variant(const PackArgs& a, bool paged, const LaunchCfg& cfg) {
+cudaError_t launch_pack_gather_t(const PackArgs& a, const GatherArgs& g, int gmode,
+                                 const LaunchCfg& cfg) {
+  auto kern = pack_gather_kernel<OF, KF, IF>;
+  constexpr int kGroup = group_of<false>();
+  constexpr int kWarps = kThreads / 32;
+  const int64_t items = (int64_t)a.num_tokens * ((a.num_heads + kGroup - 1) / kGroup);
+  const int64_t pack_ctas = (items + kWarps - 1) / kWarps;
+  const int64_t gather_ctas = ((int64_t)g.num_tokens + kWarps - 1) / kWarps;
+  const int resident = capped_grid(reinterpret_cast<const void*>(kern), kThreads,
+                                   int64_t(1) << 30);
+  int grid, gctas;
+  if (pack_ctas + gather_ctas <= resident) {  // one wave: a warp per row and per item
+    grid = (int)(pack_ctas + gather_ctas);
+    gctas = (int)gather_ctas;
+  } else {
+    grid = resident;
+    gctas = (int)std::min<int64_t>(gather_ctas, std::max(1, resident / kGatherShareDiv));
+    if (pack_ctas < grid - gctas) grid = gctas + (int)pack_ctas;
+  }
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t lc = base_cfg(cfg, attr);
+  lc.gridDim = dim3(grid);
+  lc.blockDim = dim3(kThreads);
+  return cudaLaunchKernelEx(&lc, kern, a, g, gctas, gmode);
+}
+
+// The leaf of the dispatch: the plain or paged pack, or (next_gather set; not
+// paged) the pack with the next chunk's gather in the same launch.
+template <int OF, int KF, int IF>
+cudaError_t launch_variant(const PackArgs& a, bool paged, const GatherArgs* next_gather,
+                           int gmode, const LaunchCfg& cfg) {
+  if (next_gather) {
+    if (paged) return cudaErrorInvalidValue;
+    return launch_pack_gather_t<OF, KF, IF>(a, *next_gather, gmode, cfg);
+  }
   return paged ? launch_plain_t<OF, KF, IF, true>(a, cfg)
                : launch_plain_t<OF, KF, IF, false>(a, cfg);
 }
@@ -203,13 +287,14 @@ cudaError_t launch_variant(const PackArgs& a, bool paged, const LaunchCfg& cfg) 
 // k_pe is copied raw into an fp8 key of its own format or widened into a
 // 16-bit key.
 template <int OF, int IF>
-cudaError_t launch_kpe(const PackArgs& a, int kpe_fmt, bool paged, const LaunchCfg& cfg) {
-  if (kpe_fmt == IF) return launch_variant<OF, IF, IF>(a, paged, cfg);
+cudaError_t launch_kpe(const PackArgs& a, int kpe_fmt, bool paged, const GatherArgs* ng,
+                       int gmode, const LaunchCfg& cfg) {
+  if (kpe_fmt == IF) return launch_variant<OF, IF, IF>(a, paged, ng, gmode, cfg);
   if constexpr (is16(OF) || OF == kE4M3) {
-    if (kpe_fmt == kE4M3) return launch_variant<OF, kE4M3, IF>(a, paged, cfg);
+    if (kpe_fmt == kE4M3) return launch_variant<OF, kE4M3, IF>(a, paged, ng, gmode, cfg);
   }
   if constexpr (is16(OF) || OF == kE5M2) {
-    if (kpe_fmt == kE5M2) return launch_variant<OF, kE5M2, IF>(a, paged, cfg);
+    if (kpe_fmt == kE5M2) return launch_variant<OF, kE5M2, IF>(a, paged, ng, gmode, cfg);
   }
   return cudaErrorInvalidValue;
 }
@@ -218,11 +303,11 @@ cudaError_t launch_kpe(const PackArgs& a, int kpe_fmt, bool paged, const LaunchC
 // format).
 template <int IF>
 cudaError_t launch_pack_in(const PackArgs& a, int out_fmt, int kpe_fmt, bool paged,
-                           const LaunchCfg& cfg) {
+                           const GatherArgs* ng, int gmode, const LaunchCfg& cfg) {
   switch (out_fmt) {
-    case IF: return launch_kpe<IF, IF>(a, kpe_fmt, paged, cfg);
-    case kE4M3: return launch_kpe<kE4M3, IF>(a, kpe_fmt, paged, cfg);
-    case kE5M2: return launch_kpe<kE5M2, IF>(a, kpe_fmt, paged, cfg);
+    case IF: return launch_kpe<IF, IF>(a, kpe_fmt, paged, ng, gmode, cfg);
+    case kE4M3: return launch_kpe<kE4M3, IF>(a, kpe_fmt, paged, ng, gmode, cfg);
+    case kE5M2: return launch_kpe<kE5M2, IF>(a, kpe_fmt, paged, ng, gmode, cfg);
     default: return cudaErrorInvalidValue;
   }
 }

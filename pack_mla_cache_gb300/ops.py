@@ -31,6 +31,30 @@ class MlaError(RuntimeError):
         self.status = status
 
 
+class KvPack(ctypes.Structure):
+    _fields_ = [("k_nope", ctypes.c_void_p), ("kn_token_stride", ctypes.c_int64),
+                ("kn_head_stride", ctypes.c_int64), ("v", ctypes.c_void_p),
+                ("v_token_stride", ctypes.c_int64), ("v_head_stride", ctypes.c_int64),
+                ("in_dtype", ctypes.c_int), ("k_pe", ctypes.c_void_p),
+                ("kpe_token_stride", ctypes.c_int64), ("kpe_dtype", ctypes.c_int),
+                ("num_tokens", ctypes.c_int32), ("num_heads", ctypes.c_int32),
+                ("nope_dim", ctypes.c_int32), ("rope_dim", ctypes.c_int32),
+                ("v_dim", ctypes.c_int32), ("key_out", ctypes.c_void_p),
+                ("v_out", ctypes.c_void_p), ("out_dtype", ctypes.c_int),
+                ("out_scale", ctypes.c_void_p)]
+
+
+class ContextGather(ctypes.Structure):
+    _fields_ = [("kv_cache", ctypes.c_void_p), ("cache_dtype", ctypes.c_int),
+                ("num_blocks", ctypes.c_int64), ("block_size", ctypes.c_int32),
+                ("block_stride", ctypes.c_int64), ("entry_stride", ctypes.c_int64),
+                ("entry_dim", ctypes.c_int32), ("block_table", ctypes.c_void_p),
+                ("block_table_stride", ctypes.c_int64), ("cu_chunk_lens", ctypes.c_void_p),
+                ("chunk_starts", ctypes.c_void_p), ("num_seqs", ctypes.c_int32),
+                ("num_tokens", ctypes.c_int32), ("out", ctypes.c_void_p),
+                ("out_row_stride", ctypes.c_int64), ("out_dtype", ctypes.c_int)]
+
+
 class NormRope(ctypes.Structure):
     _fields_ = [("gamma", ctypes.c_void_p), ("gamma_layer_stride", ctypes.c_int64),
                 ("eps", ctypes.c_float), ("positions", ctypes.c_void_p),
@@ -71,6 +95,8 @@ SIGNATURES = {
         _vp, _i64, _i64, _vp, _i64, _i64, _i32, _i32, _i32, _i32, ctypes.POINTER(NormRope), _vp,
         _i64, _i64, _vp, _i64, _i64, _vp, _vp]),
     "mla_rope_cos_sin_cache": (ctypes.c_int, [_vp, _i64, _i32, ctypes.c_double, _vp]),
+    "mla_context_kv_pack_gather": (ctypes.c_int, [ctypes.POINTER(KvPack),
+                                                  ctypes.POINTER(ContextGather), _vp, _vp]),
 }
 
 
@@ -273,3 +299,36 @@ def mla_rope_cos_sin_cache(out, base=10000.0, *, stream=None):
     """Fill out (fp32 [max_position, rot_dim]) with the rotary cos/sin table."""
     _check(lib().mla_rope_cos_sin_cache(_ptr(out), out.shape[0], out.shape[1], float(base),
                                         _stream(stream)))
+
+
+def kv_pack_desc(k_nope, v, k_pe, key_out, v_out, out_dtype, *, kpe_dtype=None, out_scale=None,
+                 in_dtype=None) -> KvPack:
+    """The arguments of ``mla_context_kv_pack`` as the C struct."""
+    T, H, N = k_nope.shape
+    return KvPack(_ptr(k_nope), k_nope.stride(0), k_nope.stride(1), _ptr(v), v.stride(0),
+                  v.stride(1), dtype_code(in_dtype if in_dtype is not None else k_nope.dtype),
+                  _ptr(k_pe), k_pe.stride(0),
+                  dtype_code(kpe_dtype if kpe_dtype is not None else k_pe.dtype), T, H, N,
+                  k_pe.shape[-1], v.shape[2], _ptr(key_out), _ptr(v_out), dtype_code(out_dtype),
+                  _ptr(out_scale))
+
+
+def context_gather_desc(kv_cache, cache_dtype, num_blocks, block_size, block_stride,
+                        entry_stride, entry_dim, block_table, cu_chunk_lens, chunk_starts, out,
+                        out_dtype, *, num_tokens=None) -> ContextGather:
+    """The arguments of ``mla_context_gather`` as the C struct."""
+    n = out.shape[0] if num_tokens is None else num_tokens
+    return ContextGather(_ptr(kv_cache), dtype_code(cache_dtype), num_blocks, block_size,
+                         block_stride, entry_stride, entry_dim, _ptr(block_table),
+                         _bt_stride(block_table), _ptr(cu_chunk_lens), _ptr(chunk_starts),
+                         chunk_starts.shape[0], n, _ptr(out), out.stride(0),
+                         dtype_code(out_dtype))
+
+
+def mla_context_kv_pack_gather(pack: KvPack, next_gather: ContextGather, *, err_word=None,
+                               stream=None):
+    """One launch: the pack described by ``pack`` (``kv_pack_desc``) and the
+    gather described by ``next_gather`` (``context_gather_desc``); the gather
+    must write a workspace the pack does not use."""
+    _check(lib().mla_context_kv_pack_gather(ctypes.byref(pack), ctypes.byref(next_gather),
+                                            _ptr(err_word), _stream(stream)))

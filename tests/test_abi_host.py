@@ -391,3 +391,63 @@ def test_error_message_is_thread_local(L):
     t.join()
     assert seen == [""]
     assert "num_tokens" in ops.mla_last_error()
+
+
+# ------------------------------------------------ pack + next gather, one launch
+def fused_descs(**kw):
+    """Descriptors of an fp8 pack (8192 tokens, 16 heads, k_pe from workspace
+    A) and a raw fp8 gather of 8192 rows into workspace B (fake addresses)."""
+    ws_a, ws_b = A + (1 << 30), A + (1 << 31)
+    p = dict(k_nope=A, kn_token_stride=4160, kn_head_stride=256, v=A + 256, v_token_stride=4160,
+             v_head_stride=256, in_dtype=0, k_pe=ws_a + 1024, kpe_token_stride=576, kpe_dtype=1,
+             num_tokens=8192, num_heads=16, nope_dim=128, rope_dim=64, v_dim=128,
+             key_out=A + (1 << 32), v_out=A + (1 << 33), out_dtype=1, out_scale=A + 64)
+    g = dict(kv_cache=A + (1 << 34), cache_dtype=1, num_blocks=1024, block_size=64,
+             block_stride=64 * 576, entry_stride=576, entry_dim=576, block_table=A + 4096,
+             block_table_stride=512, cu_chunk_lens=A + 8192, chunk_starts=A + 12288, num_seqs=1,
+             num_tokens=8192, out=ws_b, out_row_stride=576, out_dtype=1)
+    for k, v in kw.items():  # g_<name>: the gather's field of that name
+        if k.startswith("g_"):
+            g[k[2:]] = v
+        else:
+            (p if k in p else g)[k] = v
+    return ops.KvPack(**p), ops.ContextGather(**g)
+
+
+def fused(L, **kw):
+    import ctypes
+    pk, gk = fused_descs(**kw)
+    return L.mla_context_kv_pack_gather(ctypes.byref(pk), ctypes.byref(gk), None, None)
+
+
+def test_fused_pack_gather_argument_checks(L):
+    import ctypes
+    pk, gk = fused_descs()
+    assert L.mla_context_kv_pack_gather(None, ctypes.byref(gk), None, None) == \
+        ops.MLA_ERR_INVALID_ARG
+    assert L.mla_context_kv_pack_gather(ctypes.byref(pk), None, None, None) == \
+        ops.MLA_ERR_INVALID_ARG
+    # the gather must write its cache's type or the pack's input type
+    assert fused(L, out_dtype=0, in_dtype=3, kn_token_stride=4160) == ops.MLA_ERR_UNSUPPORTED
+    # the pack half keeps its own rules (bad head count), the gather half its own
+    assert fused(L, num_heads=0) == ops.MLA_ERR_INVALID_ARG
+    assert fused(L, num_seqs=0) == ops.MLA_ERR_INVALID_ARG
+    # both halves empty: nothing to do, no CUDA call
+    assert fused(L, num_tokens=0, g_num_tokens=0) == ops.MLA_OK
+
+
+@pytest.mark.parametrize("target", ["k_pe", "k_nope", "key_out", "v_out"])
+def test_fused_pack_gather_rejects_overlap_before_any_cuda_call(L, target):
+    """The gather's output must not overlap any buffer of the pack; the check
+    runs before any CUDA call, so it is the error even without a GPU."""
+    pk, _ = fused_descs()
+    addr = getattr(pk, target) + 64
+    assert fused(L, out=addr) == ops.MLA_ERR_INVALID_ARG
+    assert "overlaps" in ops.mla_last_error()
+
+
+def test_fused_pack_gather_without_gpu_reports_cuda_error(L):
+    if torch.cuda.is_available():
+        pytest.skip("this check is for machines without a GPU")
+    assert fused(L) == ops.MLA_ERR_CUDA
+    assert "cudaPointerGetAttributes" in ops.mla_last_error()
