@@ -6,10 +6,13 @@ One step = one pass of the whole path over one batch, the large workload:
     shared slot mapping;
   * chunked-context pack of 131072 context tokens = 16 chunks of 8192: per
     chunk a gather of the latent rows from an fp8 e4m3 paged cache (2048
-    blocks, random block table) into a reused workspace, then the K/V pack of
-    that chunk's kv_b_proj output [8192, 16 x (128 + 128)] bf16 (row stride
-    4160) into a contiguous fp8 e4m3 key [8192, 16, 192] and V [8192, 16, 128]
-    (scale 0.01).
+    blocks, random block table) into a workspace, then the K/V pack of that
+    chunk's kv_b_proj output [8192, 16 x (128 + 128)] bf16 (row stride 4160)
+    into a contiguous fp8 e4m3 key [8192, 16, 192] and V [8192, 16, 128]
+    (scale 0.01).  The chunk loop is software-pipelined: the gather of chunk 0,
+    then per chunk c one launch that packs c and gathers c + 1 into the other
+    of two workspaces (mla_context_kv_pack_gather); the unfused loop (a gather
+    and a pack launch per chunk) is timed beside it.
 The step's inputs (insert 377 MB, kv_b_proj 1.09 GB, cache 75 MB) are larger
 than L2, so no flush is needed between steps.  value = algorithmic bytes of a
 step / device time of a step (CUDA-graph replay, CUDA events on the launching
@@ -17,8 +20,8 @@ stream).  Algorithmic bytes read every input once and write every output once:
 insert 1728 B per (token, layer) + 272 B per token; gather 1152 B per token;
 pack 13376 B per token.
 
-``--impl reference`` times the CPU oracle (plain single-threaded C) on a
-bounded sample of the same workload instead.
+``--impl reference`` times the CPU oracle (plain C, its independent rows split
+over the host's cores) on a bounded sample of the same workload instead.
 """
 from __future__ import annotations
 
@@ -313,6 +316,7 @@ class Workload:
                                          kpe_dtype=1, out_scale=self.out_scale)
 
     launches_per_step = 1 + 2 * (T_CTX // CHUNK)
+    launches_per_step_pipelined = 2 + T_CTX // CHUNK
 
 
 def graph_of(fn, stream):
@@ -468,12 +472,13 @@ def run(args):
     __graft_entry__.build()
 
     w = Workload(seed=1000 + rank)
+    w.pipelined_setup()
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
         for _ in range(max(args.warmup, 3)):
-            w.step()
+            w.step_pipelined()
     torch.cuda.synchronize()
-    step_graph = graph_of(w.step, stream)
+    step_graph = graph_of(w.step_pipelined, stream)
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             step_graph.replay()
@@ -501,10 +506,14 @@ def run(args):
         g_ins = graph_of(w.insert, stream)
         g_gat = graph_of(lambda: [w.gather(c) for c in range(nch)], stream)
         g_pack = graph_of(lambda: [w.pack(c) for c in range(nch)], stream)
+        g_pg = graph_of(lambda: [w.pack_gather(c) for c in range(nch)], stream)
+        g_plain = graph_of(w.step, stream)
         reps = max(3, args.steps)
         ms_insert = time_graph(g_ins, stream, reps)
         ms_gather = time_graph(g_gat, stream, reps) / nch
         ms_pack = time_graph(g_pack, stream, reps) / nch
+        ms_pg = time_graph(g_pg, stream, reps) / nch
+        ms_plain = time_graph(g_plain, stream, reps)
         # the whole 131072-token context packed by ONE launch (fp8 and bf16 out)
         w.one_launch_setup()
         g_one = graph_of(lambda: w.pack_one_launch(False), stream)
@@ -531,7 +540,11 @@ def run(args):
     b_pack_launch = CHUNK * B_PACK_TOK
     b_ins_launch = insert_bytes(T_INSERT, L_LAYERS)
     b_gat_launch = CHUNK * B_GATHER_TOK + (CHUNK // BS) * 4
-    ach = b_pack_launch / (ms_pack * 1e-3) / 1e9
+    nch = w.pw.num_chunks
+    # the fused launches of a step: every one packs a chunk, all but the last
+    # also gather the next chunk (average bytes per launch)
+    b_pg_launch = b_pack_launch + b_gat_launch * (nch - 1) / nch
+    ach = b_pg_launch / (ms_pg * 1e-3) / 1e9
 
     def kline(b, m):
         a = b / (m * 1e-3) / 1e9
@@ -565,15 +578,19 @@ def run(args):
         "config": {"workload": WORKLOAD, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (1.55 GB read per step), no flush",
                    "timing": "CUDA-graph replay of whole steps, CUDA events on the stream",
+                   "step": ("insert; gather of chunk 0; then per chunk c one launch packing c "
+                            "and gathering c + 1 (two workspaces)"),
+                   "ms_per_step_unfused": ms_plain,
                    "step_bytes": sbytes, "frac_of_peak": value / world / peak,
                    "peak_gbs": peak, "peak_kind": peak_kind,
                    "tokens_layers_per_s_insert": T_INSERT * L_LAYERS * world / (ms * 1e-3),
                    "context_tokens_per_s": T_CTX * world / (ms * 1e-3)},
-        "roofline": {"bound": "hbm", "kernel": "pack_kernel<e4m3,e4m3>", "achieved": ach,
-                     "peak": peak, "unit": "GB/s", "frac": ach / peak,
+        "roofline": {"bound": "hbm", "kernel": "pack_gather_kernel<e4m3,e4m3,bf16>",
+                     "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
                      "peak_source": f"{peak_kind} HBM copy bandwidth",
-                     "traffic": profile_traffic("pack_fp8_h16")},
+                     "traffic": profile_traffic("pack_gather_fp8_h16")},
         "kernels": {"insert": kline(b_ins_launch, ms_insert),
+                    "pack_gather": kline(b_pg_launch, ms_pg),
                     "gather": kline(b_gat_launch, ms_gather),
                     "pack": kline(b_pack_launch, ms_pack),
                     "pack_one_launch_131072": kline(T_CTX * B_PACK_TOK, ms_one),
@@ -583,7 +600,7 @@ def run(args):
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "ms_per_step": e2e["ms"], "runs_ms": [round(r, 3) for r in e2e["reps_ms"]],
                 "bound": "pinned H2D over the host link (210 GB/s measured on this pool's GB300 boxes)"},
-        "gpu_launches": Workload.launches_per_step * args.steps,
+        "gpu_launches": Workload.launches_per_step_pipelined * args.steps,
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
@@ -594,7 +611,7 @@ def run(args):
 
 def run_e2e(w, stream, steps):
     """Whole step through the public API from pinned host buffers: H2D of the
-    step's inputs, the 33 calls, D2H of the packed key/V; wall time between
+    step's inputs, the 18 calls, D2H of the packed key/V; wall time between
     synchronisations.  Copies and kernels overlap as a serving loop would run
     them: inputs stream in on one stream, the kernels run on the compute stream
     as each chunk's input lands (event waits), results stream out on a third;
@@ -623,10 +640,11 @@ def run_e2e(w, stream, steps):
             w.k_pe.copy_(h_k_pe, non_blocking=True)
             ev_in[n].record(s_in)
         with torch.cuda.stream(stream):
+            w.ops.mla_context_gather(w.ctx_cache, 1, NB_CTX, BS, BS * ENTRY, ENTRY, ENTRY,
+                                     w.block_table, w.cu, w.starts[0], w.ws_pair[0], 1)
             for c in range(n):
                 stream.wait_event(ev_in[c])
-                w.gather(c)
-                w.pack(c)
+                w.pack_gather(c)
                 ev_done[c].record(stream)
             stream.wait_event(ev_in[n])
             w.insert()

@@ -96,11 +96,20 @@ __device__ __forceinline__ void write_row_k(uint8_t* dst, int lane, const uint4&
 // per-pair negation is skipped; rows with special values take the guarded
 // path on the restored words.  1.3% faster insert with RMSNorm (130.0 vs
 // 131.7 us for 65536 tokens x 5 layers).
-template <int F>
+//
+// CHECK false: the caller knows no value can make the first quotient overflow
+// (normalised rows of a layer whose bound allows it, see layer_needs_check), so
+// the special-value test of each 8 values is skipped (5 of 119 us for 65536
+// tokens x 5 layers); a zero or NaN still takes the fast path correctly.
+template <int F, bool CHECK = true>
 __device__ __forceinline__ uint2 neg_bf16x8_to_fp8x8(uint4 v, const DivConst& k) {
-  const uint32_t m = umax16x2(umax16x2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
-                              umax16x2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
-  if (!special_pairs(m, k.thr2)) {
+  bool fast = true;
+  if constexpr (CHECK) {
+    const uint32_t m = umax16x2(umax16x2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                                umax16x2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+    fast = !special_pairs(m, k.thr2);
+  }
+  if (fast) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     float2 q[4];
 #pragma unroll
@@ -116,14 +125,38 @@ __device__ __forceinline__ uint2 neg_bf16x8_to_fp8x8(uint4 v, const DivConst& k)
   return bf16x8_to_fp8x8<F, true>(make_uint4(v.x ^ s, v.y ^ s, v.z ^ s, v.w ^ s), k);
 }
 
-template <int F>
-__device__ __forceinline__ void write_row_neg(uint8_t* dst, int lane, const uint4& ny0,
-                                              const uint4& ny1, uint32_t p, const DivConst& k) {
-  st8(dst + lane * 8, neg_bf16x8_to_fp8x8<F>(ny0, k));
-  st8(dst + 256 + lane * 8, neg_bf16x8_to_fp8x8<F>(ny1, k));
-  const uint32_t q = bf16x2_to_fp8x2<F, true>(p, k);
-  st_u8(dst + kR + lane, q);
-  st_u8(dst + kR + kP / 2 + lane, q >> 8);
+// The kv_c part of a row (words holding -y) into an fp8 cache.
+template <int F, bool CHECK>
+__device__ __forceinline__ void write_kv_neg(uint8_t* dst, int lane, const uint4& ny0,
+                                             const uint4& ny1, const DivConst& k) {
+  st8(dst + lane * 8, neg_bf16x8_to_fp8x8<F, CHECK>(ny0, k));
+  st8(dst + 256 + lane * 8, neg_bf16x8_to_fp8x8<F, CHECK>(ny1, k));
+}
+
+// The kv_c part of a row into a bf16 or fp8 cache.
+template <int F, bool FAST>
+__device__ __forceinline__ void write_kv_k(uint8_t* dst, int lane, const uint4& y0,
+                                           const uint4& y1, const DivConst& k) {
+  if constexpr (F == kBF16) {
+    st16(dst + lane * 16, y0);
+    st16(dst + 512 + lane * 16, y1);
+  } else {
+    st8(dst + lane * 8, bf16x8_to_fp8x8<F, FAST>(y0, k));
+    st8(dst + 256 + lane * 8, bf16x8_to_fp8x8<F, FAST>(y1, k));
+  }
+}
+
+// The k_pe pair (lane, lane + 32) of a row into a bf16 or fp8 cache.
+template <int F, bool FAST>
+__device__ __forceinline__ void write_pe_k(uint8_t* dst, int lane, uint32_t p, const DivConst& k) {
+  if constexpr (F == kBF16) {
+    st_u16(dst + 2 * kR + lane * 2, p);
+    st_u16(dst + 2 * kR + kP + lane * 2, p >> 16);
+  } else {
+    const uint32_t q = bf16x2_to_fp8x2<F, FAST>(p, k);
+    st_u8(dst + kR + lane, q);
+    st_u8(dst + kR + kP / 2 + lane, q >> 8);
+  }
 }
 
 template <int F>
@@ -261,7 +294,8 @@ struct Ring {
   static constexpr int kStages = kIConsumers * 2;
   static constexpr int kOffBars = kStages * kIStageBytes;
   static constexpr int kOffLayers = kOffBars + 2 * kStages * 8 + 16;
-  static constexpr int kSmem = kOffLayers + kMaxLayers * (8 + 4);
+  // per layer: cache base (8 B), scale (4 B), needs-check flag (1 B)
+  static constexpr int kSmem = kOffLayers + kMaxLayers * (8 + 4 + 1);
   static_assert(kStages <= 64, "a producer lane owns at most two stages");
   static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
 };
@@ -271,12 +305,12 @@ struct Ring {
 // every row's sum of squares, their warp reductions interleaved, then the
 // scaling, rotation and stores -- so a warp has kRun independent dependency
 // chains to issue from instead of one.
-template <int F, bool NORM, bool ROPE, bool FAST>
+template <int F, bool NORM, bool ROPE, bool FAST, bool CHECK>
 __device__ __forceinline__ uint32_t insert_consume_item(
     const InsertArgs& a, uint32_t src, int l, int lane, int64_t cptr, const DivConst& k,
     uint32_t empty_bar, const int64_t* slot, const int64_t* pos) {
   uint32_t err = 0;
-  // the fp8 fast path takes the normalised rows negated (write_row_neg)
+  // the fp8 fast path takes the normalised rows negated (write_kv_neg)
   constexpr bool kNeg = NORM && F != kBF16 && FAST;
   // validity and destination of every row (uniform across the warp)
   uint8_t* dst[kRun];
@@ -316,11 +350,13 @@ __device__ __forceinline__ uint32_t insert_consume_item(
     g0 = ld_shared_ro16(g + lane * 16);
     g1 = ld_shared_ro16(g + 512 + lane * 16);
   }
-  // the rows, kILP at a time in lockstep
+  // the rows' kv_c, kILP at a time in lockstep; their k_pe pairs are rotated
+  // and stored after the last row, so the cos/sin loads issued above have
+  // the whole item to arrive
+  uint32_t pe[kRun];
 #pragma unroll
   for (int h = 0; h < kRun; h += kILP) {
     uint4 x0[kILP], x1[kILP], y0[kILP], y1[kILP];
-    uint32_t pe[kILP];
 #pragma unroll
     for (int i = 0; i < kILP; ++i) {
       const uint32_t row = src + (h + i) * 2 * kR;
@@ -330,7 +366,7 @@ __device__ __forceinline__ uint32_t insert_consume_item(
       uint32_t lo, hi;
       asm volatile("ld.shared.u16 %0, [%1];" : "=r"(lo) : "r"(pr));
       asm volatile("ld.shared.u16 %0, [%1];" : "=r"(hi) : "r"(pr + kP));
-      pe[i] = lo | (hi << 16);
+      pe[h + i] = lo | (hi << 16);
     }
     if (h + kILP >= kRun) {
       // every read of the stage is done: hand it back to the producer before
@@ -355,14 +391,38 @@ __device__ __forceinline__ uint32_t insert_consume_item(
     }
 #pragma unroll
     for (int i = 0; i < kILP; ++i) {
-      const uint32_t p = ROPE ? rope_pair(pe[i], cs[h + i]) : pe[i];
       if (ok[h + i]) {
-        if constexpr (kNeg) write_row_neg<F>(dst[h + i], lane, y0[i], y1[i], p, k);
-        else write_row_k<F, FAST>(dst[h + i], lane, y0[i], y1[i], p, k);
+        if constexpr (kNeg) write_kv_neg<F, CHECK>(dst[h + i], lane, y0[i], y1[i], k);
+        else write_kv_k<F, FAST>(dst[h + i], lane, y0[i], y1[i], k);
       }
     }
   }
+#pragma unroll
+  for (int r = 0; r < kRun; ++r) {
+    if (!ok[r]) continue;
+    const uint32_t p = ROPE ? rope_pair(pe[r], cs[r]) : pe[r];
+    write_pe_k<F, FAST || F == kBF16>(dst[r], lane, p, k);
+  }
   return err;
+}
+
+// Whether normalised kv_c values of a layer can make the exact division's
+// first quotient overflow, so each group of 8 needs the special-value test.
+// A normalised element is x_i * gamma_i * rstd with x_i^2 <= sum(x^2): when
+// the row's sum of squares is finite, |y_i| <= sqrt(512) |gamma_i| (1 + 2^-7)
+// < 23 gmax, and x_i * gamma_i cannot overflow while gmax < 2^64 (|x_i| <
+// 2^64 then); when it is infinite or NaN, rstd is 0 or NaN and every y_i is
+// +-0 or NaN, which the fast path also handles.  So the test can be skipped
+// when 23 gmax stays below the first value the test would flag, 2^(T - 127)
+// with T the threshold exponent field of thr2.  gmax: the layer's largest
+// |gamma| (inf / NaN: the test stays).
+__device__ __forceinline__ bool layer_needs_check(const DivConst& k, uint32_t gmax_bits) {
+  if (!k.fast) return true;
+  const uint32_t h = k.thr2 & 0xFFFFu;           // 0x8000 - (T << 7)
+  const int T = (int)((0x8000u - h) >> 7);
+  const float lim = ldexpf(1.0f, T - 127);       // inf for T = 255
+  const float g = __uint_as_float(gmax_bits << 16);
+  return !(g < 1.8446744e19f && 23.0f * g < lim);
 }
 
 template <int F, bool NORM, bool ROPE>
@@ -373,6 +433,7 @@ __global__ void __launch_bounds__(kIThreads, 1) insert_tma_kernel(const InsertAr
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kIStages);
   int64_t* s_cptr = reinterpret_cast<int64_t*>(smem + Ring<NORM>::kOffLayers);
   float* s_scale = reinterpret_cast<float*>(s_cptr + kMaxLayers);
+  uint8_t* s_check = reinterpret_cast<uint8_t*>(s_scale + kMaxLayers);
   const uint32_t stage0 = smem_addr(smem);
   const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + kIStages);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -385,17 +446,38 @@ __global__ void __launch_bounds__(kIThreads, 1) insert_tma_kernel(const InsertAr
     *abort_flag = 0;
     mbar_fence_init();
   }
-  // No early trigger of the next launch here: its CTAs would wait resident
-  // beside this kernel's for its whole run, and in a step of chunk launches
-  // after the insert that cost ~80 us (506.7 vs 588 us per step).
+  // No early trigger of the next launch: in a step of chunk launches after the
+  // insert, a trigger at the start cost ~80 us (506.7 vs 588 us per step) and
+  // one after each CTA's last copy ~60 us (0.464 vs 0.524 ms): the launch
+  // follows the last CTA's exit.
   pdl_wait();
-  for (int l = threadIdx.x; l < a.num_layers; l += kIThreads) {
-    s_cptr[l] = a.cache_ptrs[l];
-    float sc = 1.0f;
-    if constexpr (F != kBF16) sc = a.scales[l];
-    s_scale[l] = sc;
+  __syncthreads();  // the barriers are initialised
+  // The producer starts copying at once; the consumers first fill the
+  // per-layer table (one warp per layer: cache base, scale, and whether
+  // normalised rows need the special-value test) and sync among themselves.
+  if (warp < kIConsumers) {
+    for (int l = warp; l < a.num_layers; l += kIConsumers) {
+      float sc = 1.0f;
+      if constexpr (F != kBF16) sc = a.scales[l];
+      bool check = true;
+      if constexpr (NORM && F != kBF16) {
+        const uint8_t* g = a.gamma + (int64_t)l * a.gamma_ls;
+        const uint4 g0 = ld_shared_ro16(g + lane * 16), g1 = ld_shared_ro16(g + 512 + lane * 16);
+        const uint32_t m = umax16x2(umax16x2(umax16x2(g0.x & 0x7FFF7FFFu, g0.y & 0x7FFF7FFFu),
+                                             umax16x2(g0.z & 0x7FFF7FFFu, g0.w & 0x7FFF7FFFu)),
+                                    umax16x2(umax16x2(g1.x & 0x7FFF7FFFu, g1.y & 0x7FFF7FFFu),
+                                             umax16x2(g1.z & 0x7FFF7FFFu, g1.w & 0x7FFF7FFFu)));
+        const uint32_t gmax = __reduce_max_sync(0xFFFFFFFFu, max(m & 0xFFFFu, m >> 16));
+        check = layer_needs_check(div_const(sc), gmax);
+      }
+      if (lane == 0) {
+        s_cptr[l] = a.cache_ptrs[l];
+        s_scale[l] = sc;
+        s_check[l] = check ? 1 : 0;
+      }
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kIConsumers * 32) : "memory");
   }
-  __syncthreads();
 
   const int L = a.num_layers;
   const int64_t runs = ((int64_t)a.num_tokens + kRun - 1) / kRun;
@@ -469,12 +551,15 @@ __global__ void __launch_bounds__(kIThreads, 1) insert_tma_kernel(const InsertAr
       const uint32_t src = stage0 + (uint32_t)(s * kIStageBytes);
       const DivConst k = div_const(s_scale[l]);
       const int64_t cptr = s_cptr[l];
-      if (F == kBF16 || k.fast)
-        errbits |= insert_consume_item<F, NORM, ROPE, true>(a, src, l, lane, cptr, k,
-                                                            empty0 + 8 * s, slot, pos);
+      if (F != kBF16 && !k.fast)
+        errbits |= insert_consume_item<F, NORM, ROPE, false, true>(a, src, l, lane, cptr, k,
+                                                                   empty0 + 8 * s, slot, pos);
+      else if (NORM && F != kBF16 && !s_check[l])
+        errbits |= insert_consume_item<F, NORM, ROPE, true, false>(a, src, l, lane, cptr, k,
+                                                                   empty0 + 8 * s, slot, pos);
       else
-        errbits |= insert_consume_item<F, NORM, ROPE, false>(a, src, l, lane, cptr, k,
-                                                             empty0 + 8 * s, slot, pos);
+        errbits |= insert_consume_item<F, NORM, ROPE, true, true>(a, src, l, lane, cptr, k,
+                                                                  empty0 + 8 * s, slot, pos);
     }
   }
   __syncthreads();
