@@ -166,6 +166,47 @@ __device__ __forceinline__ void write_row_dc(uint8_t* dst, int lane, const uint4
   else write_row_k<F, false>(dst, lane, y0, y1, p, k);
 }
 
+// Start of the cache row of a valid slot s (0 <= s < capacity) in the cache
+// at cptr: block s / block_size, offset s % block_size.
+__device__ __forceinline__ uint8_t* slot_dst(const InsertArgs& a, int64_t s, int64_t cptr) {
+  int64_t blk, off;
+  if (a.bs_shift >= 0) {
+    blk = s >> a.bs_shift;
+    off = s & (a.block_size - 1);
+  } else {
+    blk = s / a.block_size;
+    off = s - blk * a.block_size;
+  }
+  return reinterpret_cast<uint8_t*>(cptr) + blk * a.block_stride + off * a.entry_stride;
+}
+
+// Half-warp rows (16 lanes per row, norm_rope.cuh): the kv_c part of a row
+// held as x[4] into a bf16 or fp8 cache (fp8: NEG = the words hold -y).
+template <int F, bool FAST, bool NEG, bool CHECK>
+__device__ __forceinline__ void write_kv32(uint8_t* dst, int hl, const uint4 (&x)[4],
+                                           const DivConst& k) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    if constexpr (F == kBF16) st16(dst + hl * 16 + 256 * c, x[c]);
+    else if constexpr (NEG) st8(dst + hl * 8 + 128 * c, neg_bf16x8_to_fp8x8<F, CHECK>(x[c], k));
+    else st8(dst + hl * 8 + 128 * c, bf16x8_to_fp8x8<F, FAST>(x[c], k));
+  }
+}
+
+// The k_pe words lo (elements 2 hl, 2 hl + 1) and hi (2 hl + 32, 2 hl + 33)
+// of a row held by a half warp.
+template <int F, bool FAST>
+__device__ __forceinline__ void write_pe32(uint8_t* dst, int hl, uint32_t lo, uint32_t hi,
+                                           const DivConst& k) {
+  if constexpr (F == kBF16) {
+    *reinterpret_cast<uint32_t*>(dst + 2 * kR + hl * 4) = lo;
+    *reinterpret_cast<uint32_t*>(dst + 2 * kR + kP + hl * 4) = hi;
+  } else {
+    st_u16(dst + kR + hl * 2, bf16x2_to_fp8x2<F, FAST>(lo, k));
+    st_u16(dst + kR + kP / 2 + hl * 2, bf16x2_to_fp8x2<F, FAST>(hi, k));
+  }
+}
+
 // Normalise / rotate / convert one loaded row and store it into the cache at
 // `cptr` (its layer's base; `k` its layer's division constants).  `cs` =
 // (cos, sin) of this lane's rotary pair.  Returns the error bits of a skipped
@@ -194,7 +235,7 @@ __device__ __forceinline__ uint32_t store_row(const InsertArgs& a, int l, int la
   if constexpr (NORM) {
     const uint8_t* g = a.gamma + (int64_t)l * a.gamma_ls;
     rms_norm16(r.x0, r.x1, ld_shared_ro16(g + lane * 16), ld_shared_ro16(g + 512 + lane * 16),
-               a.eps, y0, y1);
+               a.eps, y0, y1, lane);
   }
   // k_pe pair (l, l+32), optionally rotated
   uint32_t p = r.pe;
@@ -220,8 +261,13 @@ __device__ __forceinline__ bool load_rope(const InsertArgs& a, int64_t t, int la
 // and division constants in shared memory; tiny calls (decode) skip that step,
 // which would sit on their critical path, and load them per row.
 constexpr int64_t kRowPreloadMinRows = 2048;
+// From this many rows (with RMSNorm or RoPE) the row shape takes two rows per
+// warp: 5120 rows (1024 tokens x 5 layers) ran 4.57 us with one row per warp
+// against 5.37 us with two, 10240 rows 7.43 against 7.26 us, 20480 11.34
+// against 10.94 us.
+constexpr int64_t kRowPairsMinRows = 8192;
 
-template <int F, bool NORM, bool ROPE>
+template <int F, bool NORM, bool ROPE, bool PAIRS>
 __global__ void __launch_bounds__(kThreads) insert_row_kernel(const InsertArgs a) {
   __shared__ int64_t s_cptr[kMaxLayers];
   __shared__ DivConst s_k[F == kBF16 ? 1 : kMaxLayers];
@@ -236,13 +282,10 @@ __global__ void __launch_bounds__(kThreads) insert_row_kernel(const InsertArgs a
     __syncthreads();
   }
   const int lane = threadIdx.x & 31;
+  const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
   const bool rows32 = a.num_rows < (int64_t(1) << 32);
-  uint32_t errbits = 0;
-  for (int64_t r = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5; r < a.num_rows;
-       r += nwarps) {
-    int64_t t;
-    int l;
+  auto split = [&](int64_t r, int64_t& t, int& l) {
     if (rows32) {
       const uint32_t tu = (uint32_t)r / (uint32_t)a.num_layers;
       t = tu;
@@ -251,14 +294,84 @@ __global__ void __launch_bounds__(kThreads) insert_row_kernel(const InsertArgs a
       t = r / a.num_layers;
       l = (int)(r - t * a.num_layers);
     }
-    RowIn in;
-    load_row<F, ROPE>(a, t, l, lane, in);
-    float2 cs;
-    const bool pos_ok = load_rope<ROPE>(a, t, lane, cs);
-    DivConst k{};
-    if constexpr (F != kBF16) k = pre ? s_k[l] : div_const(a.scales[l]);
-    const int64_t cptr = pre ? s_cptr[l] : a.cache_ptrs[l];
-    errbits |= store_row<F, NORM, ROPE>(a, l, lane, in, pos_ok, cs, cptr, k);
+  };
+  uint32_t errbits = 0;
+  if constexpr (PAIRS) {
+    // Two rows per warp, 16 lanes each (the half-warp layout of norm_rope.cuh):
+    // the rows 2w + half, 2w + half + 2 nwarps, ...
+    const int hl = lane & 15, half = lane >> 4;
+    for (int64_t r0 = 2 * warp; r0 < a.num_rows; r0 += 2 * nwarps) {
+      const int64_t r = r0 + half;
+      const bool have = r < a.num_rows;
+      int64_t t = 0;
+      int l = 0;
+      uint4 x[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
+                    make_uint4(0, 0, 0, 0)};
+      uint32_t lo = 0, hi = 0;
+      int64_t slot = -1, pos = 0;
+      if (have) {
+        split(r, t, l);
+        const uint8_t* src = a.kv_c + t * a.kvc_ts + (int64_t)l * a.kvc_ls + hl * 16;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) x[c] = ld_stream16(src + 256 * c);
+        const uint8_t* pe = a.k_pe + t * a.kpe_ts + (int64_t)l * a.kpe_ls + hl * 4;
+        lo = __ldcs(reinterpret_cast<const uint32_t*>(pe));
+        hi = __ldcs(reinterpret_cast<const uint32_t*>(pe + kP));
+        slot = __ldg(a.slots + (int64_t)l * a.slot_ls + t);
+        if (ROPE) pos = __ldg(a.positions + t);
+      }
+      DivConst k{};
+      int64_t cptr = 0;
+      float4 cs = make_float4(1.f, 1.f, 0.f, 0.f);
+      const uint8_t* gr = a.gamma;
+      bool ok = false;
+      uint8_t* dst = nullptr;
+      if (have) {
+        if constexpr (F != kBF16) k = pre ? s_k[l] : div_const(a.scales[l]);
+        cptr = pre ? s_cptr[l] : a.cache_ptrs[l];
+        if (slot < 0) {
+        } else if (slot >= a.capacity) {
+          errbits |= kErrSlotOOB;
+        } else if (ROPE && (pos < 0 || pos >= a.max_position)) {
+          errbits |= kErrPosOOB;
+        } else if (cptr == 0 || (cptr & 15)) {
+          errbits |= kErrMisaligned;
+        } else {
+          ok = true;
+          dst = slot_dst(a, slot, cptr);
+        }
+        if (ROPE && ok) cs = load_cs2(a.cos_sin + pos * kP, hl);
+        if constexpr (NORM) gr = a.gamma + (int64_t)l * a.gamma_ls + hl * 16;
+      }
+      // every lane: the shuffles span the warp (a lane without a row reads
+      // layer 0's weights)
+      if constexpr (NORM) rms_norm32_g(x, have ? gr : a.gamma + hl * 16, a.eps);
+      if constexpr (ROPE) rope_pairs2(lo, hi, cs);
+      if (ok) {
+        if (F == kBF16 || k.fast) {
+          write_kv32<F, true, false, true>(dst, hl, x, k);
+          write_pe32<F, true>(dst, hl, lo, hi, k);
+        } else {
+          write_kv32<F, false, false, true>(dst, hl, x, k);
+          write_pe32<F, false>(dst, hl, lo, hi, k);
+        }
+      }
+    }
+    errbits = __reduce_or_sync(0xFFFFFFFFu, errbits);
+  } else {
+    for (int64_t r = warp; r < a.num_rows; r += nwarps) {
+      int64_t t;
+      int l;
+      split(r, t, l);
+      RowIn in;
+      load_row<F, ROPE>(a, t, l, lane, in);
+      float2 cs;
+      const bool pos_ok = load_rope<ROPE>(a, t, lane, cs);
+      DivConst k{};
+      if constexpr (F != kBF16) k = pre ? s_k[l] : div_const(a.scales[l]);
+      const int64_t cptr = pre ? s_cptr[l] : a.cache_ptrs[l];
+      errbits |= store_row<F, NORM, ROPE>(a, l, lane, in, pos_ok, cs, cptr, k);
+    }
   }
   if (errbits && lane == 0 && a.err) atomicOr(a.err, errbits);
 }
@@ -278,7 +391,6 @@ __global__ void __launch_bounds__(kThreads) insert_row_kernel(const InsertArgs a
 // registers (before that row is computed), so the producer refills it
 // meanwhile.
 constexpr int kRun = 4;
-constexpr int kILP = 1;  // rows of an item processed in lockstep
 constexpr int kIConsumers = 23;
 constexpr int kIThreads = (kIConsumers + 1) * 32;
 constexpr int kOffPe = kRun * 2 * kR;              // k_pe rows after the kv_c rows
@@ -300,13 +412,14 @@ struct Ring {
   static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
 };
 
-// One item (a layer's run of up to kRun tokens) from its shared-memory stage.
-// The rows are processed in lockstep -- validity and loads of every row, then
-// every row's sum of squares, their warp reductions interleaved, then the
-// scaling, rotation and stores -- so a warp has kRun independent dependency
-// chains to issue from instead of one.
+constexpr int kILP = 1;  // rows of an item processed in lockstep (full-warp form)
+
+// One item (a layer's run of up to kRun tokens) from its shared-memory stage,
+// one row at a time by the whole warp (the raw insert: without RMSNorm and
+// RoPE the half-warp form below saves little and ran 98.4 vs 94.5 us for 65536
+// tokens x 5 layers).  The k_pe pairs are stored after the last row.
 template <int F, bool NORM, bool ROPE, bool FAST, bool CHECK>
-__device__ __forceinline__ uint32_t insert_consume_item(
+__device__ __forceinline__ uint32_t insert_consume_rows(
     const InsertArgs& a, uint32_t src, int l, int lane, int64_t cptr, const DivConst& k,
     uint32_t empty_bar, const int64_t* slot, const int64_t* pos) {
   uint32_t err = 0;
@@ -350,9 +463,6 @@ __device__ __forceinline__ uint32_t insert_consume_item(
     g0 = ld_shared_ro16(g + lane * 16);
     g1 = ld_shared_ro16(g + 512 + lane * 16);
   }
-  // the rows' kv_c, kILP at a time in lockstep; their k_pe pairs are rotated
-  // and stored after the last row, so the cos/sin loads issued above have
-  // the whole item to arrive
   uint32_t pe[kRun];
 #pragma unroll
   for (int h = 0; h < kRun; h += kILP) {
@@ -377,11 +487,7 @@ __device__ __forceinline__ uint32_t insert_consume_item(
     if constexpr (NORM) {
       float ss[kILP];
 #pragma unroll
-      for (int i = 0; i < kILP; ++i) ss[i] = sum_sq16(x0[i], x1[i]);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-        for (int i = 0; i < kILP; ++i) ss[i] += __shfl_xor_sync(0xFFFFFFFFu, ss[i], o);
+      for (int i = 0; i < kILP; ++i) ss[i] = row_sum_sq(x0[i], x1[i], lane);
 #pragma unroll
       for (int i = 0; i < kILP; ++i) {
         // mean over 512 (exact power-of-two scaling) + eps, one rounding
@@ -402,6 +508,78 @@ __device__ __forceinline__ uint32_t insert_consume_item(
     if (!ok[r]) continue;
     const uint32_t p = ROPE ? rope_pair(pe[r], cs[r]) : pe[r];
     write_pe_k<F, FAST || F == kBF16>(dst[r], lane, p, k);
+  }
+  return err;
+}
+
+// One item (a layer's run of up to kRun tokens) from its shared-memory stage,
+// two rows at a time (with RMSNorm or RoPE: 102.3 vs 113.0 us with RMSNorm +
+// RoPE for 65536 tokens x 5 layers, one row per warp instruction before):
+// lanes 0-15 take rows 0 and 2 of the item, lanes 16-31
+// rows 1 and 3 (this lane's rows: slot[p] / pos[p] of row 2p + half).  The
+// rows' kv_c are normalised, converted and stored one pair of rows after the
+// other; the k_pe pairs are rotated and stored after the last, so the
+// cos/sin loads issued first have the whole item to arrive.  Returns this
+// lane's error bits.
+template <int F, bool NORM, bool ROPE, bool FAST, bool CHECK>
+__device__ __forceinline__ uint32_t insert_consume_pairs(
+    const InsertArgs& a, uint32_t src, int l, int lane, int64_t cptr, const DivConst& k,
+    uint32_t empty_bar, const int64_t (&slot)[2], const int64_t (&pos)[2]) {
+  const int hl = lane & 15, half = lane >> 4;
+  uint32_t err = 0;
+  // the fp8 fast path takes the normalised rows negated (write_kv32<.., NEG>)
+  constexpr bool kNeg = NORM && F != kBF16 && FAST;
+  // validity and destination of this lane's rows (uniform across its half)
+  uint8_t* dst[2];
+  bool ok[2];
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    const int64_t s = slot[p];
+    ok[p] = false;
+    dst[p] = nullptr;
+    if (s < 0) continue;  // padding slot or past the tail
+    if (s >= a.capacity) { err |= kErrSlotOOB; continue; }
+    if (ROPE && (pos[p] < 0 || pos[p] >= a.max_position)) { err |= kErrPosOOB; continue; }
+    if (cptr == 0 || (cptr & 15)) { err |= kErrMisaligned; continue; }
+    ok[p] = true;
+    dst[p] = slot_dst(a, s, cptr);
+  }
+  float4 cs[2];
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    cs[p] = make_float4(1.f, 1.f, 0.f, 0.f);
+    if (ROPE && ok[p]) cs[p] = load_cs2(a.cos_sin + pos[p] * kP, hl);
+  }
+  uint4 g[4];
+  if constexpr (NORM) {
+    const uint8_t* gr = a.gamma + (int64_t)l * a.gamma_ls + hl * 16;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) g[c] = ld_shared_ro16(gr + 256 * c);
+  }
+  uint32_t lo[2], hi[2];
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    const uint32_t row = src + (2 * p + half) * 2 * kR + hl * 16;
+    uint4 x[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) x[c] = lds16(row + 256 * c);
+    const uint32_t pr = src + kOffPe + (2 * p + half) * 2 * kP + hl * 4;
+    lo[p] = lds_u32(pr);
+    hi[p] = lds_u32(pr + kP);
+    if (p == 1) {
+      // every read of the stage is done: hand it back to the producer before
+      // the last rows are computed
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_bar);
+    }
+    if constexpr (NORM) rms_norm32<kNeg>(x, g, a.eps);
+    if (ok[p]) write_kv32<F, FAST, kNeg, CHECK>(dst[p], hl, x, k);
+  }
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    if (!ok[p]) continue;
+    if constexpr (ROPE) rope_pairs2(lo[p], hi[p], cs[p]);
+    write_pe32<F, FAST || F == kBF16>(dst[p], hl, lo[p], hi[p], k);
   }
   return err;
 }
@@ -534,14 +712,19 @@ __global__ void __launch_bounds__(kIThreads, 1) insert_tma_kernel(const InsertAr
       // too doubled the copies per item, and the copy rate, not the bytes,
       // then held the consumers back (129.6 vs 118.9 us for 65536 tokens x 5
       // layers).
-      int64_t slot[kRun], pos[kRun];
+      // half-warp form: this lane's rows 2p + (lane >> 4); full-warp form: all
+      // kRun rows
+      constexpr bool kPairs = NORM || ROPE;
+      constexpr int kSlots = kPairs ? 2 : kRun;
+      int64_t slot[kSlots], pos[kSlots];
 #pragma unroll
-      for (int r = 0; r < kRun; ++r) {
-        slot[r] = -1;
-        pos[r] = 0;
+      for (int p = 0; p < kSlots; ++p) {
+        const int r = kPairs ? 2 * p + (lane >> 4) : p;
+        slot[p] = -1;
+        pos[p] = 0;
         if (r < nt) {
-          slot[r] = __ldg(a.slots + (int64_t)l * a.slot_ls + t0 + r);
-          if (ROPE) pos[r] = __ldg(a.positions + t0 + r);
+          slot[p] = __ldg(a.slots + (int64_t)l * a.slot_ls + t0 + r);
+          if (ROPE) pos[p] = __ldg(a.positions + t0 + r);
         }
       }
       if (!mbar_wait(full0 + 8 * s, ((uint32_t)i / (uint32_t)kIStages) & 1u, a.wait_limit_ns)) {
@@ -551,15 +734,25 @@ __global__ void __launch_bounds__(kIThreads, 1) insert_tma_kernel(const InsertAr
       const uint32_t src = stage0 + (uint32_t)(s * kIStageBytes);
       const DivConst k = div_const(s_scale[l]);
       const int64_t cptr = s_cptr[l];
-      if (F != kBF16 && !k.fast)
-        errbits |= insert_consume_item<F, NORM, ROPE, false, true>(a, src, l, lane, cptr, k,
-                                                                   empty0 + 8 * s, slot, pos);
-      else if (NORM && F != kBF16 && !s_check[l])
-        errbits |= insert_consume_item<F, NORM, ROPE, true, false>(a, src, l, lane, cptr, k,
-                                                                   empty0 + 8 * s, slot, pos);
-      else
-        errbits |= insert_consume_item<F, NORM, ROPE, true, true>(a, src, l, lane, cptr, k,
-                                                                  empty0 + 8 * s, slot, pos);
+      const uint32_t eb = empty0 + 8 * s;
+      if constexpr (kPairs) {
+        if (F != kBF16 && !k.fast)
+          errbits |= insert_consume_pairs<F, NORM, ROPE, false, true>(a, src, l, lane, cptr, k,
+                                                                      eb, slot, pos);
+        else if (NORM && F != kBF16 && !s_check[l])
+          errbits |= insert_consume_pairs<F, NORM, ROPE, true, false>(a, src, l, lane, cptr, k,
+                                                                      eb, slot, pos);
+        else
+          errbits |= insert_consume_pairs<F, NORM, ROPE, true, true>(a, src, l, lane, cptr, k,
+                                                                     eb, slot, pos);
+      } else {
+        if (F != kBF16 && !k.fast)
+          errbits |= insert_consume_rows<F, NORM, ROPE, false, true>(a, src, l, lane, cptr, k,
+                                                                     eb, slot, pos);
+        else
+          errbits |= insert_consume_rows<F, NORM, ROPE, true, true>(a, src, l, lane, cptr, k,
+                                                                    eb, slot, pos);
+      }
     }
   }
   __syncthreads();
@@ -577,6 +770,7 @@ __global__ void __launch_bounds__(kIThreads, 1) insert_tma_kernel(const InsertAr
     }
     errbits |= kErrTimeout;
   }
+  errbits = __reduce_or_sync(0xFFFFFFFFu, errbits);  // the two halves' rows differ
   if (errbits && lane == 0 && a.err) atomicOr(a.err, errbits);
 }
 
@@ -625,8 +819,15 @@ cudaError_t launch_t(const InsertArgs& a, const LaunchCfg& cfg) {
   const int64_t min_rows = NORM ? kBulkMinRowsNorm : kBulkMinRows;
   const bool bulk = a.bulk_mode == 2 || (a.bulk_mode == 1 && a.num_rows >= min_rows);
   if (bulk && insert_tma_layout(a)) return launch_tma<F, NORM, ROPE>(a, cfg);
-  auto kern = insert_row_kernel<F, NORM, ROPE>;
-  const int64_t ctas = (a.num_rows + kThreads / 32 - 1) / (kThreads / 32);
+  // With RMSNorm or RoPE, calls from kRowPairsMinRows rows take two rows per
+  // warp (half-warp layout); smaller calls, one wave of latency-bound warps,
+  // one row per warp.  Both layouts compute the same bits.
+  const bool pairs = (NORM || ROPE) && a.num_rows >= kRowPairsMinRows;
+  auto kern = pairs ? insert_row_kernel<F, NORM, ROPE, NORM || ROPE>
+                    : insert_row_kernel<F, NORM, ROPE, false>;
+  const int64_t rows_per_warp = pairs ? 2 : 1;
+  const int64_t warps = (a.num_rows + rows_per_warp - 1) / rows_per_warp;
+  const int64_t ctas = (warps + kThreads / 32 - 1) / (kThreads / 32);
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(capped_grid(reinterpret_cast<const void*>(kern), kThreads, ctas));
   lc.blockDim = dim3(kThreads);

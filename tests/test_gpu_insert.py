@@ -405,6 +405,37 @@ def test_rope_table_matches_oracle(orc):
     assert (t != r).mean() < 1e-3
 
 
+@pytest.mark.parametrize("dtype", [0, 1])
+def test_every_layout_gives_the_same_bits(dtype):
+    """RMSNorm + RoPE rows are computed one per warp (small calls), two per
+    warp (larger row-shape calls) or by the bulk-copy ring, with one summation
+    tree for the sum of squares: one call of 2048 tokens x 5 layers (two rows
+    per warp), the same rows as two calls of 1024 tokens (one row per warp),
+    and the bulk-copy shape give the same caches bit for bit (a bf16 cache
+    shows the normalised values themselves)."""
+    wl = W.insert_workload(5, 2048, dtype, num_blocks=256, block_size=64, norm=True, rope=True,
+                           seed=41)
+    table = D.gpu_rope_table()
+    one, g1, _ = D.gpu_insert(wl, cos_sin=table, fill=0x11)
+    caches = None
+    for h in range(2):
+        sub = W.InsertWorkload(5, 1024, dtype, 256, 64,
+                               np.ascontiguousarray(wl.kv_c[:, h * 1024:(h + 1) * 1024]),
+                               np.ascontiguousarray(wl.k_pe[:, h * 1024:(h + 1) * 1024]),
+                               np.ascontiguousarray(wl.slot_mapping[:, h * 1024:(h + 1) * 1024]),
+                               True, wl.k_scales, wl.gamma,
+                               np.ascontiguousarray(wl.positions[h * 1024:(h + 1) * 1024]))
+        halves, g2, caches = D.gpu_insert(sub, cos_sin=table, fill=0x11, caches=caches)
+    prev = ops.mla_set_bulk_copy(2)
+    try:
+        ring, g3, _ = D.gpu_insert(wl, cos_sin=table, fill=0x11)
+    finally:
+        ops.mla_set_bulk_copy(prev)
+    assert g1 and g2 and g3
+    assert_exact(halves, one)
+    assert_exact(ring, one)
+
+
 # ----------------------------------------------------- full size, as benchmarked
 def test_large_insert_65536_tokens_sampled(orc, bulk):
     """65536 tokens x 5 layers, e4m3, RMSNorm + RoPE, caches of 2048 blocks x
