@@ -588,7 +588,11 @@ def run(args):
         "roofline": {"bound": "hbm", "kernel": "pack_gather_kernel<e4m3,e4m3,bf16>",
                      "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
                      "peak_source": f"{peak_kind} HBM copy bandwidth",
-                     "traffic": profile_traffic("pack_gather_fp8_h16")},
+                     "traffic": profile_traffic("pack_gather_fp8_h16"),
+                     "traffic_basis": ("ncu, one launch with its gather: dram__bytes_read.sum + "
+                                       "lts__t_sectors_srcunit_tex_op_write.sum x 32 (every stored "
+                                       "byte reaches DRAM; dram__bytes_write.sum sees only the "
+                                       "write-backs inside the launch)")},
         "kernels": {"insert": kline(b_ins_launch, ms_insert),
                     "pack_gather": kline(b_pg_launch, ms_pg),
                     "gather": kline(b_gat_launch, ms_gather),
@@ -682,6 +686,8 @@ def run_profile_case(name: str, launches: int, tokens: int | None = None,
       pack_bf16  the same with bf16 output and a bf16 k_pe
       pack_f16   the fp8 pack of an fp16 kv_b_proj output
       pack_paged the fp8 pack reading k_pe from a 4096-block fp8 cache
+      pack_gather the fp8 pack of 8192 tokens and the gather of the next 8192
+                 rows into a second workspace, one launch
       norm_rope  65536 tokens x 5 layers of the [T, L, 576] projection, RMSNorm +
                  RoPE into layer-major outputs"""
     import torch
@@ -779,6 +785,28 @@ def run_profile_case(name: str, launches: int, tokens: int | None = None,
                                                    nb, BS, BS * ENTRY, ENTRY, table, cu, st, key,
                                                    vo, 1, out_scale=sc)
         nbytes = T * (HEADS * 512 + 64 + HEADS * 320) + (T // BS) * 4
+    elif name == "pack_gather":
+        # the pack of T tokens (fp8 out, 16 heads, k_pe from workspace A) and
+        # the gather of the next T rows into workspace B, one launch
+        T, nb = tokens or 8192, 4096
+        assert 2 * T <= nb * BS
+        kvb = torch.randn((T, ROW_STRIDE), generator=g, device=dev).to(torch.bfloat16)
+        heads = kvb[:, :HEADS * 256].view(T, HEADS, 256)
+        cache = torch.randint(0, 126, (nb * BS * ENTRY,), generator=g, device=dev, dtype=torch.int32).to(torch.uint8)
+        table = torch.randperm(nb, generator=g, device=dev).to(torch.int32)[None, :].contiguous()
+        cu = torch.tensor([0, T], dtype=torch.int32, device=dev)
+        st = torch.tensor([T], dtype=torch.int32, device=dev)
+        ws_a = torch.randint(0, 126, (T, ENTRY), generator=g, device=dev, dtype=torch.int32).to(torch.uint8)
+        ws_b = torch.empty((T, ENTRY), dtype=torch.uint8, device=dev)
+        key = torch.empty((T, HEADS, 192), dtype=torch.uint8, device=dev)
+        vo = torch.empty((T, HEADS, 128), dtype=torch.uint8, device=dev)
+        sc = torch.tensor([OUT_SCALE], dtype=torch.float32, device=dev)
+        pk = ops.kv_pack_desc(heads[:, :, :128], heads[:, :, 128:], ws_a[:, 512:], key, vo, 1,
+                              kpe_dtype=1, out_scale=sc)
+        gd = ops.context_gather_desc(cache, 1, nb, BS, BS * ENTRY, ENTRY, ENTRY, table, cu, st,
+                                     ws_b, 1)
+        fn = lambda: ops.mla_context_kv_pack_gather(pk, gd)
+        nbytes = T * B_PACK_TOK + T * B_GATHER_TOK + (T // BS) * 4
     else:
         raise SystemExit(f"unknown profile case {name}")
     for _ in range(2):
