@@ -49,6 +49,10 @@ __device__ __forceinline__ uint4 ld_shared_ro16(const void* p) {
   return __ldg(reinterpret_cast<const uint4*>(p));
 }
 __device__ __forceinline__ void st16(void* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
+// Bring the line holding p into L2 (no register result, no wait).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
 __device__ __forceinline__ void st8(void* p, uint2 v) { *reinterpret_cast<uint2*>(p) = v; }
 
 // ---- bf16 ------------------------------------------------------------------

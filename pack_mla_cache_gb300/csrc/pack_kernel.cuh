@@ -158,9 +158,30 @@ __device__ __forceinline__ void pack_plain_items(const PackArgs& a, const DivCon
 }
 
 // The pack's part of a launch: its warps are warp0, warp0 + nwarps, ...
-template <int OF, int KF, int IF, bool PAGED>
+// PREFETCH: first ask L2 for the warp's first item, whose loads are issued only
+// after the scale has been read and the division form chosen, one memory
+// latency later (in the launch that also gathers: 21.30 -> 21.12 us per chunk;
+// the pack alone measured 19.36 -> 19.45 us, so it does not prefetch).
+template <int OF, int KF, int IF, bool PAGED, bool PREFETCH = false>
 __device__ __forceinline__ void pack_part(const PackArgs& a, int64_t warp0, int64_t nwarps) {
   pdl_wait();
+  if constexpr (!PAGED && PREFETCH) {
+    constexpr int kGroup = group_of<false>();
+    const int groups = (a.num_heads + kGroup - 1) / kGroup;
+    if (warp0 < (int64_t)a.num_tokens * groups) {
+      const int lane = threadIdx.x & 31, half = lane >> 4, part = lane & 15;
+      const int gshift = (groups & (groups - 1)) ? -1 : __ffs(groups) - 1;
+      const Item it = item_of<kGroup>(warp0, groups, gshift, a.num_heads);
+      const uint8_t* src =
+          (half ? a.v + it.t * a.v_ts : a.k_nope + it.t * a.kn_ts) + part * 16;
+      const int64_t hs = half ? a.v_hs : a.kn_hs;
+      if (!half || a.vout) {
+#pragma unroll
+        for (int i = 0; i < kGroup; ++i)
+          if (i < it.nh) prefetch_l2(src + (int64_t)(it.h0 + i) * hs);
+      }
+    }
+  }
   float scale = 1.0f;
   if constexpr (!is16(OF)) {
     if (a.out_scale) scale = *a.out_scale;
@@ -210,7 +231,7 @@ __global__ void __launch_bounds__(kThreads) pack_gather_kernel(const PackArgs a,
     if (errbits && lane == 0 && g.err) atomicOr(g.err, errbits);
     return;
   }
-  pack_part<OF, KF, IF, false>(
+  pack_part<OF, KF, IF, false, true>(
       a, (int64_t)(blockIdx.x - gather_ctas) * kWarps + (threadIdx.x >> 5),
       (int64_t)(gridDim.x - gather_ctas) * kWarps);
 }
