@@ -31,7 +31,8 @@ def _lib():
 
 
 def oracle_gather(orc, pw, table, cu, starts, T, out_dtype):
-    out = np.full((T, ENTRY), 0x3F if out_dtype else 0x3F3F, np.uint8 if out_dtype else np.uint16)
+    wide = out_dtype in (orc.BF16, orc.F16)
+    out = np.full((T, ENTRY), 0x3F3F if wide else 0x3F, np.uint16 if wide else np.uint8)
     err = orc.context_gather(pw.cache, pw.cache_dtype, pw.num_blocks, pw.block_size,
                              pw.block_size * ENTRY, ENTRY, ENTRY, table, cu, starts, out, out_dtype)
     return out, err
@@ -180,3 +181,42 @@ def test_empty_halves_and_overlap_check(orc):
     rk, rv = oracle_pack(orc, kvb, ws_in, H, 1, 1, 0.01)
     np.testing.assert_array_equal(D.host_u8(key), rk)
     np.testing.assert_array_equal(D.host_u8(vo), rv)
+
+
+@pytest.mark.parametrize("cfmt", [1, 2], ids=["e4m3", "e5m2"])
+def test_fp16_chunk_launch_with_widening_gather(orc, cfmt):
+    """fp16 kv_b_proj output: the chunk launch packs chunk 0 into an fp16 key
+    and V from a workspace widened to fp16, and gathers chunk 1 from an fp8
+    cache (e4m3 or e5m2) widened to fp16 into the other workspace."""
+    C, H = 2048, 16
+    pw = W.pack_workload(2 * C, C, num_blocks=128, cache_dtype=cfmt, seed=24 + cfmt)
+    g = torch.Generator().manual_seed(cfmt)
+    kvb = torch.randn((C, 4160), generator=g).to(torch.float16)
+    kvb_np = kvb.view(torch.int16).numpy().view(np.uint16)
+    cache_t, table_t = D.dev(pw.cache), D.dev(pw.block_table)
+    cu = D.dev(np.array([0, C], np.int32))
+    st0, st1 = D.dev(np.array([0], np.int32)), D.dev(np.array([C], np.int32))
+    ws = [torch.zeros((C, ENTRY), dtype=torch.float16, device="cuda") for _ in range(2)]
+    ops.mla_context_gather(cache_t, cfmt, pw.num_blocks, 64, 64 * ENTRY, ENTRY, ENTRY, table_t, cu,
+                           st0, ws[0], ops.MLA_FP16)
+    h = kvb.cuda()[:, :H * 256].view(C, H, 256)
+    key = torch.zeros((C, H, 192), dtype=torch.float16, device="cuda")
+    vo = torch.zeros((C, H, 128), dtype=torch.float16, device="cuda")
+    pack = ops.kv_pack_desc(h[:, :, :128], h[:, :, 128:], ws[0][:, 512:], key, vo, ops.MLA_FP16,
+                            kpe_dtype=ops.MLA_FP16)
+    gd = ops.context_gather_desc(cache_t, cfmt, pw.num_blocks, 64, 64 * ENTRY, ENTRY, ENTRY,
+                                 table_t, cu, st1, ws[1], ops.MLA_FP16)
+    ops.mla_context_kv_pack_gather(pack, gd)
+    torch.cuda.synchronize()
+    for c in range(2):
+        r, err = oracle_gather(orc, pw, pw.block_table, np.array([0, C], np.int32),
+                               np.array([c * C], np.int32), C, orc.F16)
+        assert err == 0
+        np.testing.assert_array_equal(D.host_u16(ws[c]), r)
+    r0, _ = oracle_gather(orc, pw, pw.block_table, np.array([0, C], np.int32),
+                          np.array([0], np.int32), C, orc.F16)
+    rk, rv = orc.context_kv_pack(kvb_np, 4160, 256, kvb_np[:, 128:], 4160, 256, r0[:, 512:], ENTRY,
+                                 orc.F16, C, H, 128, 64, 128, orc.F16, 1.0, True,
+                                 in_dtype=orc.F16)
+    np.testing.assert_array_equal(D.host_u16(key), rk)
+    np.testing.assert_array_equal(D.host_u16(vo), rv)
