@@ -27,6 +27,7 @@ std::atomic<int> g_pdl{1};
 std::atomic<int> g_bulk{1};
 std::atomic<int> g_ptr_checks{1};
 std::atomic<int> g_gather_early{0};
+std::atomic<int> g_insert_early{0};
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s: a wait that long means a fault
 std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
 std::atomic<int64_t> g_skip_item{-1};
@@ -240,6 +241,8 @@ int mla_set_pointer_checks(int enable) { return g_ptr_checks.exchange(enable ? 1
 
 int mla_set_gather_early_tables(int enable) { return g_gather_early.exchange(enable ? 1 : 0); }
 
+int mla_set_insert_early_tables(int enable) { return g_insert_early.exchange(enable ? 1 : 0); }
+
 int mla_test_insert_timeout(uint64_t wait_limit_ns, int64_t skip_item) {
   if (wait_limit_ns == 0) wait_limit_ns = kDefaultWaitNs;
   g_wait_ns.store(wait_limit_ns);
@@ -337,6 +340,7 @@ mla_status_t mla_cache_insert_grouped(
   a.bulk_mode = g_bulk.load();
   a.wait_limit_ns = g_wait_ns.load();
   a.skip_item = g_skip_item.load();
+  a.early_tables = g_insert_early.load() != 0;
   return launched(mla::launch_insert(a, (int)cache_dtype, norm, rope, cfg_for(stream)),
                   "mla_cache_insert_grouped");
 }

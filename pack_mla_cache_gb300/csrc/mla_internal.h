@@ -37,6 +37,9 @@ struct InsertArgs {
   // consumer waiting for that item runs out of time.
   uint64_t wait_limit_ns;
   int64_t skip_item;
+  // row shape: cache_ptrs and scales may be read into the per-layer table
+  // before the wait on the previous grid (the caller declared them complete)
+  bool early_tables;
 };
 
 // A paged cache and the chunk's sequences: chunk token i of sequence s

@@ -73,6 +73,7 @@ SIGNATURES = {
     "mla_set_bulk_copy": (ctypes.c_int, [ctypes.c_int]),
     "mla_set_pointer_checks": (ctypes.c_int, [ctypes.c_int]),
     "mla_set_gather_early_tables": (ctypes.c_int, [ctypes.c_int]),
+    "mla_set_insert_early_tables": (ctypes.c_int, [ctypes.c_int]),
     "mla_test_insert_timeout": (ctypes.c_int, [ctypes.c_uint64, _i64]),
     "mla_cache_insert_grouped": (ctypes.c_int, [
         _vp, _i64, _i64, _vp, _i64, _i64, _i32, _i32, _i32, _i32, _vp, _i64, _vp, _vp,
@@ -179,6 +180,13 @@ def mla_set_gather_early_tables(enable: bool) -> bool:
     launch wait (the tables must be complete before each call is enqueued);
     returns the previous setting."""
     return bool(lib().mla_set_gather_early_tables(1 if enable else 0))
+
+
+def mla_set_insert_early_tables(enable: bool) -> bool:
+    """Let the grouped insert read kv_cache_ptrs and kv_scales before the
+    programmatic launch wait (both must be complete before each call is
+    enqueued); returns the previous setting."""
+    return bool(lib().mla_set_insert_early_tables(1 if enable else 0))
 
 
 def mla_test_insert_timeout(wait_limit_ns: int = 0, skip_item: int = -1) -> None:

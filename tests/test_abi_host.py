@@ -79,6 +79,9 @@ def test_pointer_check_early_table_and_timeout_hook_toggles(L):
     prev = ops.mla_set_gather_early_tables(True)
     assert prev is False  # plain stream order by default
     assert ops.mla_set_gather_early_tables(False) is True
+    prev = ops.mla_set_insert_early_tables(True)
+    assert prev is False  # plain stream order by default
+    assert ops.mla_set_insert_early_tables(False) is True
     assert L.mla_test_insert_timeout(1000, 5) == 0
     assert L.mla_test_insert_timeout(0, -1) == 0  # defaults back
 
