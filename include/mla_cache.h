@@ -443,6 +443,9 @@ typedef struct {
  *   - the gather's output rows must not overlap any buffer of the pack
  *     (k_nope, v, k_pe, key_out, v_out; checked: MLA_ERR_INVALID_ARG) -- in
  *     particular the pack's k_pe must come from the OTHER workspace;
+ *   - key_out and v_out must not overlap the gather's cache or tables (not
+ *     checked; the two halves run concurrently, so such an overlap would not
+ *     give the result of the two calls in sequence);
  *   - either num_tokens may be 0 (that half is skipped).
  * With mla_set_gather_early_tables(1) the gather's tables are read before the
  * launch waits for the previous grid, as for mla_context_gather.
