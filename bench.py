@@ -129,7 +129,7 @@ class ClockSampler:
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
-        time.sleep(0.3)
+        time.sleep(0.05)
         return self
 
     def __exit__(self, *a):
@@ -491,6 +491,14 @@ def run(args):
 
     # ---- timed region: K steps, device time on the launching stream
     with ClockSampler(local) as clk:
+        # keep the GPU busy with untimed steps while the sampler starts, so its
+        # samples fall under load (the K timed steps alone last a few ms)
+        t_load = time.perf_counter() + 0.8
+        while time.perf_counter() < t_load:
+            with torch.cuda.stream(stream):
+                for _ in range(32):
+                    step_graph.replay()
+            stream.synchronize()
         barrier()
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
