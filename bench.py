@@ -689,6 +689,7 @@ def run_profile_case(name: str, launches: int, tokens: int | None = None,
       insert_plain the insert with the bulk-copy pipeline shape disabled (row per warp)
       gather  262144 context rows from a 4096-block fp8 cache, raw
       gather_scaled  the gather widened to bf16 times a k_scale
+      gather_bf16    the gather widened exactly to bf16
       gather_kv_c    the raw gather of the 512 kv_c columns only
       pack    32768 tokens, 16 heads, fp8 e4m3 out, fp8 k_pe
       pack_bf16  the same with bf16 output and a bf16 k_pe
@@ -727,7 +728,7 @@ def run_profile_case(name: str, launches: int, tokens: int | None = None,
                                                   positions=None if raw else pos,
                                                   cos_sin_cache=None if raw else table)
         nbytes = insert_bytes(T, L_LAYERS)
-    elif name in ("gather", "gather_scaled", "gather_kv_c"):
+    elif name in ("gather", "gather_scaled", "gather_bf16", "gather_kv_c"):
         T, nb = tokens or 262144, 4096
         cache = torch.randint(0, 126, (nb * BS * ENTRY,), generator=g, device=dev, dtype=torch.int32).to(torch.uint8)
         table = torch.randperm(nb, generator=g, device=dev).to(torch.int32)[None, :].contiguous()
@@ -738,6 +739,11 @@ def run_profile_case(name: str, launches: int, tokens: int | None = None,
             ks = torch.tensor([0.0137], dtype=torch.float32, device=dev)
             fn = lambda: ops.mla_context_gather_scaled(cache, 1, nb, BS, BS * ENTRY, ENTRY, ENTRY,
                                                        table, cu, st, out, ks)
+            nbytes = T * (ENTRY + 2 * ENTRY) + (T // BS) * 4
+        elif name == "gather_bf16":
+            out = torch.empty((T, ENTRY), dtype=torch.bfloat16, device=dev)
+            fn = lambda: ops.mla_context_gather(cache, 1, nb, BS, BS * ENTRY, ENTRY, ENTRY, table,
+                                                cu, st, out, 0)
             nbytes = T * (ENTRY + 2 * ENTRY) + (T // BS) * 4
         else:
             cols = 512 if name == "gather_kv_c" else ENTRY

@@ -355,9 +355,42 @@ __device__ __forceinline__ uint32_t fp8x2_to_f16x2(uint32_t w) {
   return h2;
 }
 
+// Whether any of the 8 fp8 codes in v is a NaN (e4m3: low 7 bits 0x7F; e5m2:
+// above 0x7C): adding 1 (3) to each byte's low 7 bits carries into its top
+// bit exactly for those codes, and never across bytes.
+template <int F>
+__device__ __forceinline__ bool fp8x8_any_nan(uint2 v) {
+  constexpr uint32_t kAdd = F == kE4M3 ? 0x01010101u : 0x03030303u;
+  const uint32_t a = ((v.x & 0x7F7F7F7Fu) + kAdd) | ((v.y & 0x7F7F7F7Fu) + kAdd);
+  return (a & 0x80808080u) != 0u;
+}
+
 // 8 fp8 (one uint2) -> 8 exact 16-bit floats of format OF (bf16 or fp16).
+// Without a NaN code among the 8 the hardware widening is final (an fp8 value
+// is exact in fp16, fp32 and bf16); a group holding one takes the per-element
+// path, which gives each NaN the quiet NaN with its code's sign.
 template <int F, int OF>
 __device__ __forceinline__ uint4 fp8x8_to_x16x8(uint2 v) {
+  if (!fp8x8_any_nan<F>(v)) {
+    const uint32_t w[4] = {v.x, v.x >> 16, v.y, v.y >> 16};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t h2;
+      const uint16_t in = static_cast<uint16_t>(w[i]);
+      if constexpr (F == kE4M3) asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+      else asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(h2) : "h"(in));
+      if constexpr (OF == kBF16) {
+        float f0, f1;
+        asm("{ .reg .b16 a, b; mov.b32 {a, b}, %2; cvt.f32.f16 %0, a; cvt.f32.f16 %1, b; }"
+            : "=f"(f0), "=f"(f1) : "r"(h2));
+        o[i] = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632);
+      } else {
+        o[i] = h2;
+      }
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+  }
   if constexpr (OF == kBF16) {
     return fp8x8_to_bf16x8<F>(v);
   } else {
