@@ -557,9 +557,13 @@ __device__ __forceinline__ uint32_t insert_consume_pairs(
     cs[p] = make_float4(1.f, 1.f, 0.f, 0.f);
     if (ROPE && ok[p]) cs[p] = load_cs2(a.cos_sin + pos[p] * kP, hl);
   }
+  // The layer's gamma: held in registers for both row pairs, or, with RoPE
+  // (whose cos/sin must be held from the start of the item), read again at
+  // each use from L1 (65536 tokens x 5 layers: 102.3 -> 100.7 us with RMSNorm
+  // + RoPE; RMSNorm alone 97.1 vs 98.2 us with the gamma held, so it keeps it).
+  const uint8_t* gr = a.gamma + (int64_t)l * a.gamma_ls + hl * 16;
   uint4 g[4];
-  if constexpr (NORM) {
-    const uint8_t* gr = a.gamma + (int64_t)l * a.gamma_ls + hl * 16;
+  if constexpr (NORM && !ROPE) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) g[c] = ld_shared_ro16(gr + 256 * c);
   }
@@ -579,7 +583,8 @@ __device__ __forceinline__ uint32_t insert_consume_pairs(
       __syncwarp();
       if (lane == 0) mbar_arrive(empty_bar);
     }
-    if constexpr (NORM) rms_norm32<kNeg>(x, g, a.eps);
+    if constexpr (NORM && ROPE) rms_norm32_g<kNeg>(x, gr, a.eps);
+    else if constexpr (NORM) rms_norm32<kNeg>(x, g, a.eps);
     if (ok[p]) write_kv32<F, FAST, kNeg, CHECK>(dst[p], hl, x, k);
   }
 #pragma unroll
