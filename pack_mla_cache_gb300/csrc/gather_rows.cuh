@@ -82,35 +82,27 @@ __device__ __forceinline__ void gather_rows(const GatherArgs& a, int64_t warp, i
       r += nwarps;
       src = r < a.num_tokens ? paged_row(a.src, sl, lane, r, errbits) : nullptr;
     }
-    return;
-  }
-  while (r < a.num_tokens) {
-    uint4 v[kGatherMaxChunks];
-#pragma unroll
-    for (int c = 0; c < kGatherMaxChunks; ++c) {
-      const int ch = lane + 32 * c;
-      v[c] = make_uint4(0, 0, 0, 0);
-      if (src && ch < a.row_chunks) v[c] = ld_stream16(src + ch * 16);
-    }
-    if (src) {
-      uint8_t* dst = a.out + r * a.out_rs;
+  } else {
+    // raw copy: 16-byte units (up to 96 per row)
+    while (r < a.num_tokens) {
+      uint4 v[kGatherMaxChunks];
 #pragma unroll
       for (int c = 0; c < kGatherMaxChunks; ++c) {
         const int ch = lane + 32 * c;
-        if (ch >= a.row_chunks) continue;
-        if constexpr (MODE == 0) {
-          st16(dst + ch * 16, v[c]);
-        } else if constexpr (SCALED) {
-          st16(dst + ch * 32, fp8x8_to_bf16x8_scaled<MODE>(make_uint2(v[c].x, v[c].y), s2));
-          st16(dst + ch * 32 + 16, fp8x8_to_bf16x8_scaled<MODE>(make_uint2(v[c].z, v[c].w), s2));
-        } else {
-          st16(dst + ch * 32, fp8x8_to_x16x8<MODE, OUT>(make_uint2(v[c].x, v[c].y)));
-          st16(dst + ch * 32 + 16, fp8x8_to_x16x8<MODE, OUT>(make_uint2(v[c].z, v[c].w)));
+        v[c] = make_uint4(0, 0, 0, 0);
+        if (src && ch < a.row_chunks) v[c] = ld_stream16(src + ch * 16);
+      }
+      if (src) {
+        uint8_t* dst = a.out + r * a.out_rs;
+#pragma unroll
+        for (int c = 0; c < kGatherMaxChunks; ++c) {
+          const int ch = lane + 32 * c;
+          if (ch < a.row_chunks) st16(dst + ch * 16, v[c]);
         }
       }
+      r += nwarps;
+      src = r < a.num_tokens ? paged_row(a.src, sl, lane, r, errbits) : nullptr;
     }
-    r += nwarps;
-    src = r < a.num_tokens ? paged_row(a.src, sl, lane, r, errbits) : nullptr;
   }
 }
 
