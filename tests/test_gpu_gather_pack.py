@@ -219,6 +219,36 @@ def test_gather_widens_every_fp8_code(orc, fmt):
     np.testing.assert_array_equal(g, r)
 
 
+@pytest.mark.parametrize("fmt", [1, 2], ids=["e4m3", "e5m2"])
+@pytest.mark.parametrize("out_dtype", [0, 3], ids=["bf16", "fp16"])
+def test_widening_nan_codes_at_every_byte_position(orc, fmt, out_dtype):
+    """The widening sends a group of 8 codes (8 bytes) through the hardware
+    conversion alone unless the group holds a NaN code.  Here every other
+    group of every row holds one NaN code of the format (each sign, each NaN
+    pattern) at a byte position that runs through 0..7, between finite codes
+    and next to groups without a NaN: every row equals the oracle's."""
+    pw = W.pack_workload(64, 64, num_blocks=1, cache_dtype=fmt, seed=4)
+    nan_codes = [0x7F, 0xFF] if fmt == 1 else [0x7D, 0x7E, 0x7F, 0xFD, 0xFE, 0xFF]
+    finite = np.array([c for c in range(256) if c not in nan_codes], np.uint8)
+    rows = pw.cache.reshape(-1, ENTRY)[:64]
+    rows[:] = np.random.default_rng(11).choice(finite, size=rows.shape)
+    for r in range(64):
+        for g in range(0, ENTRY // 8, 2):
+            rows[r, 8 * g + (r + g) % 8] = nan_codes[(7 * r + g) % len(nan_codes)]
+    cu, st = np.array([0, 64], np.int32), np.array([0], np.int32)
+    out = torch.full((64, ENTRY), 0x1234, dtype=torch.int16, device="cuda")
+    out = out.view(torch.bfloat16 if out_dtype == 0 else torch.float16)
+    ops.mla_context_gather(dev_cache(pw), fmt, pw.num_blocks, pw.block_size,
+                           pw.block_size * ENTRY, ENTRY, ENTRY, D.dev(pw.block_table), D.dev(cu),
+                           D.dev(st), out, out_dtype)
+    torch.cuda.synchronize()
+    ref = np.full((64, ENTRY), 0x1234, np.uint16)
+    err = orc.context_gather(pw.cache, fmt, pw.num_blocks, pw.block_size, pw.block_size * ENTRY,
+                             ENTRY, ENTRY, pw.block_table, cu, st, ref, out_dtype)
+    assert err == 0
+    np.testing.assert_array_equal(D.host_u16(out), ref)
+
+
 # -------------------------------------------------------------------------- pack
 def pack_io(kvb, ws, H, out_dtype, kpe_fp8, with_v=True):
     """Device views of a kv_b_proj output [T, >= H*256] and a gather workspace
