@@ -386,13 +386,14 @@ __global__ void __launch_bounds__(kThreads) insert_row_kernel(const InsertArgs a
 // Shape 2 (bulk-copy pipeline): for dense per-layer rows (kv_c token stride
 // 512, k_pe token stride 64 -- the layer-major [L, T, .] buffers), one layer's
 // run of kRun consecutive tokens is contiguous.  A work item is such a run: a
-// producer warp streams its kv_c and k_pe rows into a ring of 46 shared-memory
-// stages (Ring below) with cp.async.bulk (byte-counted on a per-stage
+// producer warp streams its kv_c rows into a ring of 46 shared-memory stages
+// (Ring below) with one cp.async.bulk per item (byte-counted on a per-stage
 // mbarrier; lane s of the producer fills stages s and s + 32), and 23 consumer
-// warps process the rows from shared memory (the item's slots and positions
-// are loaded from global memory while the consumer waits for its stage, the
-// rotary cos/sin of the item's rows together, the layer's gamma once per
-// item).  Each consumer owns the stages s == warp (mod kIConsumers) and
+// warps process the rows from shared memory (the item's slots, positions and
+// k_pe words are loaded from global memory while the consumer waits for its
+// stage -- with RMSNorm + RoPE the k_pe words only after the wait, see below
+// -- the rotary cos/sin of the item's rows together, the layer's gamma once
+// per item).  Each consumer owns the stages s == warp (mod kIConsumers) and
 // takes their fills in order, so no parity wait can alias an older phase.
 // A consumer hands the stage back as soon as the item's last row is in
 // registers (before that row is computed), so the producer refills it
@@ -400,8 +401,11 @@ __global__ void __launch_bounds__(kThreads) insert_row_kernel(const InsertArgs a
 constexpr int kRun = 4;
 constexpr int kIConsumers = 23;
 constexpr int kIThreads = (kIConsumers + 1) * 32;
-constexpr int kOffPe = kRun * 2 * kR;              // k_pe rows after the kv_c rows
-constexpr int kIStageBytes = kOffPe + kRun * 2 * kP;  // 4608
+// A stage holds an item's kv_c rows only.  Each lane reads its few k_pe
+// bytes from global memory instead: staging them as a second bulk copy per
+// item cost more (65536 tokens x 5 layers: RMSNorm + RoPE 100.7 vs 98.6 us,
+// RMSNorm alone 97.1 vs 94.5, RoPE alone 95.4 vs 93.0, raw 94.6 vs 94.3).
+constexpr int kIStageBytes = kRun * 2 * kR;  // 4096
 // The ring: 2 stages per consumer, 46 in all (producer lanes 0-13 own two).
 // 23 consumers of one row at a time (72 registers: 6 warps per SM
 // sub-partition) beat 16 consumers of two rows in lockstep (91 registers):
@@ -428,7 +432,7 @@ constexpr int kILP = 1;  // rows of an item processed in lockstep (full-warp for
 template <int F, bool NORM, bool ROPE, bool FAST, bool CHECK>
 __device__ __forceinline__ uint32_t insert_consume_rows(
     const InsertArgs& a, uint32_t src, int l, int lane, int64_t cptr, const DivConst& k,
-    uint32_t empty_bar, const int64_t* slot, const int64_t* pos) {
+    uint32_t empty_bar, const int64_t* slot, const int64_t* pos, const uint32_t* pe_in) {
   uint32_t err = 0;
   // the fp8 fast path takes the normalised rows negated (write_kv_neg)
   constexpr bool kNeg = NORM && F != kBF16 && FAST;
@@ -479,11 +483,7 @@ __device__ __forceinline__ uint32_t insert_consume_rows(
       const uint32_t row = src + (h + i) * 2 * kR;
       x0[i] = y0[i] = lds16(row + lane * 16);
       x1[i] = y1[i] = lds16(row + 512 + lane * 16);
-      const uint32_t pr = src + kOffPe + (h + i) * 2 * kP + lane * 2;
-      uint32_t lo, hi;
-      asm volatile("ld.shared.u16 %0, [%1];" : "=r"(lo) : "r"(pr));
-      asm volatile("ld.shared.u16 %0, [%1];" : "=r"(hi) : "r"(pr + kP));
-      pe[h + i] = lo | (hi << 16);
+      pe[h + i] = pe_in[h + i];
     }
     if (h + kILP >= kRun) {
       // every read of the stage is done: hand it back to the producer before
@@ -526,12 +526,18 @@ __device__ __forceinline__ uint32_t insert_consume_rows(
 // rows 1 and 3 (this lane's rows: slot[p] / pos[p] of row 2p + half).  The
 // rows' kv_c are normalised, converted and stored one pair of rows after the
 // other; the k_pe pairs are rotated and stored after the last, so the
-// cos/sin loads issued first have the whole item to arrive.  Returns this
-// lane's error bits.
+// cos/sin loads issued first have the whole item to arrive.  The k_pe words
+// (lo / hi: elements 2 hl, 2 hl + 1 and 32 + 2 hl, 33 + 2 hl of the lane's
+// rows) come loaded before the stage wait, or, with RMSNorm + RoPE (kLatePe),
+// are loaded here from global memory: held across the wait they crowd the
+// 80 registers of that form (100.9 vs 98.6 us).  Returns this lane's error
+// bits.
 template <int F, bool NORM, bool ROPE, bool FAST, bool CHECK>
 __device__ __forceinline__ uint32_t insert_consume_pairs(
     const InsertArgs& a, uint32_t src, int l, int lane, int64_t cptr, const DivConst& k,
-    uint32_t empty_bar, const int64_t (&slot)[2], const int64_t (&pos)[2]) {
+    uint32_t empty_bar, const int64_t (&slot)[2], const int64_t (&pos)[2],
+    const uint32_t (&lo_in)[2], const uint32_t (&hi_in)[2], int64_t t0, int nt) {
+  constexpr bool kLatePe = NORM && ROPE;
   const int hl = lane & 15, half = lane >> 4;
   uint32_t err = 0;
   // the fp8 fast path takes the normalised rows negated (write_kv32<.., NEG>)
@@ -570,13 +576,23 @@ __device__ __forceinline__ uint32_t insert_consume_pairs(
   uint32_t lo[2], hi[2];
 #pragma unroll
   for (int p = 0; p < 2; ++p) {
+    lo[p] = lo_in[p];
+    hi[p] = hi_in[p];
+    if constexpr (kLatePe) {
+      lo[p] = hi[p] = 0;
+      if (2 * p + half < nt) {
+        const uint8_t* pe = a.k_pe + (t0 + 2 * p + half) * a.kpe_ts + (int64_t)l * a.kpe_ls + hl * 4;
+        lo[p] = __ldcs(reinterpret_cast<const uint32_t*>(pe));
+        hi[p] = __ldcs(reinterpret_cast<const uint32_t*>(pe + kP));
+      }
+    }
+  }
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
     const uint32_t row = src + (2 * p + half) * 2 * kR + hl * 16;
     uint4 x[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) x[c] = lds16(row + 256 * c);
-    const uint32_t pr = src + kOffPe + (2 * p + half) * 2 * kP + hl * 4;
-    lo[p] = lds_u32(pr);
-    hi[p] = lds_u32(pr + kP);
     if (p == 1) {
       // every read of the stage is done: hand it back to the producer before
       // the last rows are computed
@@ -697,11 +713,9 @@ __global__ void __launch_bounds__(kIThreads, 1) insert_tma_kernel(const InsertAr
       const int nt = (int)min((int64_t)kRun, (int64_t)a.num_tokens - t0);
       const uint32_t dst = stage0 + (uint32_t)(s * kIStageBytes);
       if (b != 0 || i != a.skip_item) {  // (the test hook issues nothing for one item)
-        mbar_arrive_expect_tx(full0 + 8 * s, (uint32_t)nt * (2 * kR + 2 * kP));
+        mbar_arrive_expect_tx(full0 + 8 * s, (uint32_t)nt * (2 * kR));
         bulk_g2s(dst, a.kv_c + t0 * a.kvc_ts + (int64_t)l * a.kvc_ls, (uint32_t)nt * 2 * kR,
                  full0 + 8 * s);
-        bulk_g2s(dst + kOffPe, a.k_pe + t0 * a.kpe_ts + (int64_t)l * a.kpe_ls,
-                 (uint32_t)nt * 2 * kP, full0 + 8 * s);
         if (kIStages <= 32 || s < 32) fills0 = n + 1;
         else fills1 = n + 1;
       }
@@ -719,24 +733,36 @@ __global__ void __launch_bounds__(kIThreads, 1) insert_tma_kernel(const InsertAr
       const int l = (int)((uint32_t)j - (uint32_t)run * (uint32_t)L);
       const int64_t t0 = run * kRun;
       const int nt = (int)min((int64_t)kRun, (int64_t)a.num_tokens - t0);
-      // The item's slots and positions are read from global memory before the
-      // wait on its stage, so their latency overlaps it; bulk-copying them
-      // too doubled the copies per item, and the copy rate, not the bytes,
-      // then held the consumers back (129.6 vs 118.9 us for 65536 tokens x 5
-      // layers).
+      // The item's slots, positions and (but with RMSNorm + RoPE) k_pe words
+      // are read from global memory before the wait on its stage, so their
+      // latency overlaps it; bulk-copying slots and positions too doubled the
+      // copies per item, and the copy rate, not the bytes, then held the
+      // consumers back (129.6 vs 118.9 us for 65536 tokens x 5 layers).
       // half-warp form: this lane's rows 2p + (lane >> 4); full-warp form: all
       // kRun rows
       constexpr bool kPairs = NORM || ROPE;
       constexpr int kSlots = kPairs ? 2 : kRun;
       int64_t slot[kSlots], pos[kSlots];
+      uint32_t pe_lo[kSlots], pe_hi[kSlots];
 #pragma unroll
       for (int p = 0; p < kSlots; ++p) {
         const int r = kPairs ? 2 * p + (lane >> 4) : p;
         slot[p] = -1;
         pos[p] = 0;
+        pe_lo[p] = pe_hi[p] = 0;
         if (r < nt) {
           slot[p] = __ldg(a.slots + (int64_t)l * a.slot_ls + t0 + r);
           if (ROPE) pos[p] = __ldg(a.positions + t0 + r);
+          const uint8_t* pe = a.k_pe + (t0 + r) * a.kpe_ts + (int64_t)l * a.kpe_ls;
+          if constexpr (!kPairs) {
+            // this lane's pair (lane, lane + 32) of the row
+            const uint32_t lo = __ldcs(reinterpret_cast<const uint16_t*>(pe + lane * 2));
+            const uint32_t hi = __ldcs(reinterpret_cast<const uint16_t*>(pe + kP + lane * 2));
+            pe_lo[p] = lo | (hi << 16);
+          } else if constexpr (!(NORM && ROPE)) {
+            pe_lo[p] = __ldcs(reinterpret_cast<const uint32_t*>(pe + (lane & 15) * 4));
+            pe_hi[p] = __ldcs(reinterpret_cast<const uint32_t*>(pe + kP + (lane & 15) * 4));
+          }
         }
       }
       if (!mbar_wait(full0 + 8 * s, ((uint32_t)i / (uint32_t)kIStages) & 1u, a.wait_limit_ns)) {
@@ -749,21 +775,21 @@ __global__ void __launch_bounds__(kIThreads, 1) insert_tma_kernel(const InsertAr
       const uint32_t eb = empty0 + 8 * s;
       if constexpr (kPairs) {
         if (F != kBF16 && !k.fast)
-          errbits |= insert_consume_pairs<F, NORM, ROPE, false, true>(a, src, l, lane, cptr, k,
-                                                                      eb, slot, pos);
+          errbits |= insert_consume_pairs<F, NORM, ROPE, false, true>(
+              a, src, l, lane, cptr, k, eb, slot, pos, pe_lo, pe_hi, t0, nt);
         else if (NORM && F != kBF16 && !s_check[l])
-          errbits |= insert_consume_pairs<F, NORM, ROPE, true, false>(a, src, l, lane, cptr, k,
-                                                                      eb, slot, pos);
+          errbits |= insert_consume_pairs<F, NORM, ROPE, true, false>(
+              a, src, l, lane, cptr, k, eb, slot, pos, pe_lo, pe_hi, t0, nt);
         else
-          errbits |= insert_consume_pairs<F, NORM, ROPE, true, true>(a, src, l, lane, cptr, k,
-                                                                     eb, slot, pos);
+          errbits |= insert_consume_pairs<F, NORM, ROPE, true, true>(
+              a, src, l, lane, cptr, k, eb, slot, pos, pe_lo, pe_hi, t0, nt);
       } else {
         if (F != kBF16 && !k.fast)
           errbits |= insert_consume_rows<F, NORM, ROPE, false, true>(a, src, l, lane, cptr, k,
-                                                                     eb, slot, pos);
+                                                                     eb, slot, pos, pe_lo);
         else
           errbits |= insert_consume_rows<F, NORM, ROPE, true, true>(a, src, l, lane, cptr, k,
-                                                                    eb, slot, pos);
+                                                                    eb, slot, pos, pe_lo);
       }
     }
   }
