@@ -136,17 +136,20 @@ int mla_set_pointer_checks(int enable);
  * Returns the previous setting. */
 int mla_set_gather_early_tables(int enable);
 
-/* Let the grouped insert (mla_cache_insert_grouped) read kv_cache_ptrs and
- * kv_scales BEFORE it waits for the previous grid on the stream (1), or keep
- * plain stream order (0, the default), for every later call from this
- * process.  The same contract as mla_set_gather_early_tables: with 1 and PDL
- * on, those two arrays must be complete before the call is enqueued, or be
- * written by stream work that does not trigger its dependents early.  Used by
- * the row-per-warp shape for calls of 2048 rows (tokens x layers) or more,
- * whose per-layer table (cache bases, division constants) is then built while
- * the previous kernel finishes (4096 tokens x 5 layers back to back: 10.4 vs
- * 11.0 us); the bulk-copy shape and smaller calls read them after the wait
- * either way.  Results are identical.  Returns the previous setting. */
+/* Let the grouped insert (mla_cache_insert_grouped) read kv_cache_ptrs,
+ * kv_scales and the RMSNorm gamma BEFORE it waits for the previous grid on
+ * the stream (1), or keep plain stream order (0, the default), for every
+ * later call from this process.  The same contract as
+ * mla_set_gather_early_tables: with 1 and PDL on, those arrays must be
+ * complete before the call is enqueued, or be written by stream work that
+ * does not trigger its dependents early.  The per-layer table (cache bases,
+ * division constants; in the bulk-copy shape also whether a layer's gamma
+ * bound lets normalised rows skip the special-value test) is then built while
+ * the previous kernel finishes: row-per-warp calls of 2048 rows (tokens x
+ * layers) or more (4096 tokens x 5 layers back to back: 10.4 vs 11.0 us) and
+ * bulk-copy calls (8192 tokens x 5 layers: 17.2 vs 17.4 us); smaller calls
+ * read them after the wait either way.  Results are identical.  Returns the
+ * previous setting. */
 int mla_set_insert_early_tables(int enable);
 
 /* TESTING HOOK for the grouped insert's bulk-copy pipeline, applied to every

@@ -656,8 +656,13 @@ __global__ void __launch_bounds__(kIThreads, 1) insert_tma_kernel(const InsertAr
   // insert, a trigger at the start cost ~80 us (506.7 vs 588 us per step) and
   // one after each CTA's last copy ~60 us (0.464 vs 0.524 ms): the launch
   // follows the last CTA's exit.
-  pdl_wait();
+  // With early_tables (cache_ptrs, scales and gamma declared complete before
+  // the call) the consumers build the per-layer table before the wait on the
+  // previous grid (8192 tokens x 5 layers back to back: 17.39 -> 17.19 us);
+  // the producer, which reads kv_c, always waits first.
+  if (!a.early_tables) pdl_wait();
   __syncthreads();  // the barriers are initialised
+  if (warp == kIConsumers) pdl_wait();
   // The producer starts copying at once; the consumers first fill the
   // per-layer table (one warp per layer: cache base, scale, and whether
   // normalised rows need the special-value test) and sync among themselves.
@@ -683,6 +688,7 @@ __global__ void __launch_bounds__(kIThreads, 1) insert_tma_kernel(const InsertAr
       }
     }
     asm volatile("bar.sync 1, %0;" ::"n"(kIConsumers * 32) : "memory");
+    pdl_wait();  // (a no-op without early_tables)
   }
 
   const int L = a.num_layers;

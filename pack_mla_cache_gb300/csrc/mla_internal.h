@@ -37,8 +37,9 @@ struct InsertArgs {
   // consumer waiting for that item runs out of time.
   uint64_t wait_limit_ns;
   int64_t skip_item;
-  // row shape: cache_ptrs and scales may be read into the per-layer table
-  // before the wait on the previous grid (the caller declared them complete)
+  // cache_ptrs, scales (and, in the bulk-copy shape, gamma) may be read into
+  // the per-layer table before the wait on the previous grid (the caller
+  // declared them complete)
   bool early_tables;
 };
 

@@ -444,28 +444,34 @@ def _insert_with_tables(wl, kv_c, k_pe, slots, ptr_t, sc_t, gamma, pos, table, e
                                  eps=wl.eps, positions=pos, cos_sin_cache=table, err_word=err)
 
 
-def test_layer_tables_written_just_before_each_call(orc):
-    """With programmatic dependent launch on, per-layer cache pointers and
-    scales written by ordinary kernels enqueued just before each call (they
+@pytest.mark.parametrize("shape", [0, 2], ids=["rows", "ring"])
+def test_layer_tables_written_just_before_each_call(orc, shape):
+    """With programmatic dependent launch on, per-layer cache pointers, scales
+    and gamma written by ordinary kernels enqueued just before each call (they
     trigger no early launch) are the ones the insert uses, in plain stream
-    order (the default) and when the row shape builds its per-layer table
-    before waiting on the previous grid (mla_set_insert_early_tables): two
-    back-to-back calls of 4096 tokens x 5 layers (e4m3, RMSNorm + RoPE, the row
-    shape) through ONE pointer array and ONE scale array into two sets of
-    caches with two sets of scales.  Both modes give the same bits, and each
-    set equals the oracle with its own scales."""
+    order (the default) and when the per-layer table is built before the wait
+    on the previous grid (mla_set_insert_early_tables), in the row shape and in
+    the bulk-copy shape: two back-to-back calls of 4096 tokens x 5 layers
+    (e4m3, RMSNorm + RoPE) through ONE pointer array, ONE scale array and ONE
+    gamma array into two sets of caches with two sets of scales and gamma.
+    Both modes give the same bits, and each set equals the oracle with its own
+    scales and gamma."""
     wl = W.insert_workload(5, 4096, 1, num_blocks=128, block_size=64, norm=True, rope=True,
                            seed=43)
     scales = [wl.k_scales, (wl.k_scales * 2.5).astype(np.float32)]
+    gammas = [wl.gamma, np.ascontiguousarray(wl.gamma[::-1])]
     table = D.gpu_rope_table()
     kv_c, k_pe = D.dev_bf16(wl.kv_c), D.dev_bf16(wl.k_pe)
     slots = D.dev(np.ascontiguousarray(wl.slot_mapping[0]))
-    gamma, pos = D.dev_bf16(wl.gamma), D.dev(wl.positions)
+    pos = D.dev(wl.positions)
+    src_g = [D.dev_bf16(g) for g in gammas]
+    gamma = torch.zeros_like(src_g[0])
     nbytes = wl.num_blocks * wl.block_size * W.ENTRY
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     results = {}
     prev = ops.mla_set_pdl(True)
     prev_early = ops.mla_set_insert_early_tables(False)
+    prev_bulk = ops.mla_set_bulk_copy(shape)
     try:
         for early in (False, True):
             ops.mla_set_insert_early_tables(early)
@@ -481,10 +487,12 @@ def test_layer_tables_written_just_before_each_call(orc):
             for k in range(2):
                 ptr_t.copy_(src_ptrs[k])
                 sc_t.copy_(src_sc[k])
+                gamma.copy_(src_g[k])
                 _insert_with_tables(wl, kv_c, k_pe, slots, ptr_t, sc_t, gamma, pos, table, err)
-                if k == 0:  # scramble both arrays after the first call (kernels again)
+                if k == 0:  # scramble the arrays after the first call (kernels again)
                     ptr_t.zero_()
                     sc_t.fill_(-1.0)
+                    gamma.fill_(0.0)
             torch.cuda.synchronize()
             assert int(err.item()) == 0
             assert all(c.guards_intact() for cs in sets for c in cs)
@@ -492,16 +500,18 @@ def test_layer_tables_written_just_before_each_call(orc):
     finally:
         ops.mla_set_pdl(prev)
         ops.mla_set_insert_early_tables(prev_early)
+        ops.mla_set_bulk_copy(prev_bulk)
     for k in range(2):
         assert_exact(results[True][k], results[False][k])
-        ref, rerr = oracle_insert(orc, dataclasses.replace(wl, k_scales=scales[k]),
+        ref, rerr = oracle_insert(orc, dataclasses.replace(wl, k_scales=scales[k], gamma=gammas[k]),
                                   orc.rope_cos_sin_cache(W.MAX_POSITION, 64, W.ROPE_BASE),
                                   fill=0x33)
         assert rerr == 0
         assert_within_tolerance(results[False][k], ref, 1)
 
 
-def test_default_order_sees_layer_tables_written_by_a_pdl_kernel(orc):
+@pytest.mark.parametrize("shape", [0, 2], ids=["rows", "ring"])
+def test_default_order_sees_layer_tables_written_by_a_pdl_kernel(orc, shape):
     """In the default (plain stream order) the insert reads kv_cache_ptrs and
     kv_scales only after the previous grid has completed, even when that grid
     is a library kernel that lets its dependents launch at its start: here a
@@ -531,6 +541,7 @@ def test_default_order_sees_layer_tables_written_by_a_pdl_kernel(orc):
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     prev = ops.mla_set_pdl(True)
     prev_early = ops.mla_set_insert_early_tables(False)
+    prev_bulk = ops.mla_set_bulk_copy(shape)
     try:
         for _ in range(3):
             tab.zero_()
@@ -542,6 +553,7 @@ def test_default_order_sees_layer_tables_written_by_a_pdl_kernel(orc):
     finally:
         ops.mla_set_pdl(prev)
         ops.mla_set_insert_early_tables(prev_early)
+        ops.mla_set_bulk_copy(prev_bulk)
     assert int(err.item()) == 0
     assert all(c.guards_intact() for c in caches)
     ref, rerr = oracle_insert(orc, wl, orc.rope_cos_sin_cache(W.MAX_POSITION, 64, W.ROPE_BASE),
