@@ -256,6 +256,37 @@ __device__ __forceinline__ bool load_rope(const InsertArgs& a, int64_t t, int la
   return true;
 }
 
+// Whether normalised kv_c values of a layer can make the exact division's
+// first quotient overflow, so each group of 8 needs the special-value test.
+// A normalised element is x_i * gamma_i * rstd with x_i^2 <= sum(x^2): when
+// the row's sum of squares is finite, |y_i| <= sqrt(512) |gamma_i| (1 + 2^-7)
+// < 23 gmax, and x_i * gamma_i cannot overflow while gmax < 2^64 (|x_i| <
+// 2^64 then); when it is infinite or NaN, rstd is 0 or NaN and every y_i is
+// +-0 or NaN, which the fast path also handles.  So the test can be skipped
+// when 23 gmax stays below the first value the test would flag, 2^(T - 127)
+// with T the threshold exponent field of thr2.  gmax: the layer's largest
+// |gamma| (inf / NaN: the test stays).
+__device__ __forceinline__ bool layer_needs_check(const DivConst& k, uint32_t gmax_bits) {
+  if (!k.fast) return true;
+  const uint32_t h = k.thr2 & 0xFFFFu;           // 0x8000 - (T << 7)
+  const int T = (int)((0x8000u - h) >> 7);
+  const float lim = ldexpf(1.0f, T - 127);       // inf for T = 255
+  const float g = __uint_as_float(gmax_bits << 16);
+  return !(g < 1.8446744e19f && 23.0f * g < lim);
+}
+
+// The largest |gamma| of layer l as bf16 bits (a NaN's bits exceed every
+// finite one's), over the whole warp; all 32 lanes call it together.
+__device__ __forceinline__ uint32_t layer_gmax(const InsertArgs& a, int l, int lane) {
+  const uint8_t* g = a.gamma + (int64_t)l * a.gamma_ls;
+  const uint4 g0 = ld_shared_ro16(g + lane * 16), g1 = ld_shared_ro16(g + 512 + lane * 16);
+  const uint32_t m = umax16x2(umax16x2(umax16x2(g0.x & 0x7FFF7FFFu, g0.y & 0x7FFF7FFFu),
+                                       umax16x2(g0.z & 0x7FFF7FFFu, g0.w & 0x7FFF7FFFu)),
+                              umax16x2(umax16x2(g1.x & 0x7FFF7FFFu, g1.y & 0x7FFF7FFFu),
+                                       umax16x2(g1.z & 0x7FFF7FFFu, g1.w & 0x7FFF7FFFu)));
+  return __reduce_max_sync(0xFFFFFFFFu, max(m & 0xFFFFu, m >> 16));
+}
+
 // Shape 1: one warp per (token, layer) row, rows in token-major order.  For
 // more than a few rows per warp each CTA first puts the layers' cache bases
 // and division constants in shared memory; tiny calls (decode) skip that step,
@@ -267,10 +298,21 @@ constexpr int64_t kRowPreloadMinRows = 2048;
 // against 10.94 us.
 constexpr int64_t kRowPairsMinRows = 8192;
 
-template <int F, bool NORM, bool ROPE, bool PAIRS>
+// TRIM (normalised fp8 rows two per warp, per-layer tables built before the
+// launch wait): the rows are computed negated (the exact division then skips
+// its negation) and, per layer, without the special-value test when the gamma
+// bound allows it, as in the bulk-copy shape (4096 tokens x 5 layers back to
+// back: 10.37 -> 10.07 us).  Only with early tables: after the wait the gamma
+// loads and reduction cost more than the test they save (2048 tokens x 5
+// layers 7.43 vs 7.24 us), and the negated form with the test kept is slower
+// than the plain one (11.30 vs 10.95 us).
+template <int F, bool NORM, bool ROPE, bool PAIRS, bool TRIM = false>
 __global__ void __launch_bounds__(kThreads) insert_row_kernel(const InsertArgs a) {
+  static_assert(!TRIM || (PAIRS && NORM && F != kBF16), "TRIM: normalised fp8 pairs");
+  constexpr bool kTrim = TRIM;
   __shared__ int64_t s_cptr[kMaxLayers];
   __shared__ DivConst s_k[F == kBF16 ? 1 : kMaxLayers];
+  __shared__ uint8_t s_check[kTrim ? kMaxLayers : 1];
   pdl_trigger();
   // The per-layer table (cache bases, division constants) reads only
   // cache_ptrs and scales.  When the caller has declared them complete before
@@ -284,6 +326,13 @@ __global__ void __launch_bounds__(kThreads) insert_row_kernel(const InsertArgs a
     for (int l = threadIdx.x; l < a.num_layers; l += kThreads) {
       s_cptr[l] = a.cache_ptrs[l];
       if constexpr (F != kBF16) s_k[l] = div_const(a.scales[l]);
+    }
+    if constexpr (kTrim) {  // the gamma bound, one warp per layer
+      for (int l = threadIdx.x >> 5; l < a.num_layers; l += kThreads / 32) {
+        const bool check = layer_needs_check(div_const(a.scales[l]),
+                                             layer_gmax(a, l, threadIdx.x & 31));
+        if ((threadIdx.x & 31) == 0) s_check[l] = check ? 1 : 0;
+      }
     }
     __syncthreads();
   }
@@ -352,13 +401,24 @@ __global__ void __launch_bounds__(kThreads) insert_row_kernel(const InsertArgs a
       }
       // every lane: the shuffles span the warp (a lane without a row reads
       // layer 0's weights)
-      if constexpr (NORM) rms_norm32_g(x, have ? gr : a.gamma + hl * 16, a.eps);
+      if constexpr (NORM) rms_norm32_g<kTrim>(x, have ? gr : a.gamma + hl * 16, a.eps);
       if constexpr (ROPE) rope_pairs2(lo, hi, cs);
       if (ok) {
         if (F == kBF16 || k.fast) {
-          write_kv32<F, true, false, true>(dst, hl, x, k);
+          if constexpr (kTrim) {
+            if (s_check[l]) write_kv32<F, true, true, true>(dst, hl, x, k);
+            else write_kv32<F, true, true, false>(dst, hl, x, k);
+          } else {
+            write_kv32<F, true, false, true>(dst, hl, x, k);
+          }
           write_pe32<F, true>(dst, hl, lo, hi, k);
         } else {
+          if constexpr (kTrim) {  // undo the negation (exact: a sign flip)
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              x[c] = make_uint4(x[c].x ^ 0x80008000u, x[c].y ^ 0x80008000u,
+                                x[c].z ^ 0x80008000u, x[c].w ^ 0x80008000u);
+          }
           write_kv32<F, false, false, true>(dst, hl, x, k);
           write_pe32<F, false>(dst, hl, lo, hi, k);
         }
@@ -612,25 +672,6 @@ __device__ __forceinline__ uint32_t insert_consume_pairs(
   return err;
 }
 
-// Whether normalised kv_c values of a layer can make the exact division's
-// first quotient overflow, so each group of 8 needs the special-value test.
-// A normalised element is x_i * gamma_i * rstd with x_i^2 <= sum(x^2): when
-// the row's sum of squares is finite, |y_i| <= sqrt(512) |gamma_i| (1 + 2^-7)
-// < 23 gmax, and x_i * gamma_i cannot overflow while gmax < 2^64 (|x_i| <
-// 2^64 then); when it is infinite or NaN, rstd is 0 or NaN and every y_i is
-// +-0 or NaN, which the fast path also handles.  So the test can be skipped
-// when 23 gmax stays below the first value the test would flag, 2^(T - 127)
-// with T the threshold exponent field of thr2.  gmax: the layer's largest
-// |gamma| (inf / NaN: the test stays).
-__device__ __forceinline__ bool layer_needs_check(const DivConst& k, uint32_t gmax_bits) {
-  if (!k.fast) return true;
-  const uint32_t h = k.thr2 & 0xFFFFu;           // 0x8000 - (T << 7)
-  const int T = (int)((0x8000u - h) >> 7);
-  const float lim = ldexpf(1.0f, T - 127);       // inf for T = 255
-  const float g = __uint_as_float(gmax_bits << 16);
-  return !(g < 1.8446744e19f && 23.0f * g < lim);
-}
-
 template <int F, bool NORM, bool ROPE>
 __global__ void __launch_bounds__(kIThreads, 1) insert_tma_kernel(const InsertArgs a) {
   constexpr int kIStages = Ring<NORM>::kStages;
@@ -869,6 +910,8 @@ cudaError_t launch_t(const InsertArgs& a, const LaunchCfg& cfg) {
   const bool pairs = (NORM || ROPE) && a.num_rows >= kRowPairsMinRows;
   auto kern = pairs ? insert_row_kernel<F, NORM, ROPE, NORM || ROPE>
                     : insert_row_kernel<F, NORM, ROPE, false>;
+  if constexpr (NORM && F != kBF16)
+    if (pairs && a.early_tables) kern = insert_row_kernel<F, NORM, ROPE, true, true>;
   const int64_t rows_per_warp = pairs ? 2 : 1;
   const int64_t warps = (a.num_rows + rows_per_warp - 1) / rows_per_warp;
   const int64_t ctas = (warps + kThreads / 32 - 1) / (kThreads / 32);

@@ -438,6 +438,35 @@ def test_every_layout_gives_the_same_bits(dtype):
     assert_exact(ring, one)
 
 
+@pytest.mark.parametrize("dtype", [1, 2])
+def test_trimmed_row_shape_gives_the_same_bits(dtype):
+    """With early tables the row shape's two-rows-per-warp RMSNorm form works
+    on negated rows and skips the special-value test for layers whose gamma
+    bound allows it; it must give the bits of the plain form in every case:
+    5 layers whose scales take the fast division without the test (two
+    normal scales), the fast division with the test (a scale so small that
+    normalised values can overflow the quotient), and the guarded division (a
+    subnormal scale and a huge one), 2048 tokens x 5 layers (two rows per
+    warp, each pair's rows in different layers), with inf / NaN rows mixed in."""
+    wl = W.insert_workload(5, 2048, dtype, num_blocks=256, block_size=64, norm=True, rope=True,
+                           seed=47)
+    wl.k_scales = np.array([0.0123, 3.0, 1e-36, 1e-39, 1e38], np.float32)
+    kv = wl.kv_c.copy()
+    kv[2, 7, 5] = 0x7F80   # +inf in one row
+    kv[3, 9, 100] = 0x7FC0  # NaN in another
+    wl.kv_c = kv
+    table = D.gpu_rope_table()
+    prev = ops.mla_set_insert_early_tables(False)
+    try:
+        plain, g1, _ = D.gpu_insert(wl, cos_sin=table, fill=0x21)
+        ops.mla_set_insert_early_tables(True)
+        trimmed, g2, _ = D.gpu_insert(wl, cos_sin=table, fill=0x21)
+    finally:
+        ops.mla_set_insert_early_tables(prev)
+    assert g1 and g2
+    assert_exact(trimmed, plain)
+
+
 def _insert_with_tables(wl, kv_c, k_pe, slots, ptr_t, sc_t, gamma, pos, table, err):
     ops.mla_cache_insert_grouped(kv_c, k_pe, slots, ptr_t, sc_t, wl.cache_dtype, wl.num_blocks,
                                  wl.block_size, wl.block_stride, wl.entry_stride, gamma=gamma,
