@@ -193,6 +193,38 @@ __device__ __forceinline__ void write_kv32(uint8_t* dst, int hl, const uint4 (&x
   }
 }
 
+// Quarter-warp rows (8 lanes per row, norm_rope.cuh): the kv_c part of a row
+// held as x[8] (units ql + 16 c and ql + 8 + 16 c).
+template <int F, bool FAST, bool NEG, bool CHECK>
+__device__ __forceinline__ void write_kv64(uint8_t* dst, int ql, const uint4 (&x)[8],
+                                           const DivConst& k) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const int u = ql + 16 * (c & 3) + 8 * (c >> 2);
+    if constexpr (F == kBF16) st16(dst + u * 16, x[c]);
+    else if constexpr (NEG) st8(dst + u * 8, neg_bf16x8_to_fp8x8<F, CHECK>(x[c], k));
+    else st8(dst + u * 8, bf16x8_to_fp8x8<F, FAST>(x[c], k));
+  }
+}
+
+// The k_pe elements 4 ql .. 4 ql + 3 (lo) and 4 ql + 32 .. 4 ql + 35 (hi) of a
+// row held by a quarter warp.
+template <int F, bool FAST>
+__device__ __forceinline__ void write_pe64(uint8_t* dst, int ql, uint2 lo, uint2 hi,
+                                           const DivConst& k) {
+  if constexpr (F == kBF16) {
+    st8(dst + 2 * kR + ql * 8, lo);
+    st8(dst + 2 * kR + kP + ql * 8, hi);
+  } else {
+    const uint32_t a = (bf16x2_to_fp8x2<F, FAST>(lo.x, k) & 0xFFFFu) |
+                       (bf16x2_to_fp8x2<F, FAST>(lo.y, k) << 16);
+    const uint32_t b = (bf16x2_to_fp8x2<F, FAST>(hi.x, k) & 0xFFFFu) |
+                       (bf16x2_to_fp8x2<F, FAST>(hi.y, k) << 16);
+    *reinterpret_cast<uint32_t*>(dst + kR + ql * 4) = a;
+    *reinterpret_cast<uint32_t*>(dst + kR + kP / 2 + ql * 4) = b;
+  }
+}
+
 // The k_pe words lo (elements 2 hl, 2 hl + 1) and hi (2 hl + 32, 2 hl + 33)
 // of a row held by a half warp.
 template <int F, bool FAST>
@@ -440,6 +472,123 @@ __global__ void __launch_bounds__(kThreads) insert_row_kernel(const InsertArgs a
       errbits |= store_row<F, NORM, ROPE>(a, l, lane, in, pos_ok, cs, cptr, k);
     }
   }
+  if (errbits && lane == 0 && a.err) atomicOr(a.err, errbits);
+}
+
+// Shape 1, four rows per warp (8 lanes each, the quarter-warp layout of
+// norm_rope.cuh), for calls with RMSNorm or RoPE that it covers in one round
+// where two rows per warp would take two (see launch_t): at 80 registers (3
+// CTAs per SM) a round takes 14592 rows against 9728.  The same arithmetic,
+// hence the same bits, as the other layouts; TRIM as in insert_row_kernel.
+template <int F, bool NORM, bool ROPE, bool TRIM>
+__global__ void __launch_bounds__(kThreads, 3) insert_quad_kernel(const InsertArgs a) {
+  static_assert(NORM || ROPE, "the quad layout serves RMSNorm / RoPE rows");
+  static_assert(!TRIM || (NORM && F != kBF16), "TRIM: normalised fp8 rows");
+  __shared__ int64_t s_cptr[kMaxLayers];
+  __shared__ DivConst s_k[F == kBF16 ? 1 : kMaxLayers];
+  __shared__ uint8_t s_check[TRIM ? kMaxLayers : 1];
+  pdl_trigger();
+  if (!a.early_tables) pdl_wait();
+  for (int l = threadIdx.x; l < a.num_layers; l += kThreads) {
+    s_cptr[l] = a.cache_ptrs[l];
+    if constexpr (F != kBF16) s_k[l] = div_const(a.scales[l]);
+  }
+  if constexpr (TRIM) {  // the gamma bound, one warp per layer
+    for (int l = threadIdx.x >> 5; l < a.num_layers; l += kThreads / 32) {
+      const bool check = layer_needs_check(div_const(a.scales[l]),
+                                           layer_gmax(a, l, threadIdx.x & 31));
+      if ((threadIdx.x & 31) == 0) s_check[l] = check ? 1 : 0;
+    }
+  }
+  __syncthreads();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int ql = lane & 7, quad = lane >> 3;
+  const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
+  uint32_t errbits = 0;
+  const bool rows32 = a.num_rows < (int64_t(1) << 32);
+  // the rows 4w + quad, 4w + quad + 4 nwarps, ...
+  for (int64_t r0 = 4 * warp; r0 < a.num_rows; r0 += 4 * nwarps) {
+    const int64_t r = r0 + quad;
+    const bool have = r < a.num_rows;
+    int64_t t = 0;
+    int l = 0;
+    uint4 x[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) x[c] = make_uint4(0, 0, 0, 0);
+    uint2 lo = make_uint2(0, 0), hi = make_uint2(0, 0);
+    int64_t slot = -1, pos = 0;
+    if (have) {
+      if (rows32) {
+        const uint32_t tu = (uint32_t)r / (uint32_t)a.num_layers;
+        t = tu;
+        l = (int)((uint32_t)r - tu * (uint32_t)a.num_layers);
+      } else {
+        t = r / a.num_layers;
+        l = (int)(r - t * a.num_layers);
+      }
+      const uint8_t* src = a.kv_c + t * a.kvc_ts + (int64_t)l * a.kvc_ls + ql * 16;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) x[c] = ld_stream16(src + 256 * (c & 3) + 128 * (c >> 2));
+      const uint8_t* pe = a.k_pe + t * a.kpe_ts + (int64_t)l * a.kpe_ls + ql * 8;
+      lo = ld_stream8(pe);
+      hi = ld_stream8(pe + kP);
+      slot = __ldg(a.slots + (int64_t)l * a.slot_ls + t);
+      if (ROPE) pos = __ldg(a.positions + t);
+    }
+    DivConst k{};
+    float4 cc = make_float4(1.f, 1.f, 1.f, 1.f), sn = make_float4(0.f, 0.f, 0.f, 0.f);
+    const uint8_t* gr = a.gamma + ql * 16;
+    bool ok = false;
+    uint8_t* dst = nullptr;
+    if (have) {
+      if constexpr (F != kBF16) k = s_k[l];
+      const int64_t cptr = s_cptr[l];
+      if (slot < 0) {
+      } else if (slot >= a.capacity) {
+        errbits |= kErrSlotOOB;
+      } else if (ROPE && (pos < 0 || pos >= a.max_position)) {
+        errbits |= kErrPosOOB;
+      } else if (cptr == 0 || (cptr & 15)) {
+        errbits |= kErrMisaligned;
+      } else {
+        ok = true;
+        dst = slot_dst(a, slot, cptr);
+      }
+      if (ROPE && ok) {
+        const float* row = a.cos_sin + pos * kP;
+        cc = __ldg(reinterpret_cast<const float4*>(row + 4 * ql));
+        sn = __ldg(reinterpret_cast<const float4*>(row + 32 + 4 * ql));
+      }
+      if constexpr (NORM) gr = a.gamma + (int64_t)l * a.gamma_ls + ql * 16;
+    }
+    // every lane: the shuffles span the warp (a lane without a row reads
+    // layer 0's weights)
+    if constexpr (NORM) rms_norm64_g<TRIM>(x, gr, a.eps);
+    if constexpr (ROPE) rope_pairs4(lo, hi, cc, sn);
+    if (ok) {
+      if (F == kBF16 || k.fast) {
+        if constexpr (TRIM) {
+          if (s_check[l]) write_kv64<F, true, true, true>(dst, ql, x, k);
+          else write_kv64<F, true, true, false>(dst, ql, x, k);
+        } else {
+          write_kv64<F, true, false, true>(dst, ql, x, k);
+        }
+        write_pe64<F, true>(dst, ql, lo, hi, k);
+      } else {
+        if constexpr (TRIM) {  // undo the negation (exact: a sign flip)
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            x[c] = make_uint4(x[c].x ^ 0x80008000u, x[c].y ^ 0x80008000u,
+                              x[c].z ^ 0x80008000u, x[c].w ^ 0x80008000u);
+        }
+        write_kv64<F, false, false, true>(dst, ql, x, k);
+        write_pe64<F, false>(dst, ql, lo, hi, k);
+      }
+    }
+  }
+  errbits = __reduce_or_sync(0xFFFFFFFFu, errbits);
   if (errbits && lane == 0 && a.err) atomicOr(a.err, errbits);
 }
 
@@ -912,7 +1061,26 @@ cudaError_t launch_t(const InsertArgs& a, const LaunchCfg& cfg) {
                     : insert_row_kernel<F, NORM, ROPE, false>;
   if constexpr (NORM && F != kBF16)
     if (pairs && a.early_tables) kern = insert_row_kernel<F, NORM, ROPE, true, true>;
-  const int64_t rows_per_warp = pairs ? 2 : 1;
+  // Four rows per warp where that takes one round and two rows per warp would
+  // take two: a round of either shape costs about the same per row, but a
+  // second, partly filled round of the two-row shape costs a whole round's
+  // latency (1800 tokens x 5 layers: 5.24 vs 6.14 us; 2048: 6.51 vs 6.32;
+  // 2400: 7.25 vs 6.57; 2800: 8.27 vs 6.88; 3200: 8.41 vs 8.98).
+  bool quads = false;
+  if constexpr (NORM || ROPE) {
+    if (pairs) {
+      auto qkern = insert_quad_kernel<F, NORM, ROPE, false>;
+      const int64_t pair_rows = (int64_t)capped_grid(reinterpret_cast<const void*>(kern), kThreads,
+                                                     int64_t(1) << 30) * (kThreads / 32) * 2;
+      const int64_t quad_rows = (int64_t)capped_grid(reinterpret_cast<const void*>(qkern), kThreads,
+                                                     int64_t(1) << 30) * (kThreads / 32) * 4;
+      quads = a.num_rows > pair_rows && a.num_rows <= quad_rows;
+      if (quads) kern = insert_quad_kernel<F, NORM, ROPE, false>;
+      if constexpr (NORM && F != kBF16)
+        if (quads && a.early_tables) kern = insert_quad_kernel<F, NORM, ROPE, true>;
+    }
+  }
+  const int64_t rows_per_warp = quads ? 4 : pairs ? 2 : 1;
   const int64_t warps = (a.num_rows + rows_per_warp - 1) / rows_per_warp;
   const int64_t ctas = (warps + kThreads / 32 - 1) / (kThreads / 32);
   cudaLaunchConfig_t lc = {};

@@ -202,4 +202,57 @@ __device__ __forceinline__ float4 load_cs2(const float* row, int hl) {
   return make_float4(c.x, c.y, s.x, s.y);
 }
 
+// ---- rows held by a quarter warp ----------------------------------------------
+// Quarter-warp layout (8 lanes per row, four rows per warp): lane ql = lane & 7
+// of a quarter holds positions ql and ql + 8 of the tree above: x[c] is unit
+// ql + 16 c and x[4 + c] unit ql + 8 + 16 c (bytes 16 ql + 256 c and 16 ql +
+// 128 + 256 c of the bf16 row); its k_pe elements are 4 ql .. 4 ql + 3 (lo)
+// and 4 ql + 32 .. 4 ql + 35 (hi), the neox pairs (4 ql + j, 4 ql + 32 + j).
+// The row-uniform work is shared by the four rows a warp instruction serves.
+
+// This lane's sum of its two positions: the butterfly's offset-8 step taken
+// inside the lane (position ql first, as in the half-warp layout's lane ql).
+__device__ __forceinline__ float sum_sq64(const uint4 (&x)[8]) {
+  const float a = (unit_sq(x[0]) + unit_sq(x[1])) + (unit_sq(x[2]) + unit_sq(x[3]));
+  const float b = (unit_sq(x[4]) + unit_sq(x[5])) + (unit_sq(x[6]) + unit_sq(x[7]));
+  return a + b;
+}
+
+// The rest of the butterfly (offsets 4, 2, 1) over the 8 lanes of a quarter.
+__device__ __forceinline__ float quarter_sum(float v) {
+#pragma unroll
+  for (int o = 4; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+// RMSNorm of this lane's 64 kv_c elements in place, gamma read unit by unit
+// from `gr` (this lane's unit ql of the row's weights) where it is used.
+template <bool NEG = false>
+__device__ __forceinline__ void rms_norm64_g(uint4 (&x)[8], const uint8_t* gr, float eps) {
+  const float ss = quarter_sum(sum_sq64(x));
+  const float rstd = __frsqrt_rn(fmaf(ss, 1.0f / kNormRank, eps));
+  const uint64_t rstd2 = NEG ? f2(-rstd, -rstd) : f2(rstd, rstd);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint4 g = __ldg(reinterpret_cast<const uint4*>(gr + 256 * (c & 3) + 128 * (c >> 2)));
+    const uint32_t w[4] = {x[c].x, x[c].y, x[c].z, x[c].w};
+    const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint64_t xg = f2(fma_bf16lo(w[i], gw[i], -0.0f), fma_bf16hi(w[i], gw[i], -0.0f));
+      const float2 y = unf2(mul2(xg, rstd2));
+      o[i] = pack_bf16x2(y.x, y.y);
+    }
+    x[c] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// The neox rotation of this lane's four k_pe pairs in place; c = cos of
+// elements 4 ql .. 4 ql + 3, sn = their sin.
+__device__ __forceinline__ void rope_pairs4(uint2& lo, uint2& hi, float4 c, float4 sn) {
+  rope_pairs2(lo.x, hi.x, make_float4(c.x, c.y, sn.x, sn.y));
+  rope_pairs2(lo.y, hi.y, make_float4(c.z, c.w, sn.z, sn.w));
+}
+
 }  // namespace mla

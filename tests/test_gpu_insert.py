@@ -438,6 +438,39 @@ def test_every_layout_gives_the_same_bits(dtype):
     assert_exact(ring, one)
 
 
+@pytest.mark.parametrize("early", [False, True], ids=["stream_order", "early_tables"])
+@pytest.mark.parametrize("dtype,norm,rope,shared", [(1, True, True, True), (2, True, True, False),
+                                                    (0, True, True, True), (1, True, False, True),
+                                                    (1, False, True, False)])
+def test_four_rows_per_warp_against_oracle(orc, dtype, norm, rope, shared, early):
+    """2400 tokens x 5 layers (12000 rows): more than one round of the
+    two-rows-per-warp row shape, one round of four rows per warp, so the
+    quarter-warp kernel runs; against the oracle with RMSNorm and / or RoPE,
+    bf16 / e4m3 / e5m2 caches, shared and per-layer mappings, with an
+    out-of-range slot, a padding slot and an out-of-table position mixed in."""
+    wl = W.insert_workload(5, 2400, dtype, num_blocks=256, block_size=64, shared_slots=shared,
+                           norm=norm, rope=rope, seed=50 + dtype)
+    wl.slot_mapping = wl.slot_mapping.copy()
+    wl.slot_mapping[:, 17] = -1
+    wl.slot_mapping[:, 1000] = 256 * 64 + 5  # beyond the cache
+    if rope:
+        wl.positions = wl.positions.copy()
+        wl.positions[2222] = W.MAX_POSITION
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    prev = ops.mla_set_insert_early_tables(early)
+    try:
+        gpu, guards, _ = D.gpu_insert(wl, cos_sin=D.gpu_rope_table() if rope else None, fill=0x19,
+                                      err=err)
+    finally:
+        ops.mla_set_insert_early_tables(prev)
+    ref, oerr = oracle_insert(orc, wl, orc.rope_cos_sin_cache(W.MAX_POSITION, 64, W.ROPE_BASE)
+                              if rope else None, fill=0x1919 if dtype == 0 else 0x19)
+    assert guards
+    assert int(err.item()) == oerr
+    assert oerr & ops.MLA_ERRBIT_SLOT_OOB
+    assert_within_tolerance(gpu, ref, dtype)
+
+
 @pytest.mark.parametrize("dtype", [1, 2])
 def test_trimmed_row_shape_gives_the_same_bits(dtype):
     """With early tables the row shape's two-rows-per-warp RMSNorm form works
