@@ -324,11 +324,6 @@ __device__ __forceinline__ uint32_t layer_gmax(const InsertArgs& a, int l, int l
 // and division constants in shared memory; tiny calls (decode) skip that step,
 // which would sit on their critical path, and load them per row.
 constexpr int64_t kRowPreloadMinRows = 2048;
-// From this many rows (with RMSNorm or RoPE) the row shape takes two rows per
-// warp: 5120 rows (1024 tokens x 5 layers) ran 4.57 us with one row per warp
-// against 5.37 us with two, 10240 rows 7.43 against 7.26 us, 20480 11.34
-// against 10.94 us.
-constexpr int64_t kRowPairsMinRows = 8192;
 
 // TRIM (normalised fp8 rows two per warp, per-layer tables built before the
 // launch wait): the rows are computed negated (the exact division then skips
@@ -1053,10 +1048,19 @@ cudaError_t launch_t(const InsertArgs& a, const LaunchCfg& cfg) {
   const int64_t min_rows = NORM ? kBulkMinRowsNorm : kBulkMinRows;
   const bool bulk = a.bulk_mode == 2 || (a.bulk_mode == 1 && a.num_rows >= min_rows);
   if (bulk && insert_tma_layout(a)) return launch_tma<F, NORM, ROPE>(a, cfg);
-  // With RMSNorm or RoPE, calls from kRowPairsMinRows rows take two rows per
-  // warp (half-warp layout); smaller calls, one wave of latency-bound warps,
-  // one row per warp.  Both layouts compute the same bits.
-  const bool pairs = (NORM || ROPE) && a.num_rows >= kRowPairsMinRows;
+  // With RMSNorm or RoPE the row shape takes one, two or four rows per warp
+  // (the same bits in every layout).  Two rows per warp once one row per warp
+  // would take a second round (its
+  // 48 registers allow 5 CTAs per SM: 6080 rows a round on 152 SMs); within
+  // one round one row per warp is faster (1024 tokens x 5 layers: 4.57 vs 5.37
+  // us).  1400 tokens x 5 layers: 5.33 -> 4.87 us, 1638: 6.57 -> 5.08.
+  bool pairs = false;
+  if constexpr (NORM || ROPE) {
+    const int64_t one_rows = (int64_t)capped_grid(
+        reinterpret_cast<const void*>(insert_row_kernel<F, NORM, ROPE, false>), kThreads,
+        int64_t(1) << 30) * (kThreads / 32);
+    pairs = a.num_rows > one_rows && a.num_rows >= kRowPreloadMinRows;
+  }
   auto kern = pairs ? insert_row_kernel<F, NORM, ROPE, NORM || ROPE>
                     : insert_row_kernel<F, NORM, ROPE, false>;
   if constexpr (NORM && F != kBF16)

@@ -409,32 +409,41 @@ def test_rope_table_matches_oracle(orc):
 
 @pytest.mark.parametrize("dtype", [0, 1])
 def test_every_layout_gives_the_same_bits(dtype):
-    """RMSNorm + RoPE rows are computed one per warp (small calls), two per
-    warp (larger row-shape calls) or by the bulk-copy ring, with one summation
-    tree for the sum of squares: one call of 2048 tokens x 5 layers (two rows
-    per warp), the same rows as two calls of 1024 tokens (one row per warp),
-    and the bulk-copy shape give the same caches bit for bit (a bf16 cache
-    shows the normalised values themselves)."""
+    """RMSNorm + RoPE rows are computed one, two or four per warp in the row
+    shape (by call size) or by the bulk-copy ring, with one summation tree for
+    the sum of squares.  The same 2048 tokens x 5 layers as one call (10240
+    rows: four rows per warp), as calls of 1600 + 448 tokens (8000 rows: two
+    rows per warp; 2240: one), as two calls of 1024 tokens (one row per warp),
+    and through the bulk-copy shape give the same caches bit for bit (a bf16
+    cache shows the normalised values themselves)."""
     wl = W.insert_workload(5, 2048, dtype, num_blocks=256, block_size=64, norm=True, rope=True,
                            seed=41)
     table = D.gpu_rope_table()
+
+    def part(t0, t1):
+        return W.InsertWorkload(5, t1 - t0, dtype, 256, 64,
+                                np.ascontiguousarray(wl.kv_c[:, t0:t1]),
+                                np.ascontiguousarray(wl.k_pe[:, t0:t1]),
+                                np.ascontiguousarray(wl.slot_mapping[:, t0:t1]),
+                                True, wl.k_scales, wl.gamma,
+                                np.ascontiguousarray(wl.positions[t0:t1]))
+
     one, g1, _ = D.gpu_insert(wl, cos_sin=table, fill=0x11)
-    caches = None
-    for h in range(2):
-        sub = W.InsertWorkload(5, 1024, dtype, 256, 64,
-                               np.ascontiguousarray(wl.kv_c[:, h * 1024:(h + 1) * 1024]),
-                               np.ascontiguousarray(wl.k_pe[:, h * 1024:(h + 1) * 1024]),
-                               np.ascontiguousarray(wl.slot_mapping[:, h * 1024:(h + 1) * 1024]),
-                               True, wl.k_scales, wl.gamma,
-                               np.ascontiguousarray(wl.positions[h * 1024:(h + 1) * 1024]))
-        halves, g2, caches = D.gpu_insert(sub, cos_sin=table, fill=0x11, caches=caches)
+    results, guards = [], [g1]
+    for cuts in ((0, 1600, 2048), (0, 1024, 2048)):
+        caches = None
+        for t0, t1 in zip(cuts[:-1], cuts[1:]):
+            out, g, caches = D.gpu_insert(part(t0, t1), cos_sin=table, fill=0x11, caches=caches)
+            guards.append(g)
+        results.append(out)
     prev = ops.mla_set_bulk_copy(2)
     try:
         ring, g3, _ = D.gpu_insert(wl, cos_sin=table, fill=0x11)
     finally:
         ops.mla_set_bulk_copy(prev)
-    assert g1 and g2 and g3
-    assert_exact(halves, one)
+    assert all(guards) and g3
+    for out in results:
+        assert_exact(out, one)
     assert_exact(ring, one)
 
 
@@ -471,17 +480,19 @@ def test_four_rows_per_warp_against_oracle(orc, dtype, norm, rope, shared, early
     assert_within_tolerance(gpu, ref, dtype)
 
 
+@pytest.mark.parametrize("T", [1600, 2048], ids=["two_rows_per_warp", "four_rows_per_warp"])
 @pytest.mark.parametrize("dtype", [1, 2])
-def test_trimmed_row_shape_gives_the_same_bits(dtype):
+def test_trimmed_row_shape_gives_the_same_bits(dtype, T):
     """With early tables the row shape's two-rows-per-warp RMSNorm form works
     on negated rows and skips the special-value test for layers whose gamma
     bound allows it; it must give the bits of the plain form in every case:
     5 layers whose scales take the fast division without the test (two
     normal scales), the fast division with the test (a scale so small that
     normalised values can overflow the quotient), and the guarded division (a
-    subnormal scale and a huge one), 2048 tokens x 5 layers (two rows per
-    warp, each pair's rows in different layers), with inf / NaN rows mixed in."""
-    wl = W.insert_workload(5, 2048, dtype, num_blocks=256, block_size=64, norm=True, rope=True,
+    subnormal scale and a huge one), 1600 tokens x 5 layers (two rows per
+    warp) and 2048 (four rows per warp), the rows a warp instruction serves in
+    different layers, with inf / NaN rows mixed in."""
+    wl = W.insert_workload(5, T, dtype, num_blocks=256, block_size=64, norm=True, rope=True,
                            seed=47)
     wl.k_scales = np.array([0.0123, 3.0, 1e-36, 1e-39, 1e38], np.float32)
     kv = wl.kv_c.copy()

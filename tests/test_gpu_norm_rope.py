@@ -100,9 +100,9 @@ def test_dspark_layout_within_one_ulp(orc, tables, L, T):
 def test_rows_equal_the_bf16_insert(tables, T):
     """The same rows through a bf16 grouped insert (identity slots) and
     through the standalone kernel are bit-identical, in every pairing of
-    layouts: 1024 tokens x 5 layers (one row per warp in both), 2048 (two rows
-    per warp in both), 28000 (the insert's bulk-copy ring, two rows per warp,
-    against one row per warp here)."""
+    layouts: 1024 tokens x 5 layers (one row per warp in both), 2048 (four
+    rows per warp in the insert, two here), 28000 (the insert's bulk-copy
+    ring, two rows per warp, against one row per warp here)."""
     L = 5
     wl = W.insert_workload(L, T, 0, num_blocks=(T + 63) // 64, norm=True, rope=True, seed=60)
     wl.slot_mapping = np.ascontiguousarray(np.tile(np.arange(T, dtype=np.int64), (L, 1)))
