@@ -482,7 +482,7 @@ def test_four_rows_per_warp_against_oracle(orc, dtype, norm, rope, shared, early
 
 @pytest.mark.parametrize("T", [1600, 2048], ids=["two_rows_per_warp", "four_rows_per_warp"])
 @pytest.mark.parametrize("dtype", [1, 2])
-def test_trimmed_row_shape_gives_the_same_bits(dtype, T):
+def test_trimmed_row_shape_gives_the_same_bits(orc, dtype, T):
     """With early tables the row shape's two-rows-per-warp RMSNorm form works
     on negated rows and skips the special-value test for layers whose gamma
     bound allows it; it must give the bits of the plain form in every case:
@@ -509,6 +509,9 @@ def test_trimmed_row_shape_gives_the_same_bits(dtype, T):
         ops.mla_set_insert_early_tables(prev)
     assert g1 and g2
     assert_exact(trimmed, plain)
+    ref, _ = oracle_insert(orc, wl, orc.rope_cos_sin_cache(W.MAX_POSITION, 64, W.ROPE_BASE),
+                           fill=0x21)
+    assert_within_tolerance(plain, ref, dtype)
 
 
 def _insert_with_tables(wl, kv_c, k_pe, slots, ptr_t, sc_t, gamma, pos, table, err):
