@@ -236,10 +236,15 @@ __global__ void __launch_bounds__(kThreads) pack_gather_kernel(const PackArgs a,
       (int64_t)(gridDim.x - gather_ctas) * kWarps);
 }
 
-// Share of the CTAs that gather when the grid is capped: the gather moves far
-// fewer bytes but its rows are a chain of dependent loads, so it gets about
-// twice its share of the bytes.
-constexpr int kGatherShareDiv = 6;
+// The split of a capped grid: the gather moves far fewer bytes but its rows
+// are a chain of dependent loads, so it needs at least a seventh of the CTAs
+// (an eighth made it the longer half: 22.3 against 21.0 us per chunk); the
+// pack takes the rest, cut to the fewest warps that keep its items per warp
+// (so its last round of items is full), the gather the CTAs that frees:
+// 32768 items of an 8192-token chunk on 608 CTAs give 512 pack CTAs of 8
+// items per warp and 96 gather CTAs (21.12 -> 20.86 us per chunk against a
+// sixth of the grid, whose 507 pack CTAs left a last round 8% full).
+constexpr int kGatherMinShareDiv = 7;
 
 cudaLaunchConfig_t base_cfg(const LaunchCfg& cfg, cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t lc = {};
@@ -281,7 +286,12 @@ cudaError_t launch_pack_gather_t(const PackArgs& a, const GatherArgs& g, int gmo
     gctas = (int)gather_ctas;
   } else {
     grid = resident;
-    gctas = (int)std::min<int64_t>(gather_ctas, std::max(1, resident / kGatherShareDiv));
+    const int gmin = std::max(1, resident / kGatherMinShareDiv);
+    const int64_t pmax = (int64_t)(resident - gmin) * kWarps;  // most pack warps
+    const int64_t rounds = (items + pmax - 1) / pmax;           // items per pack warp
+    const int64_t pwarps = (items + rounds - 1) / rounds;       // fewest warps for that
+    const int pctas = (int)((pwarps + kWarps - 1) / kWarps);
+    gctas = (int)std::min<int64_t>(gather_ctas, resident - pctas);
     if (pack_ctas < grid - gctas) grid = gctas + (int)pack_ctas;
   }
   cudaLaunchAttribute attr[1];
